@@ -1,0 +1,243 @@
+/*
+ * dsa.h -- C ABI of libdsa: the DeepSeek sparse-attention (DSA) hot path on
+ * one GB300 (sm_103a).
+ *
+ * The path has three stages, as the DeepSeek-V3.2-Exp atlas page states them
+ * (MoE transformer block, "All 43 steps"):
+ *
+ *   1. the lightning indexer
+ *        S^I_{t,s} = 1/(sqrt(H_I) sqrt(D_I)) sum_h w_{t,h} ReLU(q^I_{h,t} . k^I_s)
+ *      plus the causal mask M (S~^I = S^I + M),
+ *   2. the top-k selection M^sel (top_2048 of S~^I_t per query), and
+ *   3. multi-head latent attention over the selected keys, computed in the
+ *      absorbed form: q~_h = q^C_h W_UK,h scores against the shared latent
+ *      row [c^KV | k^R] (d_c + d_r values per key), an online softmax runs
+ *      over the selected keys, and W_UV maps the latent context back to the
+ *      per-head values (the output before the output projection wo).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers unless the comment says "host".  The
+ *     caller owns every buffer.  The library never allocates device or host
+ *     memory and never synchronises the stream; scratch memory comes from a
+ *     caller buffer whose size the matching *_workspace_size call returns.
+ *   - Every launch goes on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Every call returns a dsa_status.  Arguments are validated on the host
+ *     before anything is launched; an invalid call launches nothing.
+ *     Nothing aborts the process.
+ *   - A batch is a set of sequences (dsa_seqs).  Query rows of all sequences
+ *     are stacked: rows cu_q[b] .. cu_q[b+1]-1 belong to sequence b, and
+ *     query t of sequence b sits at absolute position p = start_pos[b] + t.
+ *     Keys of sequence b are rows cu_k[b] .. cu_k[b+1]-1 of the key caches
+ *     and are numbered 0 .. S_b-1 within the sequence (S_b = cu_k[b+1]-cu_k[b]).
+ *     Causality: key s is visible to the query at position p iff s <= p.
+ *     Every sequence must satisfy start_pos[b] + T_b <= S_b.
+ *   - Element types: DSA_F32 (fp32), DSA_BF16 (bf16), DSA_E4M3 (FP8 e4m3 codes,
+ *     one byte each, with fp32 power-of-two block scales).
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dsa_status {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,  /* null pointer, bad size / stride / alignment, inconsistent sequences */
+    DSA_ERR_UNSUPPORTED = 2,  /* a dtype / shape combination no kernel handles */
+    DSA_ERR_CUDA = 3,         /* a CUDA call or launch failed: dsa_last_cuda_error() gives the code */
+    DSA_ERR_TIMEOUT = 4,      /* a device-side wait gave up (reported by dsa_check_device_error) */
+    DSA_ERR_WORKSPACE = 5     /* workspace pointer NULL, misaligned (256 B) or smaller than required */
+} dsa_status;
+
+typedef enum dsa_dtype {
+    DSA_F32 = 0,
+    DSA_BF16 = 1,
+    DSA_E4M3 = 2
+} dsa_dtype;
+
+/* Largest number of sequences in one call. */
+#define DSA_MAX_SEQS 512
+
+/* A batch of sequences.  All three arrays are HOST memory, read during the
+ * call only (the library copies what the kernels need into their launch
+ * parameters, so the arrays may be freed when the call returns). */
+typedef struct dsa_seqs {
+    int32_t B;                 /* number of sequences, 1 .. DSA_MAX_SEQS */
+    const int32_t *cu_q;       /* host [B+1]: cumulative query rows, cu_q[0] = 0 */
+    const int32_t *cu_k;       /* host [B+1]: cumulative keys in the caches, cu_k[0] = 0 */
+    const int32_t *start_pos;  /* host [B]: absolute position of each sequence's first query */
+} dsa_seqs;
+
+/* ------------------------------------------------------------------------
+ * FP8 quantisation of indexer inputs.
+ * Source: config_671B_v3.2.json excerpt on the "DeepSeek-V3.2-Exp - Block
+ * input" atlas page (dtype fp8, scale_fmt ue8m0).  The block recipe is a
+ * reading of that: a block is 128 consecutive values; its scale is 2^e with
+ * e the smallest integer such that amax <= 448 * 2^e, clamped to [-127, 127]
+ * (amax = 0 gives e = 0); codes are x / 2^e rounded to nearest-even e4m3,
+ * saturating at +-448.
+ *
+ *   x        [n_blocks * 128] values of x_dtype (DSA_F32 or DSA_BF16)
+ *   codes    out [n_blocks * 128] e4m3 codes (4-byte aligned)
+ *   scales   out [n_blocks] fp32 scales 2^e
+ * Inf and NaN inputs are not supported.
+ * Errors: DSA_ERR_INVALID_ARG (null pointer, n_blocks < 0, misaligned codes),
+ * DSA_ERR_UNSUPPORTED (x_dtype not F32/BF16), DSA_ERR_CUDA.  n_blocks = 0
+ * launches nothing.
+ * ---------------------------------------------------------------------- */
+int dsa_quant_e4m3_ue8m0(const void *x, int x_dtype, int64_t n_blocks, uint8_t *codes, float *scales,
+                         void *stream);
+
+/* ------------------------------------------------------------------------
+ * Lightning-indexer scores with the causal mask.
+ * Source: DeepSeek-V3.2-Exp atlas page, MoE transformer block, equations
+ * S^I_{t,s} and S~^I = S^I + M; the indexer's 64 heads x 128 (nnterp
+ * deepseek_v32 page, "Up to 2048 tokens ..." note and printout).
+ *
+ *   q_idx    [sum T, H_I, D_I] of idx_dtype (F32, BF16, or E4M3 codes)
+ *   q_scale  [sum T, H_I] fp32 block scales of q_idx (E4M3 only, else NULL)
+ *   k_idx    [sum S, D_I] of idx_dtype
+ *   k_scale  [sum S] fp32 block scales of k_idx (E4M3 only, else NULL)
+ *   w        [sum T, H_I] fp32 per-head weights
+ *   scores   out [sum T, ld_scores] fp32.  Row r (query t of sequence b at
+ *            position p) receives columns 0 .. S_b-1: the score for s <= p
+ *            and -inf for p < s < S_b.  Columns >= S_b are not written.
+ *   ld_scores >= max_b S_b, a multiple of 4 (16-byte rows); scores 16-byte aligned.
+ * With E4M3 the factorisation sum_h w s_q ReLU(s_k cq.ck) = s_k sum_h (w s_q)
+ * ReLU(cq.ck) holds exactly for positive power-of-two scales, so D_I must be
+ * 128 (one block per head row).
+ * Errors: DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED (H_I > 128 or D_I > 256,
+ * E4M3 with D_I != 128), DSA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+int dsa_indexer_scores(const void *q_idx, const float *q_scale, const void *k_idx, const float *k_scale,
+                       int idx_dtype, const float *w, int H_I, int D_I, const dsa_seqs *seqs,
+                       float *scores, int64_t ld_scores, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Top-k selection per query row.
+ * Source: DeepSeek-V3.2-Exp atlas page, M^sel_{t,s} = M_{t,s} if
+ * s in top_k(S~^I_t); the selection tensor is int32 key indices
+ * [batch, query, min(index_topk, seq)] (nnterp deepseek_v32 page).
+ *
+ *   scores   [sum T, ld_scores] fp32 as written by dsa_indexer_scores; only
+ *            columns 0 .. p of row r are read (the causal keys).
+ *   k        1 .. 16384
+ *   idx      out [sum T, k] int32: the n = min(k, p + 1) causal keys with the
+ *            largest scores, then -1 padding.  The exact top-n set is returned;
+ *            among keys whose score equals the n-th largest the lower key
+ *            indices win.  Order within the row: keys above the threshold
+ *            in increasing key order, then the tied keys in increasing order.
+ *            NaN scores are not supported.
+ * Errors: DSA_ERR_INVALID_ARG, DSA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+int dsa_topk_select(const float *scores, int64_t ld_scores, const dsa_seqs *seqs, int k, int32_t *idx,
+                    void *stream);
+
+/* ------------------------------------------------------------------------
+ * Sparse multi-head latent attention over selected keys (absorbed form).
+ * Source: DeepSeek-V3.2-Exp atlas page (q^C, k^C = c^KV W_UK, K_i =
+ * [K^C_i; k^R], v = c^KV W_UV, M^sel); nnterp deepseek_v32 page (unselected
+ * keys masked before the softmax; one rotary key shared by all heads);
+ * "DeepSeek-V3.2-Exp - Attention input" page (softmax scale).
+ *
+ *   q_nope   [sum T, H, d_n]  (dtype)
+ *   q_pe     [sum T, H, d_r]  (dtype)
+ *   kv_cache latent rows c^KV: row j at kv_cache + j * ld_kv, d_c values (dtype)
+ *   k_pe     rotary keys: row j at k_pe + j * ld_pe, d_r values (dtype).  A packed
+ *            [sum S, d_c + d_r] cache is k_pe = kv_cache + d_c, ld_pe = ld_kv.
+ *   W_UK     [H, d_n, d_c] (dtype): K^C[s,h,d] = sum_c W_UK[h,d,c] c[s,c]
+ *   W_UV     [H, d_c, d_v] (dtype): V[s,h,e] = sum_c c[s,c] W_UV[h,c,e]
+ *   idx      [sum T, k] int32 key indices local to the row's sequence.  Entries
+ *            outside 0 .. min(p, S_b-1) (e.g. the -1 padding) are masked.
+ *            Each listed index counts once per occurrence.
+ *   softmax_scale  multiplies q.k before the softmax (1/sqrt(d_n + d_r), or the
+ *            YaRN-scaled 0.1352 of the released model)
+ *   out      out [sum T, H, d_v] (dtype)
+ *   lse      out [sum T, H] fp32 natural-log log-sum-exp of the scaled logits,
+ *            may be NULL; a row with no live key gets out = 0, lse = -inf.
+ *   workspace / ws_bytes  caller scratch, >= dsa_sparse_mla_workspace_size(),
+ *            256-byte aligned.
+ * Strides are in elements and must keep rows 16-byte aligned.
+ * Errors: DSA_ERR_INVALID_ARG, DSA_ERR_WORKSPACE, DSA_ERR_UNSUPPORTED
+ * (dtype E4M3, or dims beyond H <= 256, d_n <= 256, d_r <= 128, d_c <= 1024,
+ * d_v <= 256), DSA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+size_t dsa_sparse_mla_workspace_size(int dtype, int H, int d_n, int d_r, int d_c, int d_v, int k,
+                                     const dsa_seqs *seqs);
+int dsa_sparse_mla_fwd(const void *q_nope, const void *q_pe, int dtype, const void *kv_cache, int64_t ld_kv,
+                       const void *k_pe, int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n,
+                       int d_r, int d_c, int d_v, const int32_t *idx, int k, const dsa_seqs *seqs,
+                       float softmax_scale, void *out, float *lse, void *workspace, size_t ws_bytes,
+                       void *stream);
+
+/* ------------------------------------------------------------------------
+ * The whole path: [quantise] -> indexer -> top-k -> sparse latent attention.
+ * Sources: as for the three stages above.  Rows are processed in chunks so
+ * that the fp32 score buffer stays bounded; the workspace size covers one
+ * chunk of scores, the selection (unless idx_out is given), the FP8 copies
+ * of q^I / k^I (idx_fp8) and the attention scratch.
+ * ---------------------------------------------------------------------- */
+typedef struct dsa_problem {
+    /* shapes */
+    int32_t H_I, D_I, top_k;          /* indexer heads, head dim, k */
+    int32_t H, d_n, d_r, d_c, d_v;    /* MLA heads and widths */
+    int32_t dtype;                    /* DSA_F32 or DSA_BF16: storage type of every tensor below but w */
+    int32_t idx_fp8;                  /* 1: quantise q^I, k^I to e4m3 + ue8m0 before the indexer */
+    float softmax_scale;
+    /* indexer inputs */
+    const void *q_idx;                /* [sum T, H_I, D_I] */
+    const void *k_idx;                /* [sum S, D_I] */
+    const float *w;                   /* [sum T, H_I] fp32 */
+    /* attention inputs (layouts as in dsa_sparse_mla_fwd) */
+    const void *q_nope, *q_pe;
+    const void *kv_cache;
+    int64_t ld_kv;
+    const void *k_pe;
+    int64_t ld_pe;
+    const void *W_UK, *W_UV;
+    /* outputs */
+    void *out;                        /* [sum T, H, d_v] (dtype) */
+    float *lse;                       /* [sum T, H] or NULL */
+    int32_t *idx_out;                 /* [sum T, top_k] or NULL (then kept in the workspace) */
+} dsa_problem;
+
+size_t dsa_forward_workspace_size(const dsa_problem *p, const dsa_seqs *seqs);
+int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Status and diagnostics.
+ * ---------------------------------------------------------------------- */
+/* Human-readable name of a dsa_status. */
+const char *dsa_status_string(int status);
+/* The cudaError_t behind the most recent DSA_ERR_CUDA on this host thread. */
+int dsa_last_cuda_error(void);
+/* Waits for `stream`, then reads and clears the device error word that the
+ * kernels' bounded waits set.  Returns DSA_OK, DSA_ERR_TIMEOUT (and stores
+ * the recorded site in *site when non-NULL), or DSA_ERR_CUDA.  This is the
+ * only entry point that synchronises. */
+int dsa_check_device_error(void *stream, int *site);
+/* Bit mask of the kernels the last entry point launched on this host thread
+ * (DSA_KERNEL_* bits), and how many kernel launches it made. */
+uint32_t dsa_last_kernels(void);
+int dsa_last_launch_count(void);
+
+#define DSA_KERNEL_QUANT        (1u << 0)
+#define DSA_KERNEL_INDEXER_SIMT (1u << 1)
+#define DSA_KERNEL_INDEXER_TC   (1u << 2)
+#define DSA_KERNEL_INDEXER_FP8  (1u << 3)
+#define DSA_KERNEL_TOPK         (1u << 4)
+#define DSA_KERNEL_ABSORB_SIMT  (1u << 5)
+#define DSA_KERNEL_ABSORB_TC    (1u << 6)
+#define DSA_KERNEL_MLA_SIMT     (1u << 7)
+#define DSA_KERNEL_MLA_TC       (1u << 8)
+#define DSA_KERNEL_COMBINE      (1u << 9)
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H */

@@ -1,0 +1,358 @@
+// The C ABI of libdsa: argument validation, workspace carving, the row-chunk
+// loop of the whole path and the dispatch between the tensor-core kernels and
+// the generic ones.  Host code only; every arithmetic step runs in the kernels.
+#include <string.h>
+
+#include <algorithm>
+
+#include "dsa_common.cuh"
+
+namespace dsa {
+namespace {
+
+thread_local int g_last_cuda = 0;
+thread_local uint32_t g_kernels = 0;
+thread_local int g_launches = 0;
+
+void reset_trace() {
+    g_kernels = 0;
+    g_launches = 0;
+}
+
+int fail_cuda(cudaError_t e) {
+    g_last_cuda = (int)e;
+    return DSA_ERR_CUDA;
+}
+
+constexpr size_t WS_ALIGN = 256;
+inline size_t align_up(size_t x, size_t a = WS_ALIGN) { return (x + a - 1) / a * a; }
+inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// A validated batch: the kernel table for all rows plus summary sizes.
+struct Batch {
+    SeqTab st;
+    int total_q = 0;
+    int64_t total_k = 0;
+    int max_S = 0;
+};
+
+int build_batch(const dsa_seqs *s, Batch &b) {
+    if (!s || s->B < 1 || s->B > DSA_MAX_SEQS || !s->cu_q || !s->cu_k || !s->start_pos) return DSA_ERR_INVALID_ARG;
+    if (s->cu_q[0] != 0 || s->cu_k[0] != 0) return DSA_ERR_INVALID_ARG;
+    memset(&b.st, 0, sizeof(b.st));
+    b.st.B = s->B;
+    b.max_S = 0;
+    for (int i = 0; i < s->B; ++i) {
+        const int64_t T = (int64_t)s->cu_q[i + 1] - s->cu_q[i];
+        const int64_t S = (int64_t)s->cu_k[i + 1] - s->cu_k[i];
+        const int64_t p0 = s->start_pos[i];
+        if (T < 0 || S < 0 || p0 < 0 || p0 + T > S) return DSA_ERR_INVALID_ARG;
+        b.st.q_off[i] = s->cu_q[i];
+        b.st.k_base[i] = s->cu_k[i];
+        b.st.k_len[i] = (int)S;
+        b.st.start_pos[i] = (int)p0;
+        b.max_S = std::max<int>(b.max_S, (int)S);
+    }
+    b.st.q_off[s->B] = s->cu_q[s->B];
+    b.total_q = s->cu_q[s->B];
+    b.total_k = s->cu_k[s->B];
+    return DSA_OK;
+}
+
+// The table of rows [r0, r1) of a validated batch: each sequence that overlaps
+// the range contributes its overlapping rows, with start_pos advanced to the
+// first of them.  Row r of the range is row r - r0 of the table.
+void sub_batch(const dsa_seqs *s, int r0, int r1, SeqTab &st, int &max_S) {
+    st.B = 0;
+    st.q_off[0] = 0;
+    max_S = 0;
+    for (int b = 0; b < s->B; ++b) {
+        const int lo = std::max(s->cu_q[b], r0), hi = std::min(s->cu_q[b + 1], r1);
+        if (lo >= hi) continue;
+        const int i = st.B++;
+        st.q_off[i + 1] = st.q_off[i] + (hi - lo);
+        st.k_base[i] = s->cu_k[b];
+        st.k_len[i] = s->cu_k[b + 1] - s->cu_k[b];
+        st.start_pos[i] = s->start_pos[b] + (lo - s->cu_q[b]);
+        max_S = std::max(max_S, st.k_len[i]);
+    }
+}
+
+bool valid_dtype(int t) { return t == DSA_F32 || t == DSA_BF16 || t == DSA_E4M3; }
+size_t dtype_bytes(int t) { return t == DSA_F32 ? 4 : (t == DSA_BF16 ? 2 : 1); }
+
+int check_indexer_shape(int idx_dtype, int H_I, int D_I) {
+    if (!valid_dtype(idx_dtype) || H_I < 1 || D_I < 1) return DSA_ERR_INVALID_ARG;
+    if (H_I > 128 || D_I > 256) return DSA_ERR_UNSUPPORTED;
+    if (idx_dtype == DSA_E4M3 && D_I != 128) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+int check_mla_shape(int dtype, int H, int d_n, int d_r, int d_c, int d_v, int k) {
+    if (H < 1 || d_n < 1 || d_r < 0 || d_c < 1 || d_v < 1 || k < 1) return DSA_ERR_INVALID_ARG;
+    if (dtype != DSA_F32 && dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
+    if (H > 256 || d_n > 256 || d_r > 128 || d_c > 1024 || d_v > 256) return DSA_ERR_UNSUPPORTED;
+    // rows of the latent cache must stay 16-byte aligned for vector loads
+    if ((d_c * dtype_bytes(dtype)) % 16 != 0) return DSA_ERR_UNSUPPORTED;
+    return DSA_OK;
+}
+
+}  // namespace
+
+void note_launch(uint32_t kernel_bit) {
+    g_kernels |= kernel_bit;
+    ++g_launches;
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+namespace dsa {
+namespace {
+
+// Scratch of the attention stage: q~ = q_nope W_UK and the latent context,
+// both fp32 [M, H, d_c] on the generic path.
+struct MlaWs {
+    size_t qt = 0, olat = 0, total = 0;
+};
+
+MlaWs mla_ws_layout(int H, int d_c, int64_t total_q) {
+    MlaWs w;
+    const size_t per = align_up((size_t)total_q * H * d_c * sizeof(float));
+    w.qt = 0;
+    w.olat = per;
+    w.total = 2 * per;
+    return w;
+}
+
+int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int64_t ld_kv, const void *k_pe,
+            int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n, int d_r, int d_c, int d_v,
+            const int32_t *idx, int k, const Batch &bt, float scale, void *out, float *lse, char *ws,
+            cudaStream_t s) {
+    const MlaWs L = mla_ws_layout(H, d_c, bt.total_q);
+    float *qt = (float *)(ws + L.qt);
+    float *olat = (float *)(ws + L.olat);
+    const int M = bt.total_q;
+    cudaError_t e;
+    // q~[m,h,:] = q_nope[m,h,:] . W_UK[h]    (K = d_n, N = d_c)
+    e = launch_absorb_simt(q_nope, dtype, (int64_t)H * d_n, W_UK, dtype, qt, DSA_F32, (int64_t)H * d_c, M, H, d_n,
+                           d_c, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = launch_mla_simt(qt, DSA_F32, q_pe, dtype, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, M, H, d_r, d_c, scale, olat,
+                        lse, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    // out[m,h,:] = o_lat[m,h,:] . W_UV[h]    (K = d_c, N = d_v)
+    e = launch_absorb_simt(olat, DSA_F32, (int64_t)H * d_c, W_UV, dtype, out, dtype, (int64_t)H * d_v, M, H, d_c,
+                           d_v, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return DSA_OK;
+}
+
+int run_indexer(const void *q, const float *q_scale, const void *k, const float *k_scale, int idx_dtype,
+                const float *w, int H_I, int D_I, const SeqTab &st, int rows, int max_S, float *scores, int64_t ld,
+                cudaStream_t s) {
+    cudaError_t e = launch_indexer_simt(q, q_scale, k, k_scale, idx_dtype, w, H_I, D_I, st, rows, max_S, scores, ld, s);
+    return e == cudaSuccess ? DSA_OK : fail_cuda(e);
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" {
+
+const char *dsa_status_string(int status) {
+    switch (status) {
+        case DSA_OK: return "DSA_OK";
+        case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+        case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+        case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+        case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+        case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+        default: return "DSA_ERR_UNKNOWN";
+    }
+}
+
+int dsa_last_cuda_error(void) { return g_last_cuda; }
+uint32_t dsa_last_kernels(void) { return g_kernels; }
+int dsa_last_launch_count(void) { return g_launches; }
+
+int dsa_check_device_error(void *stream, int *site) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (site) *site = 0;
+    return DSA_OK;
+}
+
+int dsa_quant_e4m3_ue8m0(const void *x, int x_dtype, int64_t n_blocks, uint8_t *codes, float *scales, void *stream) {
+    reset_trace();
+    if (n_blocks < 0) return DSA_ERR_INVALID_ARG;
+    if (n_blocks > 0 && (!x || !codes || !scales)) return DSA_ERR_INVALID_ARG;
+    if (x_dtype != DSA_F32 && x_dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
+    if (!aligned(codes, 4)) return DSA_ERR_INVALID_ARG;
+    cudaError_t e = launch_quant_e4m3(x, x_dtype, n_blocks, codes, scales, (cudaStream_t)stream);
+    return e == cudaSuccess ? DSA_OK : fail_cuda(e);
+}
+
+int dsa_indexer_scores(const void *q_idx, const float *q_scale, const void *k_idx, const float *k_scale, int idx_dtype,
+                       const float *w, int H_I, int D_I, const dsa_seqs *seqs, float *scores, int64_t ld_scores,
+                       void *stream) {
+    reset_trace();
+    Batch bt;
+    int rc = build_batch(seqs, bt);
+    if (rc) return rc;
+    if ((rc = check_indexer_shape(idx_dtype, H_I, D_I))) return rc;
+    if (ld_scores < bt.max_S || ld_scores % 4 != 0) return DSA_ERR_INVALID_ARG;
+    if (bt.total_q > 0 && (!q_idx || !k_idx || !w || !scores)) return DSA_ERR_INVALID_ARG;
+    if (idx_dtype == DSA_E4M3 && bt.total_q > 0 && (!q_scale || !k_scale)) return DSA_ERR_INVALID_ARG;
+    if (!aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
+    return run_indexer(q_idx, idx_dtype == DSA_E4M3 ? q_scale : nullptr, k_idx,
+                       idx_dtype == DSA_E4M3 ? k_scale : nullptr, idx_dtype, w, H_I, D_I, bt.st, bt.total_q, bt.max_S,
+                       scores, ld_scores, (cudaStream_t)stream);
+}
+
+int dsa_topk_select(const float *scores, int64_t ld_scores, const dsa_seqs *seqs, int k, int32_t *idx, void *stream) {
+    reset_trace();
+    Batch bt;
+    int rc = build_batch(seqs, bt);
+    if (rc) return rc;
+    if (k < 1 || k > 16384 || ld_scores < bt.max_S) return DSA_ERR_INVALID_ARG;
+    if (bt.total_q > 0 && (!scores || !idx)) return DSA_ERR_INVALID_ARG;
+    cudaError_t e = launch_topk(scores, ld_scores, bt.st, bt.total_q, k, idx, (cudaStream_t)stream);
+    return e == cudaSuccess ? DSA_OK : fail_cuda(e);
+}
+
+size_t dsa_sparse_mla_workspace_size(int dtype, int H, int d_n, int d_r, int d_c, int d_v, int k,
+                                     const dsa_seqs *seqs) {
+    (void)dtype; (void)d_n; (void)d_r; (void)d_v; (void)k;
+    Batch bt;
+    if (build_batch(seqs, bt) || H < 1 || d_c < 1) return 0;
+    return mla_ws_layout(H, d_c, bt.total_q).total;
+}
+
+int dsa_sparse_mla_fwd(const void *q_nope, const void *q_pe, int dtype, const void *kv_cache, int64_t ld_kv,
+                       const void *k_pe, int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n, int d_r,
+                       int d_c, int d_v, const int32_t *idx, int k, const dsa_seqs *seqs, float softmax_scale,
+                       void *out, float *lse, void *workspace, size_t ws_bytes, void *stream) {
+    reset_trace();
+    Batch bt;
+    int rc = build_batch(seqs, bt);
+    if (rc) return rc;
+    if ((rc = check_mla_shape(dtype, H, d_n, d_r, d_c, d_v, k))) return rc;
+    if (ld_kv < d_c || ld_pe < d_r) return DSA_ERR_INVALID_ARG;
+    if (bt.total_q == 0) return DSA_OK;
+    if (!q_nope || (d_r > 0 && (!q_pe || !k_pe)) || !kv_cache || !W_UK || !W_UV || !idx || !out)
+        return DSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, WS_ALIGN)) return DSA_ERR_WORKSPACE;
+    if (ws_bytes < mla_ws_layout(H, d_c, bt.total_q).total) return DSA_ERR_WORKSPACE;
+    return run_mla(q_nope, q_pe, dtype, kv_cache, ld_kv, k_pe, ld_pe, W_UK, W_UV, H, d_n, d_r, d_c, d_v, idx, k, bt,
+                   softmax_scale, out, lse, (char *)workspace, (cudaStream_t)stream);
+}
+
+}  // extern "C"
+
+namespace dsa {
+namespace {
+
+// Bound on the fp32 score buffer of one chunk of query rows.
+constexpr size_t SCORE_CHUNK_BYTES = size_t(256) << 20;
+
+struct FwdWs {
+    int64_t ld = 0;
+    int rows_per_chunk = 0;
+    size_t qcodes = 0, qscale = 0, kcodes = 0, kscale = 0, idx = 0, scores = 0, mla = 0, total = 0;
+};
+
+int check_problem(const dsa_problem *p) {
+    if (!p) return DSA_ERR_INVALID_ARG;
+    if (p->dtype != DSA_F32 && p->dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
+    int rc = check_indexer_shape(p->idx_fp8 ? DSA_E4M3 : p->dtype, p->H_I, p->D_I);
+    if (rc) return rc;
+    rc = check_mla_shape(p->dtype, p->H, p->d_n, p->d_r, p->d_c, p->d_v, p->top_k);
+    if (rc) return rc;
+    if (p->top_k > 16384) return DSA_ERR_INVALID_ARG;
+    if (p->ld_kv < p->d_c || p->ld_pe < p->d_r) return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+}
+
+FwdWs fwd_ws_layout(const dsa_problem *p, const Batch &bt) {
+    FwdWs w;
+    w.ld = ((int64_t)std::max(bt.max_S, 1) + 3) / 4 * 4;
+    const int64_t per_row = w.ld * (int64_t)sizeof(float);
+    w.rows_per_chunk = (int)std::max<int64_t>(1, std::min<int64_t>(bt.total_q, SCORE_CHUNK_BYTES / per_row));
+    size_t off = 0;
+    if (p->idx_fp8) {
+        w.qcodes = off; off += align_up((size_t)bt.total_q * p->H_I * p->D_I);
+        w.qscale = off; off += align_up((size_t)bt.total_q * p->H_I * sizeof(float));
+        w.kcodes = off; off += align_up((size_t)bt.total_k * p->D_I);
+        w.kscale = off; off += align_up((size_t)bt.total_k * sizeof(float));
+    }
+    if (!p->idx_out) {
+        w.idx = off; off += align_up((size_t)bt.total_q * p->top_k * sizeof(int32_t));
+    }
+    w.scores = off; off += align_up((size_t)w.rows_per_chunk * per_row);
+    w.mla = off; off += mla_ws_layout(p->H, p->d_c, bt.total_q).total;
+    w.total = off;
+    return w;
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" {
+
+size_t dsa_forward_workspace_size(const dsa_problem *p, const dsa_seqs *seqs) {
+    Batch bt;
+    if (check_problem(p) || build_batch(seqs, bt)) return 0;
+    return fwd_ws_layout(p, bt).total;
+}
+
+int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, size_t ws_bytes, void *stream) {
+    reset_trace();
+    int rc = check_problem(p);
+    if (rc) return rc;
+    Batch bt;
+    if ((rc = build_batch(seqs, bt))) return rc;
+    if (bt.total_q == 0) return DSA_OK;
+    if (!p->q_idx || !p->k_idx || !p->w || !p->q_nope || !p->kv_cache || !p->W_UK || !p->W_UV || !p->out ||
+        (p->d_r > 0 && (!p->q_pe || !p->k_pe)))
+        return DSA_ERR_INVALID_ARG;
+    const FwdWs L = fwd_ws_layout(p, bt);
+    if (!workspace || !aligned(workspace, WS_ALIGN) || ws_bytes < L.total) return DSA_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    char *ws = (char *)workspace;
+    cudaError_t e;
+
+    const void *q_idx = p->q_idx, *k_idx = p->k_idx;
+    const float *q_scale = nullptr, *k_scale = nullptr;
+    int idx_dtype = p->dtype;
+    if (p->idx_fp8) {
+        uint8_t *qc = (uint8_t *)(ws + L.qcodes), *kc = (uint8_t *)(ws + L.kcodes);
+        float *qs = (float *)(ws + L.qscale), *ks = (float *)(ws + L.kscale);
+        e = launch_quant_e4m3(p->q_idx, p->dtype, (int64_t)bt.total_q * p->H_I, qc, qs, s);
+        if (e != cudaSuccess) return fail_cuda(e);
+        e = launch_quant_e4m3(p->k_idx, p->dtype, bt.total_k, kc, ks, s);
+        if (e != cudaSuccess) return fail_cuda(e);
+        q_idx = qc; k_idx = kc; q_scale = qs; k_scale = ks;
+        idx_dtype = DSA_E4M3;
+    }
+    int32_t *idx = p->idx_out ? p->idx_out : (int32_t *)(ws + L.idx);
+    float *scores = (float *)(ws + L.scores);
+    const size_t qrow = dtype_bytes(idx_dtype) * p->H_I * p->D_I;
+    for (int r0 = 0; r0 < bt.total_q; r0 += L.rows_per_chunk) {
+        const int r1 = std::min(bt.total_q, r0 + L.rows_per_chunk);
+        SeqTab st;
+        int max_S = 0;
+        sub_batch(seqs, r0, r1, st, max_S);
+        rc = run_indexer((const char *)q_idx + qrow * r0, q_scale ? q_scale + (size_t)r0 * p->H_I : nullptr, k_idx,
+                         k_scale, idx_dtype, p->w + (size_t)r0 * p->H_I, p->H_I, p->D_I, st, r1 - r0, max_S, scores,
+                         L.ld, s);
+        if (rc) return rc;
+        e = launch_topk(scores, L.ld, st, r1 - r0, p->top_k, idx + (size_t)r0 * p->top_k, s);
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    return run_mla(p->q_nope, p->q_pe, p->dtype, p->kv_cache, p->ld_kv, p->k_pe, p->ld_pe, p->W_UK, p->W_UV, p->H,
+                   p->d_n, p->d_r, p->d_c, p->d_v, idx, p->top_k, bt, p->softmax_scale, p->out, p->lse, ws + L.mla, s);
+}
+
+}  // extern "C"

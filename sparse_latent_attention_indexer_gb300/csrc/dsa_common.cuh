@@ -1,0 +1,98 @@
+// Shared internals of libdsa: the per-launch sequence table, element loads,
+// launch bookkeeping and the declarations of every kernel launcher.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+// Sequence table passed BY VALUE in kernel parameters (about 6 KB), so the
+// library needs no device copy of the batch description.
+struct SeqTab {
+    int B;
+    int q_off[DSA_MAX_SEQS + 1];  // cumulative query rows of the launch
+    int k_base[DSA_MAX_SEQS];     // first cache row of each sequence
+    int k_len[DSA_MAX_SEQS];      // keys of each sequence
+    int start_pos[DSA_MAX_SEQS];  // position of each sequence's first row in this launch
+};
+
+// Largest b with q_off[b] <= r: the sequence that owns query row r (empty
+// sequences are skipped because their successor has the same offset).
+__device__ __forceinline__ int seq_of_row(const SeqTab &st, int r) {
+    int lo = 0, hi = st.B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (st.q_off[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Per-row facts every stage needs.
+struct RowInfo {
+    int b;      // sequence
+    int t;      // query index within the sequence
+    int p;      // absolute position
+    int S;      // keys of the sequence
+    int kbase;  // first cache row of the sequence
+};
+
+__device__ __forceinline__ RowInfo row_info(const SeqTab &st, int r) {
+    RowInfo ri;
+    ri.b = seq_of_row(st, r);
+    ri.t = r - st.q_off[ri.b];
+    ri.p = st.start_pos[ri.b] + ri.t;
+    ri.kbase = st.k_base[ri.b];
+    ri.S = st.k_len[ri.b];
+    return ri;
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Order-preserving map of an fp32 score to uint32 (larger float -> larger
+// key); -0 is folded onto +0 first so equal values get equal keys.
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+    f = f + 0.0f;
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// Host-side bookkeeping (dsa_api.cu)
+// ---------------------------------------------------------------------------
+void note_launch(uint32_t kernel_bit);
+
+// ---------------------------------------------------------------------------
+// Kernel launchers.  Each returns the cudaError_t of its launch.
+// ---------------------------------------------------------------------------
+cudaError_t launch_quant_e4m3(const void *x, int x_dtype, int64_t n_blocks, uint8_t *codes, float *scales,
+                              cudaStream_t s);
+
+// Generic SIMT indexer: any H_I <= 128, D_I <= 256; F32, BF16 or E4M3 inputs.
+cudaError_t launch_indexer_simt(const void *q, const float *q_scale, const void *k, const float *k_scale,
+                                int dtype, const float *w, int H_I, int D_I, const SeqTab &st, int total_q,
+                                int max_S, float *scores, int64_t ld, cudaStream_t s);
+
+cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int total_q, int k, int32_t *idx,
+                        cudaStream_t s);
+
+// Batched per-head GEMM C[m, h, :] = A[m, h, :] . B[h] (B row-major K x N).
+cudaError_t launch_absorb_simt(const void *A, int a_dtype, int64_t lda_row, const void *Bm, int b_dtype, void *C,
+                               int c_dtype, int64_t ldc_row, int M, int H, int K, int N, cudaStream_t s);
+
+// Generic SIMT sparse attention in the latent space: per (row, head) online
+// softmax over the selected keys.  qt [M, H, d_c] (qt_dtype), q_pe, cache.
+cudaError_t launch_mla_simt(const void *qt, int qt_dtype, const void *q_pe, int dtype, const void *kv,
+                            int64_t ld_kv, const void *k_pe, int64_t ld_pe, const int32_t *idx, int k,
+                            const SeqTab &st, int total_q, int H, int d_r, int d_c, float scale, float *olat,
+                            float *lse, cudaStream_t s);
+
+}  // namespace dsa
