@@ -205,8 +205,7 @@ def random_selection(wl: Workload, seed: int, density: float = 0.5) -> torch.Ten
     for b in range(wl.B):
         for p in wl.row_positions(b):
             n_causal = p + 1
-            n = min(k, max(1, int(round(n_causal * density))) if n_causal > k else n_causal)
-            n = min(n, k)
+            n = min(k, max(1, int(round(n_causal * density))))
             perm = torch.randperm(n_causal, generator=g)[:n].to(torch.int32)
             row = torch.full((k,), -1, dtype=torch.int32)
             slots = torch.randperm(k, generator=g)[:n]

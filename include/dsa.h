@@ -225,6 +225,17 @@ int dsa_check_device_error(void *stream, int *site);
 uint32_t dsa_last_kernels(void);
 int dsa_last_launch_count(void);
 
+/* Optional timing hook.  When `events` is non-NULL, dsa_forward records
+ * events[i] (cudaEvent_t handles created by the caller) on its stream at
+ * these stage boundaries:
+ *   0 start, 1 after FP8 quantisation, 2 after the indexer + top-k loop,
+ *   3 after q~ = q_nope W_UK, 4 after the sparse attention (and its
+ *   split-key combine), 5 after o_lat W_UV (the end).
+ * n_events must be DSA_STAGE_EVENTS.  Pass NULL to switch it off.  The setting
+ * is per host thread.  Returns DSA_ERR_INVALID_ARG for a wrong count. */
+#define DSA_STAGE_EVENTS 6
+int dsa_set_stage_events(void *const *events, int n_events);
+
 #define DSA_KERNEL_QUANT        (1u << 0)
 #define DSA_KERNEL_INDEXER_SIMT (1u << 1)
 #define DSA_KERNEL_INDEXER_TC   (1u << 2)

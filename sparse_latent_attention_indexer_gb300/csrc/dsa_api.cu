@@ -13,6 +13,13 @@ namespace {
 thread_local int g_last_cuda = 0;
 thread_local uint32_t g_kernels = 0;
 thread_local int g_launches = 0;
+thread_local cudaEvent_t g_stage_events[DSA_STAGE_EVENTS] = {};
+thread_local bool g_stage_on = false;
+
+// Records stage boundary i on `s` when the timing hook is on.
+void stage_mark(int i, cudaStream_t s) {
+    if (g_stage_on) cudaEventRecord(g_stage_events[i], s);
+}
 
 void reset_trace() {
     g_kernels = 0;
@@ -129,7 +136,7 @@ MlaWs mla_ws_layout(int H, int d_c, int64_t total_q) {
 int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int64_t ld_kv, const void *k_pe,
             int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n, int d_r, int d_c, int d_v,
             const int32_t *idx, int k, const Batch &bt, float scale, void *out, float *lse, char *ws,
-            cudaStream_t s) {
+            cudaStream_t s, bool mark = false) {
     const MlaWs L = mla_ws_layout(H, d_c, bt.total_q);
     float *qt = (float *)(ws + L.qt);
     float *olat = (float *)(ws + L.olat);
@@ -139,13 +146,16 @@ int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int
     e = launch_absorb_simt(q_nope, dtype, (int64_t)H * d_n, W_UK, dtype, qt, DSA_F32, (int64_t)H * d_c, M, H, d_n,
                            d_c, s);
     if (e != cudaSuccess) return fail_cuda(e);
+    if (mark) stage_mark(3, s);
     e = launch_mla_simt(qt, DSA_F32, q_pe, dtype, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, M, H, d_r, d_c, scale, olat,
                         lse, s);
     if (e != cudaSuccess) return fail_cuda(e);
+    if (mark) stage_mark(4, s);
     // out[m,h,:] = o_lat[m,h,:] . W_UV[h]    (K = d_c, N = d_v)
     e = launch_absorb_simt(olat, DSA_F32, (int64_t)H * d_c, W_UV, dtype, out, dtype, (int64_t)H * d_v, M, H, d_c,
                            d_v, s);
     if (e != cudaSuccess) return fail_cuda(e);
+    if (mark) stage_mark(5, s);
     return DSA_OK;
 }
 
@@ -174,6 +184,20 @@ const char *dsa_status_string(int status) {
 }
 
 int dsa_last_cuda_error(void) { return g_last_cuda; }
+
+int dsa_set_stage_events(void *const *events, int n_events) {
+    if (!events) {
+        g_stage_on = false;
+        return DSA_OK;
+    }
+    if (n_events != DSA_STAGE_EVENTS) return DSA_ERR_INVALID_ARG;
+    for (int i = 0; i < DSA_STAGE_EVENTS; ++i) {
+        if (!events[i]) return DSA_ERR_INVALID_ARG;
+        g_stage_events[i] = (cudaEvent_t)events[i];
+    }
+    g_stage_on = true;
+    return DSA_OK;
+}
 uint32_t dsa_last_kernels(void) { return g_kernels; }
 int dsa_last_launch_count(void) { return g_launches; }
 
@@ -322,6 +346,7 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
     cudaStream_t s = (cudaStream_t)stream;
     char *ws = (char *)workspace;
     cudaError_t e;
+    stage_mark(0, s);
 
     const void *q_idx = p->q_idx, *k_idx = p->k_idx;
     const float *q_scale = nullptr, *k_scale = nullptr;
@@ -336,6 +361,7 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
         q_idx = qc; k_idx = kc; q_scale = qs; k_scale = ks;
         idx_dtype = DSA_E4M3;
     }
+    stage_mark(1, s);
     int32_t *idx = p->idx_out ? p->idx_out : (int32_t *)(ws + L.idx);
     float *scores = (float *)(ws + L.scores);
     const size_t qrow = dtype_bytes(idx_dtype) * p->H_I * p->D_I;
@@ -351,8 +377,10 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
         e = launch_topk(scores, L.ld, st, r1 - r0, p->top_k, idx + (size_t)r0 * p->top_k, s);
         if (e != cudaSuccess) return fail_cuda(e);
     }
+    stage_mark(2, s);
     return run_mla(p->q_nope, p->q_pe, p->dtype, p->kv_cache, p->ld_kv, p->k_pe, p->ld_pe, p->W_UK, p->W_UV, p->H,
-                   p->d_n, p->d_r, p->d_c, p->d_v, idx, p->top_k, bt, p->softmax_scale, p->out, p->lse, ws + L.mla, s);
+                   p->d_n, p->d_r, p->d_c, p->d_v, idx, p->top_k, bt, p->softmax_scale, p->out, p->lse, ws + L.mla, s,
+                   true);
 }
 
 }  // extern "C"

@@ -1,0 +1,142 @@
+"""Shared helpers of the parity tests: moving a workload to the device,
+running the oracle on a subset of rows, and the acceptance rules.
+
+Acceptance rules (the tolerances the path is held to):
+  * indexer scores: |gpu - ref| <= 1e-3 * max(|ref|, A) where A is the
+    absolute-term sum 1/sqrt(H_I D_I) sum_h |w| ReLU(q.k) (so the band does
+    not vanish when cancellation makes the score ~0); masked keys must be
+    exactly -inf;
+  * top-k: the GPU set equals the oracle set except for keys whose oracle
+    score lies within tau = 1e-3 * max(|S_n|, A_n) of the oracle's n-th
+    score S_n; the GPU row holds exactly n = min(k, p+1) distinct causal keys
+    followed by -1 padding;
+  * attention output: max |gpu - ref| <= 2e-2 (unit-scale bf16 data);
+    fp32 workloads are held to 1e-4.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import sparse_latent_attention_indexer_gb300 as dsa
+
+SCORE_RTOL = 1e-3
+OUT_ATOL_BF16 = 2e-2
+OUT_ATOL_F32 = 1e-4
+
+
+def seqs_of(wl) -> dsa.Seqs:
+    return dsa.Seqs(wl.cu_q, wl.cu_k, wl.start_pos)
+
+
+def to_device(wl, dev="cuda"):
+    t = {k: v.to(dev) for k, v in wl.tensors.items()}
+    d_c = wl.shape.d_c
+    t["ckv"] = t["kv_cache"][:, :d_c]
+    t["kpe"] = t["kv_cache"][:, d_c:]
+    return t
+
+
+def gpu_forward(wl, t, **kw):
+    sh = wl.shape
+    return dsa.dsa_forward(t["qI"], t["kI"], t["w"], t["q_nope"], t["q_pe"], t["ckv"], t["kpe"], t["W_UK"],
+                           t["W_UV"], seqs_of(wl), sh.k, sh.softmax_scale, idx_fp8=sh.idx_fp8, **kw)
+
+
+def f32np(x: torch.Tensor) -> np.ndarray:
+    return x.detach().float().cpu().numpy()
+
+
+def rows_by_sequence(wl, rows):
+    """Group global row ids by sequence: {b: [(row, t), ...]}."""
+    cu = wl.cu_q
+    out = {}
+    for r in rows:
+        b = int(np.searchsorted(cu, r, side="right") - 1)
+        while cu[b + 1] <= r:  # skip empty sequences
+            b += 1
+        out.setdefault(b, []).append((r, r - cu[b]))
+    return out
+
+
+def oracle_rows(wl, rows, with_attention=True):
+    """The oracle's view of the given global rows: per row the score row,
+    absolute-term row, selection, output and lse (absorbed form for the
+    attention: pinned equal to the unabsorbed form)."""
+    sh = wl.shape
+    T = wl.tensors
+    res = {}
+    for b, items in rows_by_sequence(wl, rows).items():
+        k0, k1 = wl.cu_k[b], wl.cu_k[b + 1]
+        q0 = wl.cu_q[b]
+        glob = [r for r, _ in items]
+        loc = [t for _, t in items]
+        pos = np.array([wl.start_pos[b] + t for t in loc], np.int64)
+        qI = f32np(T["qI"][glob])
+        kI = f32np(T["kI"][k0:k1])
+        if sh.idx_fp8:
+            qc, qe = oracle.quant_e4m3_ue8m0(qI.reshape(-1, 128))
+            qI = oracle.dequant_e4m3(qc, qe).reshape(qI.shape)
+            kc, ke = oracle.quant_e4m3_ue8m0(kI)
+            kI = oracle.dequant_e4m3(kc, ke).reshape(kI.shape)
+        w = f32np(T["w"][glob])
+        scores, absterm = oracle.indexer_scores(qI, w, kI, pos, with_absterm=True)
+        idx = oracle.topk(scores, pos, sh.k)
+        entry = dict(scores=scores, absterm=absterm, idx=idx, pos=pos, b=b)
+        if with_attention:
+            cache = f32np(T["kv_cache"][k0:k1])
+            out, lse = oracle.sparse_mla_absorbed(f32np(T["q_nope"][glob]), f32np(T["q_pe"][glob]),
+                                                  cache[:, :sh.d_c], cache[:, sh.d_c:], f32np(T["W_UK"]),
+                                                  f32np(T["W_UV"]), idx, pos, sh.softmax_scale)
+            entry["out"], entry["lse"] = out, lse
+        for i, r in enumerate(glob):
+            row = dict(scores=scores[i], absterm=absterm[i], idx=idx[i], pos=int(pos[i]), b=b)
+            if with_attention:
+                row["out"], row["lse"] = entry["out"][i], entry["lse"][i]
+            res[r] = row
+    return res
+
+
+def check_score_row(gpu_row, ref_row, abs_row, p, S):
+    """gpu_row: the first S columns of the GPU score row."""
+    gpu_row = np.asarray(gpu_row, np.float64)
+    causal = slice(0, p + 1)
+    fut = gpu_row[p + 1:S]
+    assert np.all(np.isneginf(fut)), "future keys must be -inf"
+    g, r, a = gpu_row[causal], ref_row[causal], abs_row[causal]
+    assert np.all(np.isfinite(g)), "causal scores must be finite"
+    band = SCORE_RTOL * np.maximum(np.abs(r), a)
+    err = np.abs(g - r)
+    bad = err > band
+    assert not bad.any(), f"{bad.sum()} scores out of tolerance; worst err {err.max():.3e} at {int(err.argmax())}"
+
+
+def check_selection_row(gpu_idx, ref_scores, ref_abs, p, k):
+    gpu_idx = np.asarray(gpu_idx)
+    n = min(k, p + 1)
+    live = gpu_idx[:n]
+    assert np.all(gpu_idx[n:] == -1), "padding must be -1"
+    assert np.all((live >= 0) & (live <= p)), "selected keys must be causal"
+    assert len(np.unique(live)) == n, "duplicate keys in the selection"
+    causal = ref_scores[:p + 1]
+    order = np.lexsort((np.arange(p + 1), -causal))
+    ref_set = set(order[:n].tolist())
+    gpu_set = set(live.tolist())
+    if ref_set == gpu_set:
+        return 0
+    s_n = causal[order[n - 1]]
+    tau = SCORE_RTOL * max(abs(s_n), ref_abs[order[n - 1]])
+    diff = ref_set ^ gpu_set
+    far = [s for s in diff if abs(causal[s] - s_n) > tau]
+    assert not far, f"selection differs outside the tie band: keys {far[:8]}"
+    return len(diff)
+
+
+def cpu_topk_same_buffer(score_row, p, k):
+    """The top-k of an fp32 buffer on the CPU: value descending, then key
+    ascending; -0.0 and +0.0 are equal."""
+    causal = np.asarray(score_row[:p + 1], np.float32).astype(np.float64) + 0.0
+    order = np.lexsort((np.arange(p + 1), -causal))
+    n = min(k, p + 1)
+    return order[:n]

@@ -1,0 +1,107 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function
+include/dsa.h declares, and validates arguments on the host (an invalid call
+returns an error status before any CUDA call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_latent_attention_indexer_gb300 as dsa
+from sparse_latent_attention_indexer_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(dsa_[a-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_function():
+    lib = _abi.load()
+    names = _declared_functions()
+    assert len(names) >= 12, names
+    for n in names:
+        assert hasattr(lib, n), f"libdsa.so does not export {n}"
+    assert sorted(n for n, _, _ in _abi.SIGNATURES) == names
+
+
+def test_status_strings():
+    lib = _abi.load()
+    assert lib.dsa_status_string(0) == b"DSA_OK"
+    assert lib.dsa_status_string(5) == b"DSA_ERR_WORKSPACE"
+
+
+def _seqs(T, S, P):
+    return dsa.Seqs.from_lengths(T, S, P)
+
+
+def test_invalid_sequences_rejected_before_launch():
+    lib = _abi.load()
+    bad = _seqs([4], [3], [0])         # start_pos + T > S
+    st = lib.dsa_topk_select(ctypes.c_void_p(16), 4, bad.ref(), 8, ctypes.c_void_p(16), None)
+    assert st == _abi.DSA_ERR_INVALID_ARG
+    good = _seqs([4], [8], [2])
+    assert lib.dsa_topk_select(ctypes.c_void_p(16), 8, good.ref(), 0, ctypes.c_void_p(16), None) == 1  # k = 0
+    assert lib.dsa_topk_select(ctypes.c_void_p(16), 4, good.ref(), 8, ctypes.c_void_p(16), None) == 1  # ld < S
+    none = _abi.dsa_seqs(0, None, None, None)
+    assert lib.dsa_topk_select(ctypes.c_void_p(16), 8, ctypes.byref(none), 8, ctypes.c_void_p(16), None) == 1
+
+
+def test_indexer_shape_checks():
+    lib = _abi.load()
+    s = _seqs([2], [4], [0])
+    P = ctypes.c_void_p(256)
+    # E4M3 needs D_I = 128 and scales
+    assert lib.dsa_indexer_scores(P, None, P, None, _abi.DSA_E4M3, P, 4, 64, s.ref(), P, 4, None) == 2
+    assert lib.dsa_indexer_scores(P, None, P, None, _abi.DSA_E4M3, P, 4, 128, s.ref(), P, 4, None) == 1
+    assert lib.dsa_indexer_scores(P, None, P, None, _abi.DSA_BF16, P, 256, 128, s.ref(), P, 4, None) == 2
+    assert lib.dsa_indexer_scores(P, None, P, None, _abi.DSA_BF16, P, 4, 32, s.ref(), P, 3, None) == 1  # ld % 4
+
+
+def _problem(**over):
+    p = _abi.dsa_problem()
+    p.H_I, p.D_I, p.top_k = 64, 128, 2048
+    p.H, p.d_n, p.d_r, p.d_c, p.d_v = 128, 128, 64, 512, 128
+    p.dtype, p.idx_fp8, p.softmax_scale = _abi.DSA_BF16, 0, 192 ** -0.5
+    for n in ("q_idx", "k_idx", "w", "q_nope", "q_pe", "kv_cache", "k_pe", "W_UK", "W_UV", "out"):
+        setattr(p, n, 4096)
+    p.ld_kv = p.ld_pe = 576
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_forward_workspace_size_is_host_logic():
+    lib = _abi.load()
+    s = _seqs([4096], [4096], [0])
+    p = _problem()
+    ws = lib.dsa_forward_workspace_size(ctypes.byref(p), s.ref())
+    assert ws > 0 and ws % 256 == 0
+    # the selection lives in the workspace unless the caller gives idx_out
+    p2 = _problem(idx_out=8192)
+    assert lib.dsa_forward_workspace_size(ctypes.byref(p2), s.ref()) == ws - 4096 * 2048 * 4
+    # FP8 indexer adds the quantised copies
+    p3 = _problem(idx_fp8=1)
+    assert lib.dsa_forward_workspace_size(ctypes.byref(p3), s.ref()) > ws
+    # unsupported dtype -> 0
+    assert lib.dsa_forward_workspace_size(ctypes.byref(_problem(dtype=_abi.DSA_E4M3)), s.ref()) == 0
+
+
+def test_forward_rejects_small_workspace():
+    lib = _abi.load()
+    s = _seqs([16], [16], [0])
+    p = _problem()
+    need = lib.dsa_forward_workspace_size(ctypes.byref(p), s.ref())
+    st = lib.dsa_forward(ctypes.byref(p), s.ref(), ctypes.c_void_p(1 << 20), need - 256, None)
+    assert st == _abi.DSA_ERR_WORKSPACE
+    st = lib.dsa_forward(ctypes.byref(p), s.ref(), ctypes.c_void_p((1 << 20) + 8), need, None)  # misaligned
+    assert st == _abi.DSA_ERR_WORKSPACE
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        _abi.load(str(tmp_path / "libdsa.so"))

@@ -1,0 +1,246 @@
+"""GPU parity of every stage against the oracle, at sizes the oracle finishes
+in seconds that still span several tiles and ragged tails, plus edge cases.
+All calls go through the C ABI (libdsa.so) via the thin binding."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import dsa_inputs as di
+import oracle
+import sparse_latent_attention_indexer_gb300 as dsa
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+FULL_K64 = di.Shape(k=64)
+CASES = {
+    # full head shapes, three sequences: ragged tile tails, start_pos > 0, rows above and below k
+    "bf16-ragged": lambda: di.generate("bf16-ragged", di.FULL, 11, [300, 1, 77], [300, 2100, 2200], [0, 2099, 2123]),
+    # small k so most rows select a strict subset
+    "bf16-k64": lambda: di.generate("bf16-k64", FULL_K64, 12, [333], [333], [0]),
+    # FP8 indexer on the ragged batch
+    "fp8-ragged": lambda: di.generate("fp8-ragged", di.Shape(idx_fp8=True), 13, [129, 65], [129, 2300], [0, 2235]),
+    # the tiny fp32 workload in full
+    "f32-tiny": lambda: di.workload(0),
+}
+_cache = {}
+
+
+def case(name):
+    if name not in _cache:
+        wl = CASES[name]()
+        _cache[name] = (wl, H.to_device(wl))
+    return _cache[name]
+
+
+def _oracle(name):
+    key = ("oracle", name)
+    if key not in _cache:
+        wl, _ = case(name)
+        _cache[key] = H.oracle_rows(wl, list(range(wl.total_q)))
+    return _cache[key]
+
+
+def out_atol(wl):
+    return H.OUT_ATOL_F32 if wl.shape.dtype == "f32" else H.OUT_ATOL_BF16
+
+
+# ---------------------------------------------------------------------------
+# quantiser: bit-exact codes and scales
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_quant_bit_exact(dtype):
+    g = torch.Generator().manual_seed(21)
+    x = torch.randn(300, 128, generator=g) * torch.exp2(torch.randint(-30, 30, (300, 1), generator=g).float())
+    x[0] = 0.0
+    x[1] = 0.0
+    x[1, 3] = 448.0
+    x[2] = 0.0
+    x[2, 100] = -448.5
+    x[3] = 0.0
+    x[3, 0] = 1e-38
+    x[4] = -0.0
+    x = x.to(dtype)
+    codes, scales = dsa.dsa_quant_e4m3_ue8m0(x.cuda())
+    rc, re = oracle.quant_e4m3_ue8m0(x.float().numpy())
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy(), np.ldexp(1.0, re).astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# indexer scores
+# ---------------------------------------------------------------------------
+def _gpu_scores(wl, t):
+    seqs = H.seqs_of(wl)
+    if wl.shape.idx_fp8:
+        qc, qs = dsa.dsa_quant_e4m3_ue8m0(t["qI"])
+        kc, ks = dsa.dsa_quant_e4m3_ue8m0(t["kI"])
+        return dsa.dsa_indexer_scores(qc, kc, t["w"], seqs, q_scale=qs, k_scale=ks)
+    return dsa.dsa_indexer_scores(t["qI"], t["kI"], t["w"], seqs)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_indexer_scores(name):
+    wl, t = case(name)
+    ref = _oracle(name)
+    scores = _gpu_scores(wl, t).cpu().numpy()
+    for r, o in ref.items():
+        S = wl.S[o["b"]]
+        H.check_score_row(scores[r, :S], o["scores"], o["absterm"], o["pos"], S)
+
+
+# ---------------------------------------------------------------------------
+# top-k: exact on the GPU's own buffer; tie band against the oracle
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", list(CASES))
+def test_topk(name):
+    wl, t = case(name)
+    ref = _oracle(name)
+    seqs = H.seqs_of(wl)
+    scores = _gpu_scores(wl, t)
+    idx = dsa.dsa_topk_select(scores, seqs, wl.shape.k).cpu().numpy()
+    sc = scores.cpu().numpy()
+    for r, o in ref.items():
+        p, k = o["pos"], wl.shape.k
+        n = min(k, p + 1)
+        want = H.cpu_topk_same_buffer(sc[r], p, k)
+        assert sorted(idx[r, :n].tolist()) == sorted(want.tolist()), f"row {r}"
+        assert np.all(idx[r, n:] == -1)
+        H.check_selection_row(idx[r], o["scores"], o["absterm"], p, k)
+
+
+@pytest.mark.parametrize("fill", [1.0, 0.0, -3.5])
+def test_topk_all_equal_scores(fill):
+    """Every score equal: the lowest key indices win."""
+    T = S = 700
+    k = 100
+    seqs = dsa.Seqs.from_lengths([T], [S], [0])
+    scores = torch.full((T, 700), fill, dtype=torch.float32, device="cuda")
+    if fill == 0.0:
+        scores[:, ::2] = -0.0  # -0 and +0 are the same score
+    idx = dsa.dsa_topk_select(scores, seqs, k).cpu().numpy()
+    for r in range(T):
+        n = min(k, r + 1)
+        assert sorted(idx[r, :n].tolist()) == list(range(n))
+        assert np.all(idx[r, n:] == -1)
+
+
+def test_topk_threshold_ties_and_large_rows():
+    """Scores on a coarse grid (many exact ties at the threshold), rows up to
+    65536 keys; exact equality with the CPU top-k of the same buffer."""
+    g = torch.Generator().manual_seed(5)
+    S = 65536
+    rows = 24
+    seqs = dsa.Seqs([0, rows], [0, S], [S - rows])
+    scores = torch.randint(-40, 40, (rows, S), generator=g).float() / 8
+    idx = dsa.dsa_topk_select(scores.cuda(), seqs, 2048).cpu().numpy()
+    sc = scores.numpy()
+    for r in range(rows):
+        p = S - rows + r
+        want = H.cpu_topk_same_buffer(sc[r], p, 2048)
+        assert sorted(idx[r].tolist()) == sorted(want.tolist())
+
+
+# ---------------------------------------------------------------------------
+# sparse attention on a seeded selection (same idx on both sides)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", list(CASES))
+def test_sparse_mla_given_selection(name):
+    wl, t = case(name)
+    sh = wl.shape
+    sel = di.random_selection(wl, seed=31, density=0.7)
+    out, lse = dsa.dsa_sparse_mla_fwd(t["q_nope"], t["q_pe"], t["ckv"], t["kpe"], t["W_UK"], t["W_UV"],
+                                      sel.cuda(), H.seqs_of(wl), sh.softmax_scale)
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    T = wl.tensors
+    for b in range(wl.B):
+        q0, q1, k0, k1 = wl.cu_q[b], wl.cu_q[b + 1], wl.cu_k[b], wl.cu_k[b + 1]
+        if q0 == q1:
+            continue
+        pos = np.arange(wl.start_pos[b], wl.start_pos[b] + wl.T[b])
+        cache = H.f32np(T["kv_cache"][k0:k1])
+        ro, rl = oracle.sparse_mla_absorbed(H.f32np(T["q_nope"][q0:q1]), H.f32np(T["q_pe"][q0:q1]),
+                                            cache[:, :sh.d_c], cache[:, sh.d_c:], H.f32np(T["W_UK"]),
+                                            H.f32np(T["W_UV"]), sel[q0:q1].numpy(), pos, sh.softmax_scale)
+        err = np.abs(out[q0:q1] - ro).max()
+        assert err <= out_atol(wl), f"seq {b}: max abs err {err:.3e}"
+        assert np.allclose(lse[q0:q1], rl, rtol=0, atol=5e-3 if sh.dtype == "bf16" else 1e-4)
+
+
+def test_sparse_mla_masked_rows_and_out_of_window_indices():
+    """A row whose selection holds only -1, future or out-of-range keys has
+    no live key: out = 0, lse = -inf.  Such entries inside a row are ignored."""
+    wl, t = case("bf16-k64")
+    sh = wl.shape
+    k = sh.k
+    sel = torch.full((wl.total_q, k), -1, dtype=torch.int32)
+    sel[5, :3] = torch.tensor([6, 7, 100000])     # row 5 (p = 5): all masked
+    sel[9, :4] = torch.tensor([2, 10, -7, 4])     # row 9: keys 2 and 4 live
+    out, lse = dsa.dsa_sparse_mla_fwd(t["q_nope"], t["q_pe"], t["ckv"], t["kpe"], t["W_UK"], t["W_UV"], sel.cuda(),
+                                      H.seqs_of(wl), sh.softmax_scale)
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    assert np.all(out[5] == 0) and np.all(np.isneginf(lse[5]))
+    assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+    T = wl.tensors
+    cache = H.f32np(T["kv_cache"])
+    ro, rl = oracle.sparse_mla_absorbed(H.f32np(T["q_nope"][9:10]), H.f32np(T["q_pe"][9:10]), cache[:, :sh.d_c],
+                                        cache[:, sh.d_c:], H.f32np(T["W_UK"]), H.f32np(T["W_UV"]),
+                                        np.array([[2, 4]], np.int32), np.array([9]), sh.softmax_scale)
+    assert np.abs(out[9] - ro[0]).max() <= H.OUT_ATOL_BF16
+
+
+# ---------------------------------------------------------------------------
+# the whole path
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", list(CASES))
+def test_forward_end_to_end(name):
+    wl, t = case(name)
+    ref = _oracle(name)
+    out, lse, idx = H.gpu_forward(wl, t)
+    out, idx = out.float().cpu().numpy(), idx.cpu().numpy()
+    for r, o in ref.items():
+        H.check_selection_row(idx[r], o["scores"], o["absterm"], o["pos"], wl.shape.k)
+    err = max(np.abs(out[r] - o["out"]).max() for r, o in ref.items())
+    assert err <= out_atol(wl), f"max abs err {err:.3e}"
+
+
+def test_forward_dense_when_k_covers_the_sequence():
+    """k >= S: every causal key is selected (rows keep t + 1 keys) and the
+    result is plain causal attention (nnterp deepseek_v32 note)."""
+    wl = di.generate("dense", di.Shape(k=512), 14, [200], [200], [0])
+    t = H.to_device(wl)
+    out, _, idx = H.gpu_forward(wl, t)
+    idx = idx.cpu().numpy()
+    assert ((idx >= 0).sum(1) == np.arange(1, 201)).all()
+    sh = wl.shape
+    T = wl.tensors
+    cache = H.f32np(T["kv_cache"])
+    KC, V = oracle.kv_up(cache[:, :sh.d_c], H.f32np(T["W_UK"]), H.f32np(T["W_UV"]))
+    rows = [0, 1, 57, 199]
+    ref, _ = oracle.dense_masked_mla(H.f32np(T["q_nope"][rows]), H.f32np(T["q_pe"][rows]), KC, cache[:, sh.d_c:], V,
+                                     np.array(rows), sh.softmax_scale)
+    assert np.abs(out.float().cpu().numpy()[rows] - ref).max() <= H.OUT_ATOL_BF16
+
+
+def test_forward_yarn_scale_and_empty_sequence():
+    """The released model's YaRN-scaled softmax scale 0.1352, and a batch
+    holding an empty sequence (T = 0) between two others."""
+    sh = di.Shape(k=128, softmax_scale=192 ** -0.5 * (0.1 * math.log(40) + 1) ** 2)
+    wl = di.generate("yarn", sh, 15, [40, 0, 3], [300, 50, 200], [260, 10, 197])
+    t = H.to_device(wl)
+    ref = H.oracle_rows(wl, list(range(wl.total_q)))
+    out, _, idx = H.gpu_forward(wl, t)
+    out, idx = out.float().cpu().numpy(), idx.cpu().numpy()
+    for r, o in ref.items():
+        H.check_selection_row(idx[r], o["scores"], o["absterm"], o["pos"], sh.k)
+        assert np.abs(out[r] - o["out"]).max() <= H.OUT_ATOL_BF16
+
+
+def test_forward_deterministic():
+    wl, t = case("bf16-ragged")
+    a = H.gpu_forward(wl, t)
+    b = H.gpu_forward(wl, t)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[2], b[2])
+    assert torch.equal(a[1], b[1])
