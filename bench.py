@@ -39,7 +39,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=1, help="workload 0..4 (1 = the headline prefill)")
-    ap.add_argument("--cpu-rows", type=int, default=256, help="rows of the oracle's bounded sample")
+    ap.add_argument("--cpu-rows", type=int, default=1024, help="rows of the oracle's bounded sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()

@@ -120,7 +120,10 @@ __global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(const float *__r
             }
         }
         __syncthreads();
-        if (gt) out[base_gt + warp_gt[wid] + __popc(bg & lt_mask)] = s;
+        if (gt) {
+            const int rank = base_gt + warp_gt[wid] + __popc(bg & lt_mask);
+            if (rank < n_gt) out[rank] = s;
+        }
         if (eq) {
             const int rank = base_eq + warp_eq[wid] + __popc(be & lt_mask);
             if (rank < remaining) out[n_gt + rank] = s;
