@@ -8,7 +8,6 @@
 #include "dsa_common.cuh"
 
 namespace dsa {
-namespace {
 
 thread_local int g_last_cuda = 0;
 thread_local uint32_t g_kernels = 0;
@@ -31,17 +30,13 @@ int fail_cuda(cudaError_t e) {
     return DSA_ERR_CUDA;
 }
 
+namespace {
+
 constexpr size_t WS_ALIGN = 256;
 inline size_t align_up(size_t x, size_t a = WS_ALIGN) { return (x + a - 1) / a * a; }
 inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-// A validated batch: the kernel table for all rows plus summary sizes.
-struct Batch {
-    SeqTab st;
-    int total_q = 0;
-    int64_t total_k = 0;
-    int max_S = 0;
-};
+}  // namespace
 
 int build_batch(const dsa_seqs *s, Batch &b) {
     if (!s || s->B < 1 || s->B > DSA_MAX_SEQS || !s->cu_q || !s->cu_k || !s->start_pos) return DSA_ERR_INVALID_ARG;
@@ -65,6 +60,8 @@ int build_batch(const dsa_seqs *s, Batch &b) {
     b.total_k = s->cu_k[s->B];
     return DSA_OK;
 }
+
+namespace {
 
 // The table of rows [r0, r1) of a validated batch: each sequence that overlaps
 // the range contributes its overlapping rows, with start_pos advanced to the
@@ -95,6 +92,8 @@ int check_indexer_shape(int idx_dtype, int H_I, int D_I) {
     return DSA_OK;
 }
 
+}  // namespace
+
 int check_mla_shape(int dtype, int H, int d_n, int d_r, int d_c, int d_v, int k) {
     if (H < 1 || d_n < 1 || d_r < 0 || d_c < 1 || d_v < 1 || k < 1) return DSA_ERR_INVALID_ARG;
     if (dtype != DSA_F32 && dtype != DSA_BF16) return DSA_ERR_UNSUPPORTED;
@@ -103,8 +102,6 @@ int check_mla_shape(int dtype, int H, int d_n, int d_r, int d_c, int d_v, int k)
     if ((d_c * dtype_bytes(dtype)) % 16 != 0) return DSA_ERR_UNSUPPORTED;
     return DSA_OK;
 }
-
-}  // namespace
 
 void note_launch(uint32_t kernel_bit) {
     g_kernels |= kernel_bit;
@@ -116,14 +113,9 @@ void note_launch(uint32_t kernel_bit) {
 using namespace dsa;
 
 namespace dsa {
-namespace {
 
 // Scratch of the attention stage: q~ = q_nope W_UK and the latent context,
 // both fp32 [M, H, d_c] on the generic path.
-struct MlaWs {
-    size_t qt = 0, olat = 0, total = 0;
-};
-
 MlaWs mla_ws_layout(int H, int d_c, int64_t total_q) {
     MlaWs w;
     const size_t per = align_up((size_t)total_q * H * d_c * sizeof(float));
@@ -136,7 +128,7 @@ MlaWs mla_ws_layout(int H, int d_c, int64_t total_q) {
 int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int64_t ld_kv, const void *k_pe,
             int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n, int d_r, int d_c, int d_v,
             const int32_t *idx, int k, const Batch &bt, float scale, void *out, float *lse, char *ws,
-            cudaStream_t s, bool mark = false) {
+            cudaStream_t s, bool mark) {
     const MlaWs L = mla_ws_layout(H, d_c, bt.total_q);
     float *qt = (float *)(ws + L.qt);
     float *olat = (float *)(ws + L.olat);
@@ -158,6 +150,23 @@ int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int
     if (mark) stage_mark(5, s);
     return DSA_OK;
 }
+
+size_t mla_workspace_bytes(int H, int d_c, int64_t total_q) { return mla_ws_layout(H, d_c, total_q).total; }
+
+int validate_mla_call(const void *q_nope, const void *q_pe, int dtype, const void *kv_cache, int64_t ld_kv,
+                      const void *k_pe, int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n, int d_r,
+                      int d_c, int d_v, const int32_t *idx, int k, const dsa_seqs *seqs, void *out, Batch &bt) {
+    int rc = build_batch(seqs, bt);
+    if (rc) return rc;
+    if ((rc = check_mla_shape(dtype, H, d_n, d_r, d_c, d_v, k))) return rc;
+    if (ld_kv < d_c || ld_pe < d_r) return DSA_ERR_INVALID_ARG;
+    if (bt.total_q == 0) return DSA_OK;
+    if (!q_nope || (d_r > 0 && (!q_pe || !k_pe)) || !kv_cache || !W_UK || !W_UV || !idx || !out)
+        return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+}
+
+namespace {
 
 int run_indexer(const void *q, const float *q_scale, const void *k, const float *k_scale, int idx_dtype,
                 const float *w, int H_I, int D_I, const SeqTab &st, int rows, int max_S, float *scores, int64_t ld,
@@ -260,15 +269,11 @@ int dsa_sparse_mla_fwd(const void *q_nope, const void *q_pe, int dtype, const vo
                        void *out, float *lse, void *workspace, size_t ws_bytes, void *stream) {
     reset_trace();
     Batch bt;
-    int rc = build_batch(seqs, bt);
-    if (rc) return rc;
-    if ((rc = check_mla_shape(dtype, H, d_n, d_r, d_c, d_v, k))) return rc;
-    if (ld_kv < d_c || ld_pe < d_r) return DSA_ERR_INVALID_ARG;
-    if (bt.total_q == 0) return DSA_OK;
-    if (!q_nope || (d_r > 0 && (!q_pe || !k_pe)) || !kv_cache || !W_UK || !W_UV || !idx || !out)
-        return DSA_ERR_INVALID_ARG;
+    int rc = validate_mla_call(q_nope, q_pe, dtype, kv_cache, ld_kv, k_pe, ld_pe, W_UK, W_UV, H, d_n, d_r, d_c, d_v,
+                               idx, k, seqs, out, bt);
+    if (rc || bt.total_q == 0) return rc;
     if (!workspace || !aligned(workspace, WS_ALIGN)) return DSA_ERR_WORKSPACE;
-    if (ws_bytes < mla_ws_layout(H, d_c, bt.total_q).total) return DSA_ERR_WORKSPACE;
+    if (ws_bytes < mla_workspace_bytes(H, d_c, bt.total_q)) return DSA_ERR_WORKSPACE;
     return run_mla(q_nope, q_pe, dtype, kv_cache, ld_kv, k_pe, ld_pe, W_UK, W_UV, H, d_n, d_r, d_c, d_v, idx, k, bt,
                    softmax_scale, out, lse, (char *)workspace, (cudaStream_t)stream);
 }

@@ -66,9 +66,37 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 }
 
 // ---------------------------------------------------------------------------
-// Host-side bookkeeping (dsa_api.cu)
+// Host-side bookkeeping and shared host logic (dsa_api.cu)
 // ---------------------------------------------------------------------------
 void note_launch(uint32_t kernel_bit);
+void reset_trace();
+int fail_cuda(cudaError_t e);
+
+// A validated batch: the kernel table for all rows plus summary sizes.
+struct Batch {
+    SeqTab st;
+    int total_q = 0;
+    int64_t total_k = 0;
+    int max_S = 0;
+};
+int build_batch(const dsa_seqs *s, Batch &b);
+int check_mla_shape(int dtype, int H, int d_n, int d_r, int d_c, int d_v, int k);
+
+// Scratch layout of the attention stage.
+struct MlaWs {
+    size_t qt = 0, olat = 0, total = 0;
+};
+MlaWs mla_ws_layout(int H, int d_c, int64_t total_q);
+size_t mla_workspace_bytes(int H, int d_c, int64_t total_q);
+// Every host-side check of dsa_sparse_mla_fwd except the workspace ones.
+int validate_mla_call(const void *q_nope, const void *q_pe, int dtype, const void *kv_cache, int64_t ld_kv,
+                      const void *k_pe, int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n, int d_r,
+                      int d_c, int d_v, const int32_t *idx, int k, const dsa_seqs *seqs, void *out, Batch &bt);
+// The attention stage (q~ absorb, sparse attention, W_UV) with scratch `ws`.
+int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int64_t ld_kv, const void *k_pe,
+            int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n, int d_r, int d_c, int d_v,
+            const int32_t *idx, int k, const Batch &bt, float scale, void *out, float *lse, char *ws,
+            cudaStream_t s, bool mark = false);
 
 // ---------------------------------------------------------------------------
 // Kernel launchers.  Each returns the cudaError_t of its launch.
