@@ -175,6 +175,39 @@ int dsa_sparse_mla_fwd(const void *q_nope, const void *q_pe, int dtype, const vo
                        void *stream);
 
 /* ------------------------------------------------------------------------
+ * Sparse latent attention without a caller workspace.
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that cannot obtain device memory when they run the attention, e.g. a
+ * serving runtime that has already handed all of HBM to its own KV-cache
+ * pool (a late cudaMalloc would fail or stall every stream), or a plugin
+ * called from such a runtime that receives only its input and output
+ * tensors.  It computes exactly what dsa_sparse_mla_fwd computes, with the
+ * same arguments minus the workspace, using scratch memory the library
+ * reserves on every GPU that loads it (DSA_NOALLOC_SCRATCH_BYTES, held until
+ * the process exits) instead of a caller buffer.  It allocates nothing.
+ *
+ *   - Limit: the call needs the same scratch as dsa_sparse_mla_workspace_size()
+ *     reports; a call needing more than DSA_NOALLOC_SCRATCH_BYTES returns
+ *     DSA_ERR_WORKSPACE and launches nothing.  With the 671B head shapes and
+ *     this version's scratch layout that is up to 128 query rows per call,
+ *     e.g. one decode step of up to 128 sequences.
+ *   - The first call on each device looks up the scratch's device address
+ *     (with that device current) and caches it; make that first call before
+ *     any stream capture.
+ *   - Every call on a device shares the one scratch array, which keeps the
+ *     previous call's contents (the attention writes every scratch byte it
+ *     reads, so nothing needs clearing).  Calls that overlap on the GPU --
+ *     on different streams, or from several host threads without ordering --
+ *     race on it and give wrong results.
+ * Errors: as dsa_sparse_mla_fwd, plus DSA_ERR_WORKSPACE beyond the limit.
+ * ---------------------------------------------------------------------- */
+#define DSA_NOALLOC_SCRATCH_BYTES (64u << 20)
+int dsa_sparse_mla_fwd_noalloc(const void *q_nope, const void *q_pe, int dtype, const void *kv_cache,
+                               int64_t ld_kv, const void *k_pe, int64_t ld_pe, const void *W_UK, const void *W_UV,
+                               int H, int d_n, int d_r, int d_c, int d_v, const int32_t *idx, int k,
+                               const dsa_seqs *seqs, float softmax_scale, void *out, float *lse, void *stream);
+
+/* ------------------------------------------------------------------------
  * The whole path: [quantise] -> indexer -> top-k -> sparse latent attention.
  * Sources: as for the three stages above.  Rows are processed in chunks so
  * that the fp32 score buffer stays bounded; the workspace size covers one

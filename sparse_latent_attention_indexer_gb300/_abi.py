@@ -10,6 +10,7 @@ LIB_PATH = os.path.join(HERE, "libdsa.so")
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR_WORKSPACE = range(6)
 DSA_F32, DSA_BF16, DSA_E4M3 = 0, 1, 2
 DSA_MAX_SEQS = 512
+DSA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 KERNEL_BITS = {
     "quant": 1 << 0, "indexer_simt": 1 << 1, "indexer_tc": 1 << 2, "indexer_fp8": 1 << 3, "topk": 1 << 4,
@@ -46,6 +47,7 @@ SIGNATURES = [
     ("dsa_topk_select", I, [P, I64, SEQS, I, P, P]),
     ("dsa_sparse_mla_workspace_size", SZ, [I, I, I, I, I, I, I, SEQS]),
     ("dsa_sparse_mla_fwd", I, [P, P, I, P, I64, P, I64, P, P, I, I, I, I, I, P, I, SEQS, F, P, P, P, SZ, P]),
+    ("dsa_sparse_mla_fwd_noalloc", I, [P, P, I, P, I64, P, I64, P, P, I, I, I, I, I, P, I, SEQS, F, P, P, P]),
     ("dsa_forward_workspace_size", SZ, [PROB, SEQS]),
     ("dsa_forward", I, [PROB, SEQS, P, SZ, P]),
     ("dsa_status_string", ctypes.c_char_p, [I]),
