@@ -1,6 +1,7 @@
 // The C ABI of libdsa: argument validation, workspace carving, the row-chunk
 // loop of the whole path and the dispatch between the tensor-core kernels and
 // the generic ones.  Host code only; every arithmetic step runs in the kernels.
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -23,6 +24,11 @@ void stage_mark(int i, cudaStream_t s) {
 void reset_trace() {
     g_kernels = 0;
     g_launches = 0;
+}
+
+bool force_generic() {
+    const char *v = getenv("DSA_FORCE_GENERIC");
+    return v && v[0] == '1';
 }
 
 int fail_cuda(cudaError_t e) {
@@ -169,9 +175,13 @@ int validate_mla_call(const void *q_nope, const void *q_pe, int dtype, const voi
 namespace {
 
 int run_indexer(const void *q, const float *q_scale, const void *k, const float *k_scale, int idx_dtype,
-                const float *w, int H_I, int D_I, const SeqTab &st, int rows, int max_S, float *scores, int64_t ld,
-                cudaStream_t s) {
-    cudaError_t e = launch_indexer_simt(q, q_scale, k, k_scale, idx_dtype, w, H_I, D_I, st, rows, max_S, scores, ld, s);
+                const float *w, int H_I, int D_I, const SeqTab &st, int rows, int max_S, int64_t total_k,
+                float *scores, int64_t ld, bool fill_future, cudaStream_t s) {
+    cudaError_t e;
+    if (!force_generic() && indexer_tc_supported(idx_dtype, H_I, D_I) && aligned(q, 16) && aligned(k, 16))
+        e = launch_indexer_tc(q, q_scale, k, k_scale, idx_dtype, w, st, total_k, scores, ld, fill_future, s);
+    else
+        e = launch_indexer_simt(q, q_scale, k, k_scale, idx_dtype, w, H_I, D_I, st, rows, max_S, scores, ld, s);
     return e == cudaSuccess ? DSA_OK : fail_cuda(e);
 }
 
@@ -214,7 +224,7 @@ int dsa_check_device_error(void *stream, int *site) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     if (site) *site = 0;
-    return DSA_OK;
+    return indexer_tc_read_error(site);
 }
 
 int dsa_quant_e4m3_ue8m0(const void *x, int x_dtype, int64_t n_blocks, uint8_t *codes, float *scales, void *stream) {
@@ -241,7 +251,7 @@ int dsa_indexer_scores(const void *q_idx, const float *q_scale, const void *k_id
     if (!aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
     return run_indexer(q_idx, idx_dtype == DSA_E4M3 ? q_scale : nullptr, k_idx,
                        idx_dtype == DSA_E4M3 ? k_scale : nullptr, idx_dtype, w, H_I, D_I, bt.st, bt.total_q, bt.max_S,
-                       scores, ld_scores, (cudaStream_t)stream);
+                       bt.total_k, scores, ld_scores, true, (cudaStream_t)stream);
 }
 
 int dsa_topk_select(const float *scores, int64_t ld_scores, const dsa_seqs *seqs, int k, int32_t *idx, void *stream) {
@@ -376,8 +386,8 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
         int max_S = 0;
         sub_batch(seqs, r0, r1, st, max_S);
         rc = run_indexer((const char *)q_idx + qrow * r0, q_scale ? q_scale + (size_t)r0 * p->H_I : nullptr, k_idx,
-                         k_scale, idx_dtype, p->w + (size_t)r0 * p->H_I, p->H_I, p->D_I, st, r1 - r0, max_S, scores,
-                         L.ld, s);
+                         k_scale, idx_dtype, p->w + (size_t)r0 * p->H_I, p->H_I, p->D_I, st, r1 - r0, max_S,
+                         bt.total_k, scores, L.ld, false, s);
         if (rc) return rc;
         e = launch_topk(scores, L.ld, st, r1 - r0, p->top_k, idx + (size_t)r0 * p->top_k, s);
         if (e != cudaSuccess) return fail_cuda(e);

@@ -109,6 +109,17 @@ cudaError_t launch_indexer_simt(const void *q, const float *q_scale, const void 
                                 int dtype, const float *w, int H_I, int D_I, const SeqTab &st, int total_q,
                                 int max_S, float *scores, int64_t ld, cudaStream_t s);
 
+// tcgen05 indexer for H_I = 64, D_I = 128 (BF16 or E4M3 inputs).
+bool indexer_tc_supported(int dtype, int H_I, int D_I);
+cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k, const float *k_scale, int dtype,
+                              const float *w, const SeqTab &st, int64_t total_k, float *scores, int64_t ld,
+                              bool fill_future, cudaStream_t s);
+int indexer_tc_read_error(int *site);
+
+// DSA_FORCE_GENERIC=1 in the environment routes every stage to the generic
+// CUDA-core kernels (used by the tests to cross-check the tensor-core ones).
+bool force_generic();
+
 cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int total_q, int k, int32_t *idx,
                         cudaStream_t s);
 

@@ -1,0 +1,333 @@
+// Lightning indexer on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+//   S~^I_{t,s} = 1/(sqrt(H_I) sqrt(D_I)) sum_h w_{t,h} ReLU(q^I_{h,t} . k^I_s) + M_{t,s}
+// (DeepSeek-V3.2-Exp atlas page, MoE transformer block, indexer equations;
+// H_I = 64 heads of D_I = 128, the released configuration.)
+//
+// The head dot products are one dense contraction: for a block of 128 keys
+// and a group of 4 query tokens, D[128 keys, 4 x 64 (token, head)] =
+// K[128 x 128] . Q[256 x 128]^T, one tcgen05.mma chain (M = 128, N = 256,
+// K = 128) with the fp32 accumulator in tensor memory.  Keys sit on the MMA's
+// M axis, so after the MMA each epilogue thread owns one key (one TMEM lane)
+// and reduces that key's 64 head columns in registers: ReLU, the per-head
+// weight (with the constant 1/sqrt(H_I D_I) and, for FP8, the q block scale
+// folded in), the head sum, the k block scale, and the causal mask.  No
+// [T, 64, S] tensor ever reaches memory; only the [T, S] scores are stored.
+//
+// CTA = one group of 4 query rows (one sequence) x a strided subset of its
+// causal key blocks.  Warp roles: warp 0 issues TMA loads (the 4 x 64 query
+// rows once, then key blocks through a STAGES-deep ring), warp 1 issues the
+// MMAs, warp 2 owns the tensor memory (512 columns = two 256-column
+// accumulators, so the epilogue of block i overlaps the MMAs of block i+1),
+// warps 4..11 run the epilogue (two warps per TMEM lane quarter, each taking
+// two of the four tokens).  Every wait is bounded; a timeout records its
+// site in the device error word and the CTA drains and exits.
+//
+// FP8 variant: q^I and k^I are e4m3 codes with one power-of-two scale per
+// 128-value row (ue8m0), MMA kind::f8f6f4.  Because each scale covers a whole
+// head row, sum_h w s_q ReLU(s_k cq.ck) = s_k sum_h (w s_q) ReLU(cq.ck) holds
+// exactly, so the scales need no block-scaled MMA.
+#include "tc_common.cuh"
+
+namespace dsa {
+
+__device__ int g_indexer_tc_error = 0;
+
+namespace {
+
+constexpr int BM = 128;         // keys per block (MMA M)
+constexpr int TOK = 4;          // query tokens per group
+constexpr int HI = 64;          // indexer heads
+constexpr int DI = 128;         // indexer head dim
+constexpr int BN = TOK * HI;    // 256 (MMA N)
+constexpr int NUM_THREADS = 384;
+constexpr int EPI_WARP0 = 4;
+
+template <bool FP8>
+struct Cfg {
+    static constexpr int ELT = FP8 ? 1 : 2;
+    static constexpr int HALVES = FP8 ? 1 : 2;              // 128-byte column slabs per row
+    static constexpr int B_BYTES = BN * DI * ELT;           // 64 KB (bf16) / 32 KB (fp8)
+    static constexpr int A_BYTES = BM * DI * ELT;           // 32 KB / 16 KB
+    static constexpr int B_HALF = BN * 128;                 // bytes of one 128-byte slab of B
+    static constexpr int A_HALF = BM * 128;
+    static constexpr int STAGES = FP8 ? 6 : 4;
+    static constexpr int KSTEPS = FP8 ? 4 : 8;              // MMAs per block (K = 32 / 16 each)
+    static constexpr uint32_t IDESC =
+        FP8 ? tc::instr_desc(tc::kFmtE4M3, tc::kFmtE4M3, BM, BN, 0, 0) : tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, BM, BN, 0, 0);
+    static constexpr int SMEM = 1024 /*align slack*/ + B_BYTES + STAGES * A_BYTES + TOK * HI * 4 + 256;
+};
+
+struct IdxParams {
+    int B;
+    int q_off[DSA_MAX_SEQS + 1];
+    int k_base[DSA_MAX_SEQS];
+    int k_len[DSA_MAX_SEQS];
+    int start_pos[DSA_MAX_SEQS];
+    int g_off[DSA_MAX_SEQS + 1];  // cumulative query groups
+    int total_groups;
+    int splits;                    // CTAs per group (strided key blocks)
+    int fill_future;
+    int64_t ld;
+    float c;
+};
+
+template <bool FP8>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const float *__restrict__ w, const float *__restrict__ q_scale,
+                      const float *__restrict__ k_scale, const __grid_constant__ IdxParams P,
+                      float *__restrict__ scores) {
+    using C = Cfg<FP8>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *Bt = base;
+    uint8_t *As = Bt + C::B_BYTES;
+    float *wsm = (float *)(As + C::STAGES * C::A_BYTES);
+    uint64_t *bars = (uint64_t *)(wsm + TOK * HI);
+    uint64_t *full = bars, *empty = bars + C::STAGES, *bfull = bars + 2 * C::STAGES;
+    uint64_t *tfull = bfull + 1, *tempty = tfull + 2, *mmadone = tempty + 2;
+    uint32_t *tmem_slot = (uint32_t *)(mmadone + 1);
+    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+    __shared__ int never;  // an abort flag nobody raises, for the drain waits
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Heavier groups (later tokens of a sequence see more keys) start first.
+    const int lin = P.total_groups * P.splits - 1 - (int)blockIdx.x;
+    const int g = lin / P.splits, split = lin % P.splits;
+    int b = 0;
+    {
+        int lo = 0, hi = P.B - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (P.g_off[mid] <= g) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+    }
+    const int T_b = P.q_off[b + 1] - P.q_off[b];
+    const int t0 = (g - P.g_off[b]) * TOK;
+    const int ntok = min(TOK, T_b - t0);
+    const int r0 = P.q_off[b] + t0;
+    const int p0 = P.start_pos[b] + t0;
+    const int S = P.k_len[b], kbase = P.k_base[b];
+    const int nblk = (p0 + ntok - 1) / BM + 1;  // blocks holding keys 0 .. last position
+    const int mine = split < nblk ? (nblk - split + P.splits - 1) / P.splits : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::STAGES; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], 1);
+        }
+        tc::mbar_init(bfull, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&tfull[i], 1);
+            tc::mbar_init(&tempty[i], 8);
+        }
+        tc::mbar_init(mmadone, 1);
+        *abort_flag = 0;
+        never = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 2) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    if (warp >= EPI_WARP0) {
+        for (int i = threadIdx.x - EPI_WARP0 * 32; i < TOK * HI; i += (NUM_THREADS - EPI_WARP0 * 32)) {
+            const int tt = i / HI, h = i % HI;
+            float v = 0.0f;
+            if (tt < ntok) {
+                const int64_t qi = (int64_t)(r0 + tt) * HI + h;
+                v = w[qi] * P.c * (FP8 ? q_scale[qi] : 1.0f);
+            }
+            wsm[i] = v;
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (mine > 0) {
+        if (warp == 0 && lane == 0) {
+            // ---------------- TMA producer ----------------
+            tc::prefetch_tmap(&tm_q);
+            tc::prefetch_tmap(&tm_k);
+            tc::mbar_arrive_expect_tx(bfull, C::B_BYTES);
+            for (int h = 0; h < C::HALVES; ++h) tc::tma_load_2d(Bt + h * C::B_HALF, &tm_q, bfull, h * 64, r0 * HI);
+            int issued = 0;
+            for (int i = 0; i < mine; ++i) {
+                const int st = i % C::STAGES;
+                if (!tc::mbar_wait(&empty[st], ((i / C::STAGES) & 1) ^ 1, abort_flag, &g_indexer_tc_error, 1)) break;
+                const int row = kbase + (split + i * P.splits) * BM;
+                tc::mbar_arrive_expect_tx(&full[st], C::A_BYTES);
+                for (int h = 0; h < C::HALVES; ++h)
+                    tc::tma_load_2d(As + st * C::A_BYTES + h * C::A_HALF, &tm_k, &full[st], h * 64, row);
+                ++issued;
+            }
+            // Drain: the last loads of each stage must have landed before the CTA exits.
+            tc::mbar_wait(bfull, 0, (volatile int *)&never, &g_indexer_tc_error, 2);
+            for (int j = max(0, issued - C::STAGES); j < issued; ++j)
+                tc::mbar_wait(&full[j % C::STAGES], (j / C::STAGES) & 1, (volatile int *)&never, &g_indexer_tc_error, 3);
+        } else if (warp == 1 && lane == 0) {
+            // ---------------- MMA issuer ----------------
+            bool ok = tc::mbar_wait(bfull, 0, abort_flag, &g_indexer_tc_error, 4);
+            int issued = 0;
+            for (int i = 0; ok && i < mine; ++i) {
+                const int st = i % C::STAGES, acc = i & 1;
+                if (!tc::mbar_wait(&tempty[acc], ((i >> 1) & 1) ^ 1, abort_flag, &g_indexer_tc_error, 5)) break;
+                if (!tc::mbar_wait(&full[st], (i / C::STAGES) & 1, abort_flag, &g_indexer_tc_error, 6)) break;
+                tc::tc_fence_after();
+                const uint32_t d = tmem + acc * BN;
+                const uint32_t a0 = tc::smem_u32(As + st * C::A_BYTES), b0 = tc::smem_u32(Bt);
+#pragma unroll
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    // 32 bytes of K per step: 16 bf16 or 32 e4m3 values.
+                    const int slab = FP8 ? 0 : kk / 4, off = (FP8 ? kk : kk % 4) * 32;
+                    const uint64_t ad = tc::smem_desc(a0 + slab * C::A_HALF + off, 16, 1024);
+                    const uint64_t bd = tc::smem_desc(b0 + slab * C::B_HALF + off, 16, 1024);
+                    if (FP8) tc::mma_f8(d, ad, bd, C::IDESC, kk > 0);
+                    else tc::mma_f16(d, ad, bd, C::IDESC, kk > 0);
+                }
+                tc::mma_commit(&empty[st]);
+                tc::mma_commit(&tfull[acc]);
+                ++issued;
+            }
+            // No MMA may still be running when the tensor memory is released.
+            if (issued > 0) {
+                tc::mma_commit(mmadone);
+                tc::mbar_wait(mmadone, 0, (volatile int *)&never, &g_indexer_tc_error, 7);
+            }
+        } else if (warp >= EPI_WARP0) {
+            // ---------------- epilogue ----------------
+            const int q = warp & 3, hf = (warp - EPI_WARP0) >> 2;
+            float *out_base = scores + (int64_t)r0 * P.ld;
+            for (int i = 0; i < mine; ++i) {
+                const int acc = i & 1;
+                if (!tc::mbar_wait(&tfull[acc], (i >> 1) & 1, abort_flag, &g_indexer_tc_error, 8)) break;
+                tc::tc_fence_after();
+                const int key = (split + i * P.splits) * BM + q * 32 + lane;
+                const float ks = (FP8 && key < S) ? k_scale[kbase + key] : 1.0f;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int tt = 2 * hf + j;
+                    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + tt * HI;
+                    float v0[32], v1[32];
+                    tc::tmem_ld32(taddr, v0);
+                    tc::tmem_ld32(taddr + 32, v1);
+                    tc::tmem_ld_wait();
+                    const float4 *wv = (const float4 *)(wsm + tt * HI);
+                    float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+                    for (int h4 = 0; h4 < 8; ++h4) {
+                        const float4 a = wv[h4], c = wv[8 + h4];
+                        s0 = fmaf(a.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
+                        s1 = fmaf(c.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
+                        s0 = fmaf(a.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
+                        s1 = fmaf(c.y, fmaxf(v1[4 * h4 + 1], 0.0f), s1);
+                        s0 = fmaf(a.z, fmaxf(v0[4 * h4 + 2], 0.0f), s0);
+                        s1 = fmaf(c.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
+                        s0 = fmaf(a.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
+                        s1 = fmaf(c.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
+                    }
+                    if (tt < ntok && key < S)
+                        out_base[(int64_t)tt * P.ld + key] = (key <= p0 + tt) ? (s0 + s1) * ks : -INFINITY;
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+            }
+        }
+    }
+    __syncthreads();
+    // Masked tail: keys past every computed block are future keys of all rows.
+    if (P.fill_future && split == 0 && warp >= EPI_WARP0) {
+        const int start = nblk * BM;
+        for (int tt = 0; tt < ntok; ++tt)
+            for (int s = start + threadIdx.x - EPI_WARP0 * 32; s < S; s += NUM_THREADS - EPI_WARP0 * 32)
+                scores[(int64_t)(r0 + tt) * P.ld + s] = -INFINITY;
+    }
+    if (warp == 2) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool indexer_tc_supported(int dtype, int H_I, int D_I) {
+    return (dtype == DSA_BF16 || dtype == DSA_E4M3) && H_I == HI && D_I == DI;
+}
+
+int indexer_tc_read_error(int *site) {
+    int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_indexer_tc_error, sizeof(int));
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (v) {
+        e = cudaMemcpyToSymbol(g_indexer_tc_error, &zero, sizeof(int));
+        if (e != cudaSuccess) return fail_cuda(e);
+        if (site) *site = v;
+        return DSA_ERR_TIMEOUT;
+    }
+    return DSA_OK;
+}
+
+cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k, const float *k_scale, int dtype,
+                              const float *w, const SeqTab &st, int64_t total_k, float *scores, int64_t ld,
+                              bool fill_future, cudaStream_t s) {
+    const bool fp8 = dtype == DSA_E4M3;
+    static thread_local IdxParams P;  // ~10 KB: keep it off the host stack
+    P.B = st.B;
+    P.g_off[0] = 0;
+    for (int i = 0; i < st.B; ++i) {
+        P.q_off[i] = st.q_off[i];
+        P.k_base[i] = st.k_base[i];
+        P.k_len[i] = st.k_len[i];
+        P.start_pos[i] = st.start_pos[i];
+        const int T = st.q_off[i + 1] - st.q_off[i];
+        P.g_off[i + 1] = P.g_off[i] + (T + TOK - 1) / TOK;
+    }
+    P.q_off[st.B] = st.q_off[st.B];
+    P.total_groups = P.g_off[st.B];
+    if (P.total_groups == 0) return cudaSuccess;
+    const int want = 2 * 152;
+    P.splits = P.total_groups >= want ? 1 : std::min(16, (want + P.total_groups - 1) / P.total_groups);
+    P.fill_future = fill_future ? 1 : 0;
+    P.ld = ld;
+    P.c = 1.0f / sqrtf((float)(HI * DI));
+
+    const int total_q = st.q_off[st.B];
+    CUtensorMap tq, tk;
+    const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t row_bytes = (uint64_t)DI * (fp8 ? 1 : 2);
+    const uint32_t inner = fp8 ? 128 : 64;
+    {
+        uint64_t dims[2] = {(uint64_t)DI, (uint64_t)total_q * HI};
+        uint64_t strides[1] = {row_bytes};
+        uint32_t box[2] = {inner, (uint32_t)BN};
+        if (!make_tmap(&tq, ty, 2, q, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        uint64_t dims[2] = {(uint64_t)DI, (uint64_t)std::max<int64_t>(total_k, 1)};
+        uint64_t strides[1] = {row_bytes};
+        uint32_t box[2] = {inner, (uint32_t)BM};
+        if (!make_tmap(&tk, ty, 2, k, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    const unsigned grid = (unsigned)P.total_groups * P.splits;
+    cudaError_t e;
+    if (fp8) {
+        e = cudaFuncSetAttribute(indexer_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true>::SMEM);
+        if (e != cudaSuccess) return e;
+        indexer_tc_kernel<true><<<grid, NUM_THREADS, Cfg<true>::SMEM, s>>>(tq, tk, w, q_scale, k_scale, P, scores);
+        note_launch(DSA_KERNEL_INDEXER_FP8);
+    } else {
+        e = cudaFuncSetAttribute(indexer_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg<false>::SMEM);
+        if (e != cudaSuccess) return e;
+        indexer_tc_kernel<false><<<grid, NUM_THREADS, Cfg<false>::SMEM, s>>>(tq, tk, w, nullptr, nullptr, P, scores);
+        note_launch(DSA_KERNEL_INDEXER_TC);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace dsa

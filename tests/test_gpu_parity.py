@@ -244,3 +244,27 @@ def test_forward_deterministic():
     b = H.gpu_forward(wl, t)
     assert torch.equal(a[0], b[0]) and torch.equal(a[2], b[2])
     assert torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("name", ["bf16-ragged", "bf16-k64", "fp8-ragged"])
+def test_indexer_tensor_core_matches_generic(name, monkeypatch):
+    """The tcgen05 indexer and the CUDA-core indexer on the same inputs agree
+    to fp32 summation-order noise, and the tensor-core kernel is the one the
+    default dispatch runs for the 64 x 128 indexer shape."""
+    wl, t = case(name)
+    tc_scores = _gpu_scores(wl, t)
+    kernels = dsa.last_kernels()
+    assert ("indexer_fp8" if wl.shape.idx_fp8 else "indexer_tc") in kernels, kernels
+    monkeypatch.setenv("DSA_FORCE_GENERIC", "1")
+    gen_scores = _gpu_scores(wl, t)
+    assert "indexer_simt" in dsa.last_kernels()
+    monkeypatch.delenv("DSA_FORCE_GENERIC")
+    a, b = tc_scores.cpu().numpy(), gen_scores.cpu().numpy()
+    for bq in range(wl.B):
+        rows = slice(wl.cu_q[bq], wl.cu_q[bq + 1])
+        S = wl.S[bq]
+        x, y = a[rows, :S], b[rows, :S]
+        assert np.array_equal(np.isneginf(x), np.isneginf(y))
+        fin = np.isfinite(y)
+        scale = np.abs(y[fin]).max() if fin.any() else 1.0
+        assert np.abs(x[fin] - y[fin]).max() <= 1e-5 * scale
