@@ -123,30 +123,58 @@ namespace dsa {
 // Scratch of the attention stage: q~ = q_nope W_UK and the latent context,
 // both fp32 [M, H, d_c] on the generic path.
 MlaWs mla_ws_layout(int H, int d_c, int64_t total_q) {
+    // Generic path: q~ and the latent context in fp32.  Tensor-core path: the
+    // bf16 [q~ | q_pe] rows and bf16 context fit in the same two regions, plus
+    // the split partials of short batches.
     MlaWs w;
     const size_t per = align_up((size_t)total_q * H * d_c * sizeof(float));
     w.qt = 0;
     w.olat = per;
-    w.total = 2 * per;
+    w.part = 2 * per;
+    w.total = w.part + align_up(mla_tc_partial_bytes((int)total_q));
     return w;
 }
 
 int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int64_t ld_kv, const void *k_pe,
             int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n, int d_r, int d_c, int d_v,
             const int32_t *idx, int k, const Batch &bt, float scale, void *out, float *lse, char *ws,
-            cudaStream_t s, bool mark) {
+            cudaStream_t s, bool mark, bool prefix_valid) {
     const MlaWs L = mla_ws_layout(H, d_c, bt.total_q);
-    float *qt = (float *)(ws + L.qt);
-    float *olat = (float *)(ws + L.olat);
     const int M = bt.total_q;
     cudaError_t e;
+    const bool fast = !force_generic() && absorb_tc_supported(dtype, H, d_n, d_r, d_c, d_v) && aligned(q_nope, 16) &&
+                      aligned(q_pe, 16) && aligned(W_UK, 16) && aligned(W_UV, 16) && aligned(out, 16);
+    if (fast) {
+        // q~ rows [M, H, d_c + d_r] bf16 = [q_nope W_UK | q_pe]; latent context bf16 [M, H, d_c].
+        __nv_bfloat16 *qt = (__nv_bfloat16 *)(ws + L.qt);
+        __nv_bfloat16 *olat = (__nv_bfloat16 *)(ws + L.olat);
+        const int W = d_c + d_r;
+        e = launch_absorb_q_tc(q_nope, W_UK, q_pe, qt, M, H, d_r, s);
+        if (e != cudaSuccess) return fail_cuda(e);
+        if (mark) stage_mark(3, s);
+        if (mla_tc_supported(dtype, H, d_n, d_r, d_c, d_v) && aligned(kv, 16) && aligned(k_pe, 16) && ld_kv % 8 == 0 &&
+            ld_pe % 8 == 0)
+            e = launch_mla_tc(qt, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, bt.total_k, M, scale, prefix_valid, olat, lse,
+                              ws + L.part, s);
+        else
+            e = launch_mla_simt(qt, DSA_BF16, W, qt + d_c, W, dtype, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, M, H, d_r,
+                                d_c, scale, olat, DSA_BF16, lse, s);
+        if (e != cudaSuccess) return fail_cuda(e);
+        if (mark) stage_mark(4, s);
+        e = launch_absorb_v_tc(olat, W_UV, out, M, H, s);
+        if (e != cudaSuccess) return fail_cuda(e);
+        if (mark) stage_mark(5, s);
+        return DSA_OK;
+    }
+    float *qt = (float *)(ws + L.qt);
+    float *olat = (float *)(ws + L.olat);
     // q~[m,h,:] = q_nope[m,h,:] . W_UK[h]    (K = d_n, N = d_c)
     e = launch_absorb_simt(q_nope, dtype, (int64_t)H * d_n, W_UK, dtype, qt, DSA_F32, (int64_t)H * d_c, M, H, d_n,
                            d_c, s);
     if (e != cudaSuccess) return fail_cuda(e);
     if (mark) stage_mark(3, s);
-    e = launch_mla_simt(qt, DSA_F32, q_pe, dtype, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, M, H, d_r, d_c, scale, olat,
-                        lse, s);
+    e = launch_mla_simt(qt, DSA_F32, d_c, q_pe, d_r, dtype, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, M, H, d_r, d_c,
+                        scale, olat, DSA_F32, lse, s);
     if (e != cudaSuccess) return fail_cuda(e);
     if (mark) stage_mark(4, s);
     // out[m,h,:] = o_lat[m,h,:] . W_UV[h]    (K = d_c, N = d_v)
@@ -224,7 +252,10 @@ int dsa_check_device_error(void *stream, int *site) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     if (site) *site = 0;
-    return indexer_tc_read_error(site);
+    int rc = indexer_tc_read_error(site);
+    if (rc) return rc;
+    if ((rc = absorb_tc_read_error(site))) return rc;
+    return mla_tc_read_error(site);
 }
 
 int dsa_quant_e4m3_ue8m0(const void *x, int x_dtype, int64_t n_blocks, uint8_t *codes, float *scales, void *stream) {
@@ -395,7 +426,7 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
     stage_mark(2, s);
     return run_mla(p->q_nope, p->q_pe, p->dtype, p->kv_cache, p->ld_kv, p->k_pe, p->ld_pe, p->W_UK, p->W_UV, p->H,
                    p->d_n, p->d_r, p->d_c, p->d_v, idx, p->top_k, bt, p->softmax_scale, p->out, p->lse, ws + L.mla, s,
-                   true);
+                   true, true);
 }
 
 }  // extern "C"

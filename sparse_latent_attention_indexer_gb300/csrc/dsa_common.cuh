@@ -84,7 +84,7 @@ int check_mla_shape(int dtype, int H, int d_n, int d_r, int d_c, int d_v, int k)
 
 // Scratch layout of the attention stage.
 struct MlaWs {
-    size_t qt = 0, olat = 0, total = 0;
+    size_t qt = 0, olat = 0, part = 0, total = 0;
 };
 MlaWs mla_ws_layout(int H, int d_c, int64_t total_q);
 size_t mla_workspace_bytes(int H, int d_c, int64_t total_q);
@@ -96,7 +96,7 @@ int validate_mla_call(const void *q_nope, const void *q_pe, int dtype, const voi
 int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int64_t ld_kv, const void *k_pe,
             int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n, int d_r, int d_c, int d_v,
             const int32_t *idx, int k, const Batch &bt, float scale, void *out, float *lse, char *ws,
-            cudaStream_t s, bool mark = false);
+            cudaStream_t s, bool mark = false, bool prefix_valid = false);
 
 // ---------------------------------------------------------------------------
 // Kernel launchers.  Each returns the cudaError_t of its launch.
@@ -128,10 +128,32 @@ cudaError_t launch_absorb_simt(const void *A, int a_dtype, int64_t lda_row, cons
                                int c_dtype, int64_t ldc_row, int M, int H, int K, int N, cudaStream_t s);
 
 // Generic SIMT sparse attention in the latent space: per (row, head) online
-// softmax over the selected keys.  qt [M, H, d_c] (qt_dtype), q_pe, cache.
-cudaError_t launch_mla_simt(const void *qt, int qt_dtype, const void *q_pe, int dtype, const void *kv,
-                            int64_t ld_kv, const void *k_pe, int64_t ld_pe, const int32_t *idx, int k,
-                            const SeqTab &st, int total_q, int H, int d_r, int d_c, float scale, float *olat,
-                            float *lse, cudaStream_t s);
+// softmax over the selected keys.  qt rows [M, H, qt_ld] (qt_dtype) hold q~ in
+// their first d_c columns; q_pe rows [M, H, qpe_ld]; the latent context is
+// written [M, H, d_c] as olat_dtype.
+cudaError_t launch_mla_simt(const void *qt, int qt_dtype, int qt_ld, const void *q_pe, int qpe_ld, int dtype,
+                            const void *kv, int64_t ld_kv, const void *k_pe, int64_t ld_pe, const int32_t *idx, int k,
+                            const SeqTab &st, int total_q, int H, int d_r, int d_c, float scale, void *olat,
+                            int olat_dtype, float *lse, cudaStream_t s);
+
+// tcgen05 absorption GEMMs (bf16, d_n = 128, d_c = 512, d_v = 128):
+// qt [M, H, 512 + d_r] = [q_nope W_UK | q_pe];  out [M, H, 128] = olat W_UV.
+bool absorb_tc_supported(int dtype, int H, int d_n, int d_r, int d_c, int d_v);
+cudaError_t launch_absorb_q_tc(const void *q_nope, const void *W_UK, const void *q_pe, void *qt, int M, int H,
+                               int d_r, cudaStream_t s);
+cudaError_t launch_absorb_v_tc(const void *olat, const void *W_UV, void *out, int M, int H, cudaStream_t s);
+int absorb_tc_read_error(int *site);
+
+// tcgen05 sparse latent attention (bf16, H = 128, d_c = 512, d_r = 64): qt rows
+// [M, 128, 576] = [q~ | q_pe] -> olat [M, 128, 512] bf16 and lse.  Rows with
+// few entries per split write fp32 partials to part_ws (mla_tc_partial_bytes)
+// and a combine kernel merges them.
+bool mla_tc_supported(int dtype, int H, int d_n, int d_r, int d_c, int d_v);
+int mla_tc_splits(int M);
+size_t mla_tc_partial_bytes(int M);
+cudaError_t launch_mla_tc(const void *qt, const void *kv, int64_t ld_kv, const void *kpe, int64_t ld_pe,
+                          const int32_t *idx, int k, const SeqTab &st, int64_t total_k, int M, float scale,
+                          bool prefix_valid, void *olat, float *lse, void *part_ws, cudaStream_t s);
+int mla_tc_read_error(int *site);
 
 }  // namespace dsa

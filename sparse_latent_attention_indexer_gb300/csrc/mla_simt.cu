@@ -83,13 +83,14 @@ constexpr int HG = 8;             // heads per CTA (one warp each)
 constexpr int KC = 32;            // keys per chunk
 constexpr int MAX_PER_LANE = 32;  // d_c <= 1024
 
-template <typename TQ, typename T>
-__global__ void __launch_bounds__(HG * 32) mla_simt_kernel(const TQ *__restrict__ qt, const T *__restrict__ q_pe,
+template <typename TQ, typename T, typename TO>
+__global__ void __launch_bounds__(HG * 32) mla_simt_kernel(const TQ *__restrict__ qt, int qt_ld,
+                                                           const T *__restrict__ q_pe, int qpe_ld,
                                                            const T *__restrict__ kv, int64_t ld_kv,
                                                            const T *__restrict__ kpe, int64_t ld_pe,
                                                            const int32_t *__restrict__ idx, int k,
                                                            const __grid_constant__ SeqTab st, int H, int d_r, int d_c,
-                                                           float scale, float *__restrict__ olat,
+                                                           float scale, TO *__restrict__ olat,
                                                            float *__restrict__ lse) {
     extern __shared__ float smem[];
     __shared__ int keys[KC];
@@ -105,8 +106,8 @@ __global__ void __launch_bounds__(HG * 32) mla_simt_kernel(const TQ *__restrict_
         const int hh = i / W, c = i - hh * W;
         float v = 0.0f;
         if (h0 + hh < H)
-            v = c < d_c ? to_f32(qt[((int64_t)r * H + h0 + hh) * d_c + c])
-                        : to_f32(q_pe[((int64_t)r * H + h0 + hh) * d_r + (c - d_c)]);
+            v = c < d_c ? to_f32(qt[((int64_t)r * H + h0 + hh) * qt_ld + c])
+                        : to_f32(q_pe[((int64_t)r * H + h0 + hh) * qpe_ld + (c - d_c)]);
         qs[i] = v;
     }
     float o[MAX_PER_LANE];
@@ -172,21 +173,21 @@ __global__ void __launch_bounds__(HG * 32) mla_simt_kernel(const TQ *__restrict_
 #pragma unroll
     for (int i = 0; i < MAX_PER_LANE; ++i) {
         const int d = lane + 32 * i;
-        if (d < d_c) olat[((int64_t)r * H + h) * d_c + d] = o[i] * inv;
+        if (d < d_c) olat[((int64_t)r * H + h) * d_c + d] = from_f32<TO>(o[i] * inv);
     }
     if (lse && lane == 0) lse[(int64_t)r * H + h] = l > 0.0f ? m + logf(l) : -INFINITY;
 }
 
-template <typename TQ, typename T>
-cudaError_t mla_simt_typed(const void *qt, const void *q_pe, const void *kv, int64_t ld_kv, const void *k_pe,
-                           int64_t ld_pe, const int32_t *idx, int k, const SeqTab &st, dim3 grid, size_t smem, int H,
-                           int d_r, int d_c, float scale, float *olat, float *lse, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(mla_simt_kernel<TQ, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <typename TQ, typename T, typename TO>
+cudaError_t mla_simt_typed(const void *qt, int qt_ld, const void *q_pe, int qpe_ld, const void *kv, int64_t ld_kv,
+                           const void *k_pe, int64_t ld_pe, const int32_t *idx, int k, const SeqTab &st, dim3 grid,
+                           size_t smem, int H, int d_r, int d_c, float scale, void *olat, float *lse, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(mla_simt_kernel<TQ, T, TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    mla_simt_kernel<TQ, T><<<grid, HG * 32, smem, s>>>((const TQ *)qt, (const T *)q_pe, (const T *)kv, ld_kv,
-                                                       (const T *)k_pe, ld_pe, idx, k, st, H, d_r, d_c, scale, olat,
-                                                       lse);
+    mla_simt_kernel<TQ, T, TO><<<grid, HG * 32, smem, s>>>((const TQ *)qt, qt_ld, (const T *)q_pe, qpe_ld,
+                                                           (const T *)kv, ld_kv, (const T *)k_pe, ld_pe, idx, k, st,
+                                                           H, d_r, d_c, scale, (TO *)olat, lse);
     return cudaGetLastError();
 }
 
@@ -211,23 +212,28 @@ cudaError_t launch_absorb_simt(const void *A, int a_dtype, int64_t lda_row, cons
     return e;
 }
 
-cudaError_t launch_mla_simt(const void *qt, int qt_dtype, const void *q_pe, int dtype, const void *kv, int64_t ld_kv,
-                            const void *k_pe, int64_t ld_pe, const int32_t *idx, int k, const SeqTab &st, int total_q,
-                            int H, int d_r, int d_c, float scale, float *olat, float *lse, cudaStream_t s) {
+cudaError_t launch_mla_simt(const void *qt, int qt_dtype, int qt_ld, const void *q_pe, int qpe_ld, int dtype,
+                            const void *kv, int64_t ld_kv, const void *k_pe, int64_t ld_pe, const int32_t *idx, int k,
+                            const SeqTab &st, int total_q, int H, int d_r, int d_c, float scale, void *olat,
+                            int olat_dtype, float *lse, cudaStream_t s) {
     if (total_q == 0) return cudaSuccess;
     dim3 grid(total_q, (H + HG - 1) / HG);
     const int W = d_c + d_r;
     const size_t smem = ((size_t)HG * W + (size_t)KC * (W + 1)) * sizeof(float);
     cudaError_t e;
     if (qt_dtype == DSA_F32 && dtype == DSA_F32)
-        e = mla_simt_typed<float, float>(qt, q_pe, kv, ld_kv, k_pe, ld_pe, idx, k, st, grid, smem, H, d_r, d_c, scale,
-                                         olat, lse, s);
+        e = mla_simt_typed<float, float, float>(qt, qt_ld, q_pe, qpe_ld, kv, ld_kv, k_pe, ld_pe, idx, k, st, grid,
+                                                smem, H, d_r, d_c, scale, olat, lse, s);
     else if (qt_dtype == DSA_F32)
-        e = mla_simt_typed<float, __nv_bfloat16>(qt, q_pe, kv, ld_kv, k_pe, ld_pe, idx, k, st, grid, smem, H, d_r,
-                                                 d_c, scale, olat, lse, s);
+        e = mla_simt_typed<float, __nv_bfloat16, float>(qt, qt_ld, q_pe, qpe_ld, kv, ld_kv, k_pe, ld_pe, idx, k, st,
+                                                        grid, smem, H, d_r, d_c, scale, olat, lse, s);
+    else if (olat_dtype == DSA_BF16)
+        e = mla_simt_typed<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(qt, qt_ld, q_pe, qpe_ld, kv, ld_kv, k_pe,
+                                                                        ld_pe, idx, k, st, grid, smem, H, d_r, d_c,
+                                                                        scale, olat, lse, s);
     else
-        e = mla_simt_typed<__nv_bfloat16, __nv_bfloat16>(qt, q_pe, kv, ld_kv, k_pe, ld_pe, idx, k, st, grid, smem, H,
-                                                         d_r, d_c, scale, olat, lse, s);
+        e = mla_simt_typed<__nv_bfloat16, __nv_bfloat16, float>(qt, qt_ld, q_pe, qpe_ld, kv, ld_kv, k_pe, ld_pe, idx,
+                                                                k, st, grid, smem, H, d_r, d_c, scale, olat, lse, s);
     note_launch(DSA_KERNEL_MLA_SIMT);
     return e;
 }

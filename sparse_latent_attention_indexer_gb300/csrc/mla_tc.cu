@@ -1,0 +1,533 @@
+// Sparse multi-head latent attention in absorbed form on tcgen05 tensor cores.
+//
+// For one query row (all 128 heads) and its selected keys s_j:
+//   z[h,j]   = scale (q~[h] . c[s_j] + q_pe[h] . k_pe[s_j])      (576-wide dot)
+//   P        = online softmax over j (running max, lazily rescaled)
+//   o_lat[h] = sum_j P[h,j] c[s_j]                               (512-wide)
+// (DeepSeek-V3.2-Exp atlas page, MoE transformer block: Q = [Q^C; Q^R],
+// K_i = [K^C_i; k^R], v = c^KV W_UV, M^sel; W_UK folded into q~ beforehand
+// and W_UV applied afterwards.)
+//
+// The 128 x 512 fp32 context alone fills a CTA's tensor memory, so a query
+// row is handled by a cluster of two CTAs on two SMs:
+//   * CTA 0 holds latent columns 0..255, CTA 1 latent 256..511 and the rope
+//     part -- of q~ (resident, loaded once by TMA) and of each gathered key
+//     tile (64 keys, rows fetched with TMA gather4 from the packed cache).
+//   * Each CTA computes a partial score tile S_c = Q_c K_c^T (M = 128 heads,
+//     N = 64 keys) over its columns; the softmax warps swap partial tiles
+//     through distributed shared memory and both add them (in the same
+//     order), so both CTAs hold the identical full score tile.
+//   * Both run the same online softmax (identical decisions), write
+//     P (bf16) to shared memory, and accumulate O_c += P V_c for their own 256
+//     latent columns in tensor memory (N = 256, V read MN-major straight from
+//     the gathered tile).
+// The running maximum is only moved (and O rescaled in tensor memory) when
+// a tile's maximum exceeds it by more than 2^8, which after the first tiles
+// almost never happens.  Key tiles are double-buffered in shared memory and
+// score tiles in tensor memory, so the QK^T of tile i+1 overlaps the
+// softmax of tile i.  Waits are bounded; a timeout records its site in the
+// device error word and both CTAs drain and exit.
+//
+// Long rows can be split across several clusters (decode: few rows, many
+// keys); each split writes a normalised partial context and its lse, and a
+// small combine kernel merges them.
+#include "tc_common.cuh"
+
+namespace dsa {
+
+__device__ int g_mla_tc_error = 0;
+
+namespace {
+
+constexpr int NH = 128;                      // heads (MMA M)
+constexpr int DC = 512;                      // latent width
+constexpr int QW = 576;                      // q~ row: [q~ (512) | q_pe (64)]
+constexpr int BK = 64;                       // keys per tile (MMA N of QK^T, K of PV)
+constexpr int NSLAB_MAX = 5;                 // 64-column slabs per CTA (CTA 1: 4 latent + rope)
+constexpr int SLAB_Q = NH * 128;             // 16 KB
+constexpr int SLAB_K = BK * 128;             // 8 KB
+constexpr int KV_STAGE = NSLAB_MAX * SLAB_K; // 40 KB
+constexpr int NSTAGE = 2;
+constexpr int Q_BYTES = NSLAB_MAX * SLAB_Q;  // 80 KB
+constexpr int P_BYTES = NH * 128;            // 16 KB: [128 heads][64 keys] bf16
+constexpr int X_BYTES = NH * BK * 4;         // 32 KB: the peer's partial scores
+constexpr int SMEM = 1024 + Q_BYTES + NSTAGE * KV_STAGE + P_BYTES + X_BYTES + NSTAGE * BK + 256;
+constexpr int NUM_THREADS = 256;             // warps 0-3: TMA, MMA, TMEM; warps 4-7: softmax
+constexpr uint32_t IDESC_QK = tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, NH, BK, 0, 0);
+constexpr uint32_t IDESC_PV = tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, NH, 256, 0, 1);
+constexpr float RESCALE_LOG2 = 8.0f;
+constexpr float LN2 = 0.69314718055994530942f;
+
+struct MlaParams {
+    int B;
+    int q_off[DSA_MAX_SEQS + 1];
+    int k_base[DSA_MAX_SEQS];
+    int k_len[DSA_MAX_SEQS];
+    int start_pos[DSA_MAX_SEQS];
+    int total_q;
+    int k;             // entries per selection row
+    int splits;        // clusters per row
+    int prefix_valid;  // rows list their min(k, p+1) keys first (the top-k output)
+    float scale_log2;  // softmax scale * log2(e)
+};
+
+__device__ __forceinline__ int find_seq(const MlaParams &P, int r) {
+    int lo = 0, hi = P.B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (P.q_off[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+struct Bars {
+    uint64_t q_full, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_empty[2], p_full, p_empty, xfull, xempty,
+        o_done;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
+                  const __grid_constant__ CUtensorMap tm_pe, const int32_t *__restrict__ idx,
+                  const __grid_constant__ MlaParams P, __nv_bfloat16 *__restrict__ olat, float *__restrict__ lse,
+                  float *__restrict__ opart, float *__restrict__ lpart) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *Qs = base;
+    uint8_t *KV = Qs + Q_BYTES;
+    uint8_t *Ps = KV + NSTAGE * KV_STAGE;
+    float *X = (float *)(Ps + P_BYTES);
+    uint8_t *kvalid = (uint8_t *)X + X_BYTES;          // [NSTAGE][BK]
+    Bars *bar = (Bars *)(kvalid + NSTAGE * BK);
+    uint32_t *tmem_slot = (uint32_t *)(bar + 1);
+    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+    __shared__ int never;
+    volatile int *nv = (volatile int *)&never;
+    int *err = &g_mla_tc_error;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_rank(), peer = rank ^ 1u;
+    const int nslab = rank ? 5 : 4, gslab0 = rank ? 4 : 0;
+
+    // Work item: heavier rows (later positions) first.
+    const int w = (int)(gridDim.x / 2) - 1 - (int)(blockIdx.x / 2);
+    const int r = w / P.splits, split = w % P.splits;
+    const int b = find_seq(P, r);
+    const int p = P.start_pos[b] + (r - P.q_off[b]);
+    const int S = P.k_len[b], kbase = P.k_base[b];
+    const int len = P.prefix_valid ? min(P.k, p + 1) : P.k;
+    const int per = (len + P.splits - 1) / P.splits;
+    const int chunk = (per + BK - 1) / BK * BK;
+    const int e0 = split * chunk, e1 = min(len, e0 + chunk);
+    const int n = e1 > e0 ? (e1 - e0 + BK - 1) / BK : 0;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar->q_full, 1);
+        for (int i = 0; i < NSTAGE; ++i) {
+            tc::mbar_init(&bar->kv_full[i], 16);
+            tc::mbar_init(&bar->kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&bar->s_full[i], 1);
+            tc::mbar_init(&bar->s_empty[i], 4);
+        }
+        tc::mbar_init(&bar->p_full, 4);
+        tc::mbar_init(&bar->p_empty, 1);
+        tc::mbar_init(&bar->xfull, NH);
+        tc::mbar_init(&bar->xempty, NH);
+        tc::mbar_init(&bar->o_done, 1);
+        *abort_flag = 0;
+        never = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 2) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    tc::cluster_sync();  // both CTAs' barriers exist before any remote arrive
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_o = tmem + 256;
+
+    if (warp == 0 && n > 0) {
+        // ---------------- producer: q~ once, then key tiles by gather4 ----------------
+        if (lane == 0) {
+            tc::prefetch_tmap(&tm_q);
+            tc::prefetch_tmap(&tm_c);
+            tc::prefetch_tmap(&tm_pe);
+            tc::mbar_arrive_expect_tx(&bar->q_full, nslab * SLAB_Q);
+            for (int j = 0; j < nslab; ++j) tc::tma_load_2d(Qs + j * SLAB_Q, &tm_q, &bar->q_full, (gslab0 + j) * 64, r * NH);
+        }
+        int issued = 0;
+        if (lane < 16) {
+            const int32_t *row_idx = idx + (int64_t)r * P.k;
+            const int last = min(p, S - 1);
+            for (int i = 0; i < n; ++i) {
+                const int st = i % NSTAGE;
+                if (!tc::mbar_wait(&bar->kv_empty[st], ((i / NSTAGE) & 1) ^ 1, abort_flag, err, 21)) break;
+                int rows[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int e = e0 + i * BK + 4 * lane + u;
+                    const int s = e < e1 ? row_idx[e] : -1;
+                    const bool ok = s >= 0 && s <= last;
+                    rows[u] = kbase + (ok ? s : 0);
+                    kvalid[st * BK + 4 * lane + u] = ok ? 1 : 0;
+                }
+                tc::mbar_arrive_expect_tx(&bar->kv_full[st], nslab * 4 * 128);
+                uint8_t *dst = KV + st * KV_STAGE + lane * 4 * 128;
+                for (int j = 0; j < nslab; ++j) {
+                    const int g = gslab0 + j;
+                    if (g < 8) tc::tma_gather4(dst + j * SLAB_K, &tm_c, &bar->kv_full[st], g * 64, rows[0], rows[1], rows[2], rows[3]);
+                    else tc::tma_gather4(dst + j * SLAB_K, &tm_pe, &bar->kv_full[st], 0, rows[0], rows[1], rows[2], rows[3]);
+                }
+                ++issued;
+            }
+            // Drain: every load of this CTA has landed before it may exit.
+            if (lane == 0) tc::mbar_wait(&bar->q_full, 0, nv, err, 22);
+            for (int j = max(0, issued - NSTAGE); j < issued; ++j)
+                tc::mbar_wait(&bar->kv_full[j % NSTAGE], (j / NSTAGE) & 1, nv, err, 23);
+        }
+    } else if (warp == 1 && lane == 0 && n > 0) {
+        // ---------------- MMA issuer ----------------
+        bool ok = tc::mbar_wait(&bar->q_full, 0, abort_flag, err, 24);
+        const uint32_t q0 = tc::smem_u32(Qs), kv0 = tc::smem_u32(KV), p0s = tc::smem_u32(Ps);
+        auto issue_qk = [&](int j) -> bool {
+            const int st = j % NSTAGE, sb = j & 1;
+            if (!tc::mbar_wait(&bar->kv_full[st], (j / NSTAGE) & 1, abort_flag, err, 25)) return false;
+            if (!tc::mbar_wait(&bar->s_empty[sb], ((j >> 1) & 1) ^ 1, abort_flag, err, 26)) return false;
+            tc::tc_fence_after();
+            for (int js = 0; js < nslab; ++js)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = tc::smem_desc(q0 + js * SLAB_Q + kk * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc(kv0 + st * KV_STAGE + js * SLAB_K + kk * 32, 16, 1024);
+                    tc::mma_f16(tmem + sb * BK, ad, bd, IDESC_QK, (js | kk) != 0);
+                }
+            tc::mma_commit(&bar->s_full[sb]);
+            return true;
+        };
+        if (ok) ok = issue_qk(0);
+        int pv = 0;
+        for (int i = 0; ok && i < n; ++i) {
+            if (i + 1 < n && !(ok = issue_qk(i + 1))) break;
+            if (!(ok = tc::mbar_wait(&bar->p_full, i & 1, abort_flag, err, 27))) break;
+            tc::tc_fence_after();
+            const int st = i % NSTAGE;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = tc::smem_desc(p0s + kk * 32, 16, 1024);
+                // V: MN-major view of latent slabs 0..3 of the tile (LBO = slab stride, SBO = 8 keys).
+                const uint64_t bd = tc::smem_desc(kv0 + st * KV_STAGE + kk * 16 * 128, SLAB_K, 1024);
+                tc::mma_f16(tmem_o, ad, bd, IDESC_PV, (i | kk) != 0);
+            }
+            tc::mma_commit(&bar->kv_empty[st]);
+            tc::mma_commit(&bar->p_empty);
+            ++pv;
+        }
+        tc::mma_commit(&bar->o_done);
+        tc::mbar_wait(&bar->o_done, 0, nv, err, 28);
+    } else if (warp >= 4) {
+        // ---------------- softmax (one thread per head = TMEM lane) ----------------
+        const int q = warp & 3, h = q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const uint32_t x_row = tc::smem_u32(X) + h * 256;
+        const uint32_t peer_x_row = tc::map_peer(x_row, peer);
+        const uint32_t peer_xfull = tc::map_peer(tc::smem_u32(&bar->xfull), peer);
+        const uint32_t peer_xempty = tc::map_peer(tc::smem_u32(&bar->xempty), peer);
+        float m_used = -INFINITY, l = 0.0f;
+        bool done_ok = true;
+        for (int i = 0; i < n; ++i) {
+            const int sb = i & 1, st = i % NSTAGE;
+            if (!tc::mbar_wait(&bar->s_full[sb], (i >> 1) & 1, abort_flag, err, 31)) { done_ok = false; break; }
+            tc::tc_fence_after();
+            float v[64];
+            {
+                float a[32], c[32];
+                tc::tmem_ld32(tmem + lane_off + sb * BK, a);
+                tc::tmem_ld32(tmem + lane_off + sb * BK + 32, c);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    v[j] = a[j];
+                    v[32 + j] = c[j];
+                }
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bar->s_empty[sb]);
+            // swap partial scores with the peer CTA
+            if (i > 0 && !tc::mbar_wait(&bar->xempty, (i - 1) & 1, abort_flag, err, 32)) { done_ok = false; break; }
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                tc::st_cluster_v4(peer_x_row + ((c ^ (h & 15)) << 4),
+                                  make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+            tc::mbar_arrive_cluster(peer_xfull);
+            if (!tc::mbar_wait_cluster(&bar->xfull, i & 1, abort_flag, err, 33)) { done_ok = false; break; }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const float4 x = *(const float4 *)((const uint8_t *)X + h * 256 + ((c ^ (h & 15)) << 4));
+                v[4 * c] += x.x;
+                v[4 * c + 1] += x.y;
+                v[4 * c + 2] += x.z;
+                v[4 * c + 3] += x.w;
+            }
+            tc::mbar_arrive_cluster(peer_xempty);
+            // mask (selection entries that are padding, future or outside the sequence)
+            if (!tc::mbar_wait(&bar->kv_full[st], (i / NSTAGE) & 1, abort_flag, err, 34)) { done_ok = false; break; }
+            float mt = -INFINITY;
+            {
+                const uint32_t *kvw = (const uint32_t *)(kvalid + st * BK);
+#pragma unroll
+                for (int wd = 0; wd < 16; ++wd) {
+                    const uint32_t bits = kvw[wd];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int j = 4 * wd + u;
+                        v[j] = ((bits >> (8 * u)) & 0xffu) ? v[j] * P.scale_log2 : -INFINITY;
+                        mt = fmaxf(mt, v[j]);
+                    }
+                }
+            }
+            bool rescale = false;
+            float alpha = 1.0f;
+            if (mt != -INFINITY) {
+                if (m_used == -INFINITY) {
+                    m_used = mt;
+                } else if (mt > m_used + RESCALE_LOG2) {
+                    alpha = exp2f(m_used - mt);
+                    l *= alpha;
+                    m_used = mt;
+                    rescale = true;
+                }
+            }
+            uint32_t pk[32];
+            float psum = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = v[2 * j] == -INFINITY ? 0.0f : exp2f(v[2 * j] - m_used);
+                const float p1 = v[2 * j + 1] == -INFINITY ? 0.0f : exp2f(v[2 * j + 1] - m_used);
+                const __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
+                psum += __low2float(t2) + __high2float(t2);
+                pk[j] = *(const uint32_t *)&t2;
+            }
+            l += psum;
+            if (i > 0 && !tc::mbar_wait(&bar->p_empty, (i - 1) & 1, abort_flag, err, 35)) { done_ok = false; break; }
+            // tcgen05.ld/st are warp-wide: rescale the whole warp's rows when any row needs it
+            // (rows that do not keep alpha = 1).
+            if (__any_sync(0xffffffffu, rescale)) {
+                tc::tc_fence_after();
+#pragma unroll 1
+                for (int cc = 0; cc < 8; ++cc) {
+                    float o[32];
+                    uint32_t ob[32];
+                    tc::tmem_ld32(tmem_o + lane_off + cc * 32, o);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ob[j] = __float_as_uint(o[j] * alpha);
+                    tc::tmem_st32(tmem_o + lane_off + cc * 32, ob);
+                }
+                tc::tmem_st_wait();
+            }
+            // P row h: 64 bf16 = 128 bytes in the 128-byte-swizzled K-major layout
+            uint8_t *prow = Ps + h * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *(uint4 *)(prow + ((c ^ (h & 7)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bar->p_full);
+        }
+        // ---------------- epilogue: normalise and store this CTA's 256 columns ----------------
+        const int64_t rh = (int64_t)r * NH + h;
+        const bool have = __all_sync(0xffffffffu, n > 0 && done_ok && tc::mbar_wait(&bar->o_done, 0, abort_flag, err, 36));
+        const float inv = (have && l > 0.0f) ? 1.0f / l : 0.0f;
+        const float row_lse = (have && l > 0.0f) ? (m_used + log2f(l)) * LN2 : -INFINITY;
+        if (have) tc::tc_fence_after();
+        if (P.splits == 1) {
+            __nv_bfloat16 *dst = olat + rh * DC + rank * 256;
+#pragma unroll 1
+            for (int cc = 0; cc < 8; ++cc) {
+                float o[32];
+                if (have) {
+                    tc::tmem_ld32(tmem_o + lane_off + cc * 32, o);
+                    tc::tmem_ld_wait();
+                }
+                uint32_t pw[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const __nv_bfloat162 t2 = have ? __floats2bfloat162_rn(o[2 * e] * inv, o[2 * e + 1] * inv)
+                                                   : __floats2bfloat162_rn(0.0f, 0.0f);
+                    pw[e] = *(const uint32_t *)&t2;
+                }
+                uint4 *d4 = (uint4 *)(dst + cc * 32);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pw[4 * e], pw[4 * e + 1], pw[4 * e + 2], pw[4 * e + 3]);
+            }
+            if (rank == 0 && lse) lse[rh] = row_lse;
+        } else {
+            const int64_t part = ((int64_t)r * P.splits + split) * NH + h;
+            float *dst = opart + part * DC + rank * 256;
+#pragma unroll 1
+            for (int cc = 0; cc < 8; ++cc) {
+                float o[32];
+                if (have) {
+                    tc::tmem_ld32(tmem_o + lane_off + cc * 32, o);
+                    tc::tmem_ld_wait();
+                }
+                float4 *d4 = (float4 *)(dst + cc * 32);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    d4[e] = have ? make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv)
+                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+            if (rank == 0) lpart[part] = row_lse;
+        }
+    }
+    __syncthreads();
+    tc::cluster_sync();  // no DSMEM traffic may target a CTA that has exited
+    if (warp == 2) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// Merge the normalised partial contexts of the splits of one row:
+// lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.  One warp per (row, head).
+__global__ void __launch_bounds__(256) mla_combine_kernel(const float *__restrict__ opart,
+                                                          const float *__restrict__ lpart, int M, int splits,
+                                                          __nv_bfloat16 *__restrict__ olat, float *__restrict__ lse) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rh = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (rh >= (int64_t)M * NH) return;
+    const int64_t r = rh / NH, h = rh % NH;
+    float mx = -INFINITY;
+    for (int s = 0; s < splits; ++s) mx = fmaxf(mx, lpart[(r * splits + s) * NH + h]);
+    float wsum = 0.0f;
+    for (int s = 0; s < splits; ++s) {
+        const float ls = lpart[(r * splits + s) * NH + h];
+        wsum += ls == -INFINITY ? 0.0f : expf(ls - mx);
+    }
+    const float tot = wsum > 0.0f ? mx + logf(wsum) : -INFINITY;
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+    for (int s = 0; s < splits; ++s) {
+        const float ls = lpart[(r * splits + s) * NH + h];
+        if (ls == -INFINITY) continue;
+        const float wgt = expf(ls - tot);
+        const float4 *src = (const float4 *)(opart + ((r * splits + s) * NH + h) * DC) + lane * 4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 x = src[j];
+            acc[4 * j] += wgt * x.x;
+            acc[4 * j + 1] += wgt * x.y;
+            acc[4 * j + 2] += wgt * x.z;
+            acc[4 * j + 3] += wgt * x.w;
+        }
+    }
+    uint32_t pw[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const __nv_bfloat162 t2 = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+        pw[e] = *(const uint32_t *)&t2;
+    }
+    uint4 *dst = (uint4 *)(olat + rh * DC + lane * 16);
+    dst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+    dst[1] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+    if (lse && lane == 0) lse[rh] = tot;
+}
+
+}  // namespace
+
+bool mla_tc_supported(int dtype, int H, int d_n, int d_r, int d_c, int d_v) {
+    return dtype == DSA_BF16 && H == NH && d_n == 128 && d_r == 64 && d_c == DC && d_v == 128;
+}
+
+// Clusters per row: enough rows fill the GPU on their own; a few long rows
+// (decode) are split so that about two clusters per SM pair run.
+int mla_tc_splits(int M) {
+    if (M >= 152) return 1;
+    const int want = (152 + M - 1) / M;
+    int s = 1;
+    while (s < want && s < 8) s *= 2;
+    return s;
+}
+
+size_t mla_tc_partial_bytes(int M) {
+    const int s = mla_tc_splits(M);
+    if (s == 1) return 0;
+    return (size_t)M * s * NH * DC * sizeof(float) + 256 + (size_t)M * s * NH * sizeof(float);
+}
+
+cudaError_t launch_mla_tc(const void *qt, const void *kv, int64_t ld_kv, const void *kpe, int64_t ld_pe,
+                          const int32_t *idx, int k, const SeqTab &st, int64_t total_k, int M, float scale,
+                          bool prefix_valid, void *olat, float *lse, void *part_ws, cudaStream_t s) {
+    if (M == 0) return cudaSuccess;
+    static thread_local MlaParams P;
+    P.B = st.B;
+    for (int i = 0; i < st.B; ++i) {
+        P.q_off[i] = st.q_off[i];
+        P.k_base[i] = st.k_base[i];
+        P.k_len[i] = st.k_len[i];
+        P.start_pos[i] = st.start_pos[i];
+    }
+    P.q_off[st.B] = st.q_off[st.B];
+    P.total_q = M;
+    P.k = k;
+    P.splits = mla_tc_splits(M);
+    P.prefix_valid = prefix_valid ? 1 : 0;
+    P.scale_log2 = scale * 1.4426950408889634f;
+    CUtensorMap tq, tcm, tpe;
+    {
+        uint64_t dims[2] = {(uint64_t)QW, (uint64_t)M * NH};
+        uint64_t strides[1] = {(uint64_t)QW * 2};
+        uint32_t box[2] = {64, (uint32_t)NH};
+        if (!make_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qt, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        uint64_t dims[2] = {(uint64_t)DC, (uint64_t)std::max<int64_t>(total_k, 1)};
+        uint64_t strides[1] = {(uint64_t)ld_kv * 2};
+        uint32_t box[2] = {64, 1};
+        if (!make_tmap(&tcm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        uint64_t dims[2] = {64, (uint64_t)std::max<int64_t>(total_k, 1)};
+        uint64_t strides[1] = {(uint64_t)ld_pe * 2};
+        uint32_t box[2] = {64, 1};
+        if (!make_tmap(&tpe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kpe, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    float *opart = nullptr, *lpart = nullptr;
+    if (P.splits > 1) {
+        opart = (float *)part_ws;
+        lpart = (float *)((char *)part_ws + (((size_t)M * P.splits * NH * DC * sizeof(float) + 255) / 256) * 256);
+    }
+    cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)M * P.splits * 2;
+    mla_tc_kernel<<<grid, NUM_THREADS, SMEM, s>>>(tq, tcm, tpe, idx, P, (__nv_bfloat16 *)olat, lse, opart, lpart);
+    note_launch(DSA_KERNEL_MLA_TC);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || P.splits == 1) return e;
+    const unsigned cgrid = (unsigned)(((int64_t)M * NH + 7) / 8);
+    mla_combine_kernel<<<cgrid, 256, 0, s>>>(opart, lpart, M, P.splits, (__nv_bfloat16 *)olat, lse);
+    note_launch(DSA_KERNEL_COMBINE);
+    return cudaGetLastError();
+}
+
+int mla_tc_read_error(int *site) {
+    int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_mla_tc_error, sizeof(int));
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (v) {
+        e = cudaMemcpyToSymbol(g_mla_tc_error, &zero, sizeof(int));
+        if (e != cudaSuccess) return fail_cuda(e);
+        if (site) *site = v;
+        return DSA_ERR_TIMEOUT;
+    }
+    return DSA_OK;
+}
+
+}  // namespace dsa

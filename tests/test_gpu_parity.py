@@ -268,3 +268,22 @@ def test_indexer_tensor_core_matches_generic(name, monkeypatch):
         fin = np.isfinite(y)
         scale = np.abs(y[fin]).max() if fin.any() else 1.0
         assert np.abs(x[fin] - y[fin]).max() <= 1e-5 * scale
+
+
+@pytest.mark.parametrize("name", ["bf16-ragged", "bf16-k64"])
+def test_attention_stage_tensor_core_matches_generic(name, monkeypatch):
+    """The tensor-core attention stage (tcgen05 absorption GEMMs, bf16 q~ and
+    latent context) against the generic fp32 stage on the same selection:
+    equal within the bf16 output tolerance."""
+    wl, t = case(name)
+    sh = wl.shape
+    sel = di.random_selection(wl, seed=37, density=0.8).cuda()
+    args = (t["q_nope"], t["q_pe"], t["ckv"], t["kpe"], t["W_UK"], t["W_UV"], sel, H.seqs_of(wl), sh.softmax_scale)
+    fast, lf = dsa.dsa_sparse_mla_fwd(*args)
+    assert "absorb_tc" in dsa.last_kernels(), dsa.last_kernels()
+    monkeypatch.setenv("DSA_FORCE_GENERIC", "1")
+    gen, lg = dsa.dsa_sparse_mla_fwd(*args)
+    assert "absorb_simt" in dsa.last_kernels()
+    monkeypatch.delenv("DSA_FORCE_GENERIC")
+    assert (fast.float() - gen.float()).abs().max().item() <= H.OUT_ATOL_BF16
+    assert (lf - lg).abs().max().item() <= 5e-3
