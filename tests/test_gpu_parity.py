@@ -280,7 +280,7 @@ def test_attention_stage_tensor_core_matches_generic(name, monkeypatch):
     sel = di.random_selection(wl, seed=37, density=0.8).cuda()
     args = (t["q_nope"], t["q_pe"], t["ckv"], t["kpe"], t["W_UK"], t["W_UV"], sel, H.seqs_of(wl), sh.softmax_scale)
     fast, lf = dsa.dsa_sparse_mla_fwd(*args)
-    assert "absorb_tc" in dsa.last_kernels(), dsa.last_kernels()
+    assert {"absorb_tc", "mla_tc"} <= dsa.last_kernels(), dsa.last_kernels()
     monkeypatch.setenv("DSA_FORCE_GENERIC", "1")
     gen, lg = dsa.dsa_sparse_mla_fwd(*args)
     assert "absorb_simt" in dsa.last_kernels()
