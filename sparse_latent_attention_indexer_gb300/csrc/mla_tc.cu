@@ -44,15 +44,15 @@ constexpr int DC = 512;                      // latent width
 constexpr int QW = 576;                      // q~ row: [q~ (512) | q_pe (64)]
 constexpr int BK = 64;                       // keys per tile (MMA N of QK^T, K of PV)
 constexpr int NSLAB_MAX = 5;                 // 64-column slabs per CTA (CTA 1: 4 latent + rope)
-constexpr int SLAB_Q = NH * 128;             // 16 KB
-constexpr int SLAB_K = BK * 128;             // 8 KB
+constexpr int SLAB_K = BK * 128;             // 8 KB: 64 keys x 64 columns, 128-byte swizzle
 constexpr int KV_STAGE = NSLAB_MAX * SLAB_K; // 40 KB
-constexpr int NSTAGE = 2;
-constexpr int Q_BYTES = NSLAB_MAX * SLAB_Q;  // 80 KB
-constexpr int P_BYTES = NH * 128;            // 16 KB: [128 heads][64 keys] bf16
+constexpr int NSTAGE = 4;
 constexpr int X_BYTES = NH * BK * 4;         // 32 KB: the peer's partial scores
-constexpr int SMEM = 1024 + Q_BYTES + NSTAGE * KV_STAGE + P_BYTES + X_BYTES + NSTAGE * BK + 256;
+constexpr int SMEM = 1024 + NSTAGE * KV_STAGE + X_BYTES + NSTAGE * BK + 256;
 constexpr int NUM_THREADS = 256;             // warps 0-3: TMA, MMA, TMEM; warps 4-7: softmax
+// Tensor-memory columns (512 per CTA): scores, probabilities (bf16 pairs),
+// the resident q~ slice (bf16 pairs, A operand of QK^T) and the context.
+constexpr uint32_t COL_S = 0, COL_P = 64, COL_Q = 96, COL_O = 256;
 constexpr uint32_t IDESC_QK = tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, NH, BK, 0, 0);
 constexpr uint32_t IDESC_PV = tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, NH, 256, 0, 1);
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -81,22 +81,19 @@ __device__ __forceinline__ int find_seq(const MlaParams &P, int r) {
 }
 
 struct Bars {
-    uint64_t q_full, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_empty[2], p_full, p_empty, xfull, xempty,
-        o_done;
+    uint64_t q_ready, kv_full[NSTAGE], kv_empty[NSTAGE], s_full, s_empty, p_full, p_empty, xfull, xempty, o_done;
 };
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
-                  const __grid_constant__ CUtensorMap tm_pe, const int32_t *__restrict__ idx,
+    mla_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_pe,
+                  const __nv_bfloat16 *__restrict__ qt, const int32_t *__restrict__ idx,
                   const __grid_constant__ MlaParams P, __nv_bfloat16 *__restrict__ olat, float *__restrict__ lse,
                   float *__restrict__ opart, float *__restrict__ lpart) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *Qs = base;
-    uint8_t *KV = Qs + Q_BYTES;
-    uint8_t *Ps = KV + NSTAGE * KV_STAGE;
-    float *X = (float *)(Ps + P_BYTES);
-    uint8_t *kvalid = (uint8_t *)X + X_BYTES;          // [NSTAGE][BK]
+    uint8_t *KV = base;
+    float *X = (float *)(KV + NSTAGE * KV_STAGE);
+    uint8_t *kvalid = (uint8_t *)X + X_BYTES;  // [NSTAGE][BK]
     Bars *bar = (Bars *)(kvalid + NSTAGE * BK);
     uint32_t *tmem_slot = (uint32_t *)(bar + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
@@ -121,19 +118,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int n = e1 > e0 ? (e1 - e0 + BK - 1) / BK : 0;
 
     if (threadIdx.x == 0) {
-        tc::mbar_init(&bar->q_full, 1);
+        tc::mbar_init(&bar->q_ready, 4);
         for (int i = 0; i < NSTAGE; ++i) {
             tc::mbar_init(&bar->kv_full[i], 16);
             tc::mbar_init(&bar->kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&bar->s_full[i], 1);
-            tc::mbar_init(&bar->s_empty[i], 4);
-        }
+        tc::mbar_init(&bar->s_full, 1);
+        tc::mbar_init(&bar->s_empty, 4);
         tc::mbar_init(&bar->p_full, 4);
         tc::mbar_init(&bar->p_empty, 1);
-        tc::mbar_init(&bar->xfull, NH);
-        tc::mbar_init(&bar->xempty, NH);
+        tc::mbar_init(&bar->xfull, 1);   // armed locally with the 32 KB the peer sends
+        tc::mbar_init(&bar->xempty, 4);  // one arrival per peer softmax warp
         tc::mbar_init(&bar->o_done, 1);
         *abort_flag = 0;
         never = 0;
@@ -148,68 +143,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tc::tc_fence_after();
     tc::cluster_sync();  // both CTAs' barriers exist before any remote arrive
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o = tmem + 256;
 
     if (warp == 0 && n > 0) {
-        // ---------------- producer: q~ once, then key tiles by gather4 ----------------
+        // ---------------- producer: key tiles by TMA gather4 ----------------
         if (lane == 0) {
-            tc::prefetch_tmap(&tm_q);
             tc::prefetch_tmap(&tm_c);
             tc::prefetch_tmap(&tm_pe);
-            tc::mbar_arrive_expect_tx(&bar->q_full, nslab * SLAB_Q);
-            for (int j = 0; j < nslab; ++j) tc::tma_load_2d(Qs + j * SLAB_Q, &tm_q, &bar->q_full, (gslab0 + j) * 64, r * NH);
         }
         int issued = 0;
         if (lane < 16) {
             const int32_t *row_idx = idx + (int64_t)r * P.k;
             const int last = min(p, S - 1);
-            for (int i = 0; i < n; ++i) {
-                const int st = i % NSTAGE;
-                if (!tc::mbar_wait(&bar->kv_empty[st], ((i / NSTAGE) & 1) ^ 1, abort_flag, err, 21)) break;
-                int rows[4];
+            int rows[4];
+            uint32_t ok4 = 0;
+            auto fetch = [&](int i) {  // the 4 cache rows this lane gathers for tile i
+                ok4 = 0;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int e = e0 + i * BK + 4 * lane + u;
-                    const int s = e < e1 ? row_idx[e] : -1;
+                    const int s = e < e1 ? __ldg(row_idx + e) : -1;
                     const bool ok = s >= 0 && s <= last;
                     rows[u] = kbase + (ok ? s : 0);
-                    kvalid[st * BK + 4 * lane + u] = ok ? 1 : 0;
+                    ok4 |= (ok ? 1u : 0u) << (8 * u);
                 }
+            };
+            fetch(0);
+            for (int i = 0; i < n; ++i) {
+                const int st = i % NSTAGE;
+                if (!tc::mbar_wait(&bar->kv_empty[st], ((i / NSTAGE) & 1) ^ 1, abort_flag, err, 21)) break;
+                *(uint32_t *)(kvalid + st * BK + 4 * lane) = ok4;
                 tc::mbar_arrive_expect_tx(&bar->kv_full[st], nslab * 4 * 128);
                 uint8_t *dst = KV + st * KV_STAGE + lane * 4 * 128;
                 for (int j = 0; j < nslab; ++j) {
                     const int g = gslab0 + j;
-                    if (g < 8) tc::tma_gather4(dst + j * SLAB_K, &tm_c, &bar->kv_full[st], g * 64, rows[0], rows[1], rows[2], rows[3]);
-                    else tc::tma_gather4(dst + j * SLAB_K, &tm_pe, &bar->kv_full[st], 0, rows[0], rows[1], rows[2], rows[3]);
+                    if (g < 8)
+                        tc::tma_gather4(dst + j * SLAB_K, &tm_c, &bar->kv_full[st], g * 64, rows[0], rows[1], rows[2],
+                                        rows[3]);
+                    else
+                        tc::tma_gather4(dst + j * SLAB_K, &tm_pe, &bar->kv_full[st], 0, rows[0], rows[1], rows[2],
+                                        rows[3]);
                 }
                 ++issued;
+                if (i + 1 < n) fetch(i + 1);  // overlaps the wait for the next free stage
             }
             // Drain: every load of this CTA has landed before it may exit.
-            if (lane == 0) tc::mbar_wait(&bar->q_full, 0, nv, err, 22);
             for (int j = max(0, issued - NSTAGE); j < issued; ++j)
                 tc::mbar_wait(&bar->kv_full[j % NSTAGE], (j / NSTAGE) & 1, nv, err, 23);
         }
     } else if (warp == 1 && lane == 0 && n > 0) {
         // ---------------- MMA issuer ----------------
-        bool ok = tc::mbar_wait(&bar->q_full, 0, abort_flag, err, 24);
-        const uint32_t q0 = tc::smem_u32(Qs), kv0 = tc::smem_u32(KV), p0s = tc::smem_u32(Ps);
+        bool ok = tc::mbar_wait(&bar->q_ready, 0, abort_flag, err, 24);
+        const uint32_t kv0 = tc::smem_u32(KV);
         auto issue_qk = [&](int j) -> bool {
-            const int st = j % NSTAGE, sb = j & 1;
+            const int st = j % NSTAGE;
             if (!tc::mbar_wait(&bar->kv_full[st], (j / NSTAGE) & 1, abort_flag, err, 25)) return false;
-            if (!tc::mbar_wait(&bar->s_empty[sb], ((j >> 1) & 1) ^ 1, abort_flag, err, 26)) return false;
+            if (!tc::mbar_wait(&bar->s_empty, (j & 1) ^ 1, abort_flag, err, 26)) return false;
             tc::tc_fence_after();
             for (int js = 0; js < nslab; ++js)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = tc::smem_desc(q0 + js * SLAB_Q + kk * 32, 16, 1024);
                     const uint64_t bd = tc::smem_desc(kv0 + st * KV_STAGE + js * SLAB_K + kk * 32, 16, 1024);
-                    tc::mma_f16(tmem + sb * BK, ad, bd, IDESC_QK, (js | kk) != 0);
+                    tc::mma_f16_ts(tmem + COL_S, tmem + COL_Q + js * 32 + kk * 8, bd, IDESC_QK, (js | kk) != 0);
                 }
-            tc::mma_commit(&bar->s_full[sb]);
+            tc::mma_commit(&bar->s_full);
             return true;
         };
         if (ok) ok = issue_qk(0);
-        int pv = 0;
         for (int i = 0; ok && i < n; ++i) {
             if (i + 1 < n && !(ok = issue_qk(i + 1))) break;
             if (!(ok = tc::mbar_wait(&bar->p_full, i & 1, abort_flag, err, 27))) break;
@@ -217,14 +216,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const int st = i % NSTAGE;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = tc::smem_desc(p0s + kk * 32, 16, 1024);
                 // V: MN-major view of latent slabs 0..3 of the tile (LBO = slab stride, SBO = 8 keys).
                 const uint64_t bd = tc::smem_desc(kv0 + st * KV_STAGE + kk * 16 * 128, SLAB_K, 1024);
-                tc::mma_f16(tmem_o, ad, bd, IDESC_PV, (i | kk) != 0);
+                tc::mma_f16_ts(tmem + COL_O, tmem + COL_P + kk * 8, bd, IDESC_PV, (i | kk) != 0);
             }
             tc::mma_commit(&bar->kv_empty[st]);
             tc::mma_commit(&bar->p_empty);
-            ++pv;
         }
         tc::mma_commit(&bar->o_done);
         tc::mbar_wait(&bar->o_done, 0, nv, err, 28);
@@ -232,21 +229,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         // ---------------- softmax (one thread per head = TMEM lane) ----------------
         const int q = warp & 3, h = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const uint32_t x_row = tc::smem_u32(X) + h * 256;
-        const uint32_t peer_x_row = tc::map_peer(x_row, peer);
+        const uint32_t peer_x_row = tc::map_peer(tc::smem_u32(X) + h * 256, peer);
         const uint32_t peer_xfull = tc::map_peer(tc::smem_u32(&bar->xfull), peer);
         const uint32_t peer_xempty = tc::map_peer(tc::smem_u32(&bar->xempty), peer);
         float m_used = -INFINITY, l = 0.0f;
         bool done_ok = true;
+        if (n > 0) {
+            // This CTA's slice of the head's q~ row -> tensor memory (A operand of QK^T).
+            const uint4 *src = (const uint4 *)(qt + ((int64_t)r * NH + h) * QW + gslab0 * 64);
+            for (int js = 0; js < nslab; ++js) {
+                uint32_t qv[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint4 t4 = __ldg(src + js * 8 + e);
+                    qv[4 * e] = t4.x;
+                    qv[4 * e + 1] = t4.y;
+                    qv[4 * e + 2] = t4.z;
+                    qv[4 * e + 3] = t4.w;
+                }
+                tc::tmem_st32(tmem + lane_off + COL_Q + js * 32, qv);
+            }
+            tc::tmem_st_wait();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bar->q_ready);
+        }
         for (int i = 0; i < n; ++i) {
-            const int sb = i & 1, st = i % NSTAGE;
-            if (!tc::mbar_wait(&bar->s_full[sb], (i >> 1) & 1, abort_flag, err, 31)) { done_ok = false; break; }
+            const int st = i % NSTAGE;
+            if (!tc::mbar_wait(&bar->s_full, i & 1, abort_flag, err, 31)) { done_ok = false; break; }
             tc::tc_fence_after();
             float v[64];
             {
                 float a[32], c[32];
-                tc::tmem_ld32(tmem + lane_off + sb * BK, a);
-                tc::tmem_ld32(tmem + lane_off + sb * BK + 32, c);
+                tc::tmem_ld32(tmem + lane_off + COL_S, a);
+                tc::tmem_ld32(tmem + lane_off + COL_S + 32, c);
                 tc::tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -256,14 +272,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             }
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bar->s_empty[sb]);
-            // swap partial scores with the peer CTA
-            if (i > 0 && !tc::mbar_wait(&bar->xempty, (i - 1) & 1, abort_flag, err, 32)) { done_ok = false; break; }
+            if (lane == 0) tc::mbar_arrive(&bar->s_empty);  // the MMA may now compute the next tile's scores
+            // swap partial scores with the peer CTA: st.async into its X, counted on its xfull
+            if (threadIdx.x == 4 * 32) tc::mbar_arrive_expect_tx(&bar->xfull, X_BYTES);
+            if (i > 0 && !tc::mbar_wait_cluster(&bar->xempty, (i - 1) & 1, abort_flag, err, 32)) { done_ok = false; break; }
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-                tc::st_cluster_v4(peer_x_row + ((c ^ (h & 15)) << 4),
-                                  make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
-            tc::mbar_arrive_cluster(peer_xfull);
+                tc::st_async_v4(peer_x_row + ((c ^ (h & 15)) << 4),
+                                make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]), peer_xfull);
             if (!tc::mbar_wait_cluster(&bar->xfull, i & 1, abort_flag, err, 33)) { done_ok = false; break; }
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
@@ -273,7 +289,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 v[4 * c + 2] += x.z;
                 v[4 * c + 3] += x.w;
             }
-            tc::mbar_arrive_cluster(peer_xempty);
+            // X may be overwritten by the peer's next tile once every warp has read it.
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster(peer_xempty);
             // mask (selection entries that are padding, future or outside the sequence)
             if (!tc::mbar_wait(&bar->kv_full[st], (i / NSTAGE) & 1, abort_flag, err, 34)) { done_ok = false; break; }
             float mt = -INFINITY;
@@ -313,29 +331,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 pk[j] = *(const uint32_t *)&t2;
             }
             l += psum;
+            // the previous PV product must be done before P and O are touched
             if (i > 0 && !tc::mbar_wait(&bar->p_empty, (i - 1) & 1, abort_flag, err, 35)) { done_ok = false; break; }
+            tc::tc_fence_after();
             // tcgen05.ld/st are warp-wide: rescale the whole warp's rows when any row needs it
             // (rows that do not keep alpha = 1).
             if (__any_sync(0xffffffffu, rescale)) {
-                tc::tc_fence_after();
 #pragma unroll 1
                 for (int cc = 0; cc < 8; ++cc) {
                     float o[32];
                     uint32_t ob[32];
-                    tc::tmem_ld32(tmem_o + lane_off + cc * 32, o);
+                    tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) ob[j] = __float_as_uint(o[j] * alpha);
-                    tc::tmem_st32(tmem_o + lane_off + cc * 32, ob);
+                    tc::tmem_st32(tmem + lane_off + COL_O + cc * 32, ob);
                 }
-                tc::tmem_st_wait();
             }
-            // P row h: 64 bf16 = 128 bytes in the 128-byte-swizzled K-major layout
-            uint8_t *prow = Ps + h * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *(uint4 *)(prow + ((c ^ (h & 7)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            tc::fence_proxy_async_smem();
+            tc::tmem_st32(tmem + lane_off + COL_P, pk);  // P row: 64 bf16 as 32 packed columns
+            tc::tmem_st_wait();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bar->p_full);
@@ -352,7 +366,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             for (int cc = 0; cc < 8; ++cc) {
                 float o[32];
                 if (have) {
-                    tc::tmem_ld32(tmem_o + lane_off + cc * 32, o);
+                    tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
                     tc::tmem_ld_wait();
                 }
                 uint32_t pw[16];
@@ -374,7 +388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             for (int cc = 0; cc < 8; ++cc) {
                 float o[32];
                 if (have) {
-                    tc::tmem_ld32(tmem_o + lane_off + cc * 32, o);
+                    tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
                     tc::tmem_ld_wait();
                 }
                 float4 *d4 = (float4 *)(dst + cc * 32);
@@ -480,13 +494,7 @@ cudaError_t launch_mla_tc(const void *qt, const void *kv, int64_t ld_kv, const v
     P.splits = mla_tc_splits(M);
     P.prefix_valid = prefix_valid ? 1 : 0;
     P.scale_log2 = scale * 1.4426950408889634f;
-    CUtensorMap tq, tcm, tpe;
-    {
-        uint64_t dims[2] = {(uint64_t)QW, (uint64_t)M * NH};
-        uint64_t strides[1] = {(uint64_t)QW * 2};
-        uint32_t box[2] = {64, (uint32_t)NH};
-        if (!make_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qt, dims, strides, box)) return cudaErrorInvalidValue;
-    }
+    CUtensorMap tcm, tpe;
     {
         uint64_t dims[2] = {(uint64_t)DC, (uint64_t)std::max<int64_t>(total_k, 1)};
         uint64_t strides[1] = {(uint64_t)ld_kv * 2};
@@ -507,7 +515,8 @@ cudaError_t launch_mla_tc(const void *qt, const void *kv, int64_t ld_kv, const v
     cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)M * P.splits * 2;
-    mla_tc_kernel<<<grid, NUM_THREADS, SMEM, s>>>(tq, tcm, tpe, idx, P, (__nv_bfloat16 *)olat, lse, opart, lpart);
+    mla_tc_kernel<<<grid, NUM_THREADS, SMEM, s>>>(tcm, tpe, (const __nv_bfloat16 *)qt, idx, P, (__nv_bfloat16 *)olat,
+                                                   lse, opart, lpart);
     note_launch(DSA_KERNEL_MLA_TC);
     e = cudaGetLastError();
     if (e != cudaSuccess || P.splits == 1) return e;
