@@ -12,7 +12,7 @@
 // row is handled by a cluster of two CTAs on two SMs:
 //   * CTA 0 holds latent columns 0..255, CTA 1 latent 256..511 and the rope
 //     part -- of q~ (resident, loaded once by TMA) and of each gathered key
-//     tile (64 keys, rows fetched with TMA gather4 from the packed cache).
+//     tile (64 keys, rows gathered with cp.async by two producer warps).
 //   * Each CTA computes a partial score tile S_c = Q_c K_c^T (M = 128 heads,
 //     N = 64 keys) over its columns; the softmax warps swap partial tiles
 //     through distributed shared memory and both add them (in the same
@@ -46,9 +46,9 @@ constexpr int BK = 64;                       // keys per tile (MMA N of QK^T, K 
 constexpr int NSLAB_MAX = 5;                 // 64-column slabs per CTA (CTA 1: 4 latent + rope)
 constexpr int SLAB_K = BK * 128;             // 8 KB: 64 keys x 64 columns, 128-byte swizzle
 constexpr int KV_STAGE = NSLAB_MAX * SLAB_K; // 40 KB
-constexpr int NSTAGE = 4;
-constexpr int X_BYTES = NH * BK * 4;         // 32 KB: the peer's partial scores
-constexpr int SMEM = 1024 + NSTAGE * KV_STAGE + X_BYTES + NSTAGE * BK + 256;
+constexpr int NSTAGE = 3;
+constexpr int X_BYTES = NH * BK * 4;         // 32 KB: partial scores (received X, sent Y)
+constexpr int SMEM = 1024 + NSTAGE * KV_STAGE + 2 * X_BYTES + NSTAGE * BK + 256;
 constexpr int NUM_THREADS = 256;             // warps 0-3: TMA, MMA, TMEM; warps 4-7: softmax
 // Tensor-memory columns (512 per CTA): scores, probabilities (bf16 pairs),
 // the resident q~ slice (bf16 pairs, A operand of QK^T) and the context.
@@ -85,15 +85,16 @@ struct Bars {
 };
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    mla_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_pe,
-                  const __nv_bfloat16 *__restrict__ qt, const int32_t *__restrict__ idx,
+    mla_tc_kernel(const __nv_bfloat16 *__restrict__ kv, int64_t ld_kv, const __nv_bfloat16 *__restrict__ kpe,
+                  int64_t ld_pe, const __nv_bfloat16 *__restrict__ qt, const int32_t *__restrict__ idx,
                   const __grid_constant__ MlaParams P, __nv_bfloat16 *__restrict__ olat, float *__restrict__ lse,
                   float *__restrict__ opart, float *__restrict__ lpart) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *KV = base;
-    float *X = (float *)(KV + NSTAGE * KV_STAGE);
-    uint8_t *kvalid = (uint8_t *)X + X_BYTES;  // [NSTAGE][BK]
+    float *X = (float *)(KV + NSTAGE * KV_STAGE);     // the peer's partial scores land here
+    float *Y = X + NH * BK;                            // this CTA's partial scores, staged for the peer
+    uint8_t *kvalid = (uint8_t *)(Y + NH * BK);        // [NSTAGE][BK]
     Bars *bar = (Bars *)(kvalid + NSTAGE * BK);
     uint32_t *tmem_slot = (uint32_t *)(bar + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
@@ -120,7 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         tc::mbar_init(&bar->q_ready, 4);
         for (int i = 0; i < NSTAGE; ++i) {
-            tc::mbar_init(&bar->kv_full[i], 16);
+            tc::mbar_init(&bar->kv_full[i], 64);  // every gathering thread arrives
             tc::mbar_init(&bar->kv_empty[i], 1);
         }
         tc::mbar_init(&bar->s_full, 1);
@@ -144,51 +145,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tc::cluster_sync();  // both CTAs' barriers exist before any remote arrive
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && n > 0) {
-        // ---------------- producer: key tiles by TMA gather4 ----------------
-        if (lane == 0) {
-            tc::prefetch_tmap(&tm_c);
-            tc::prefetch_tmap(&tm_pe);
-        }
-        int issued = 0;
-        if (lane < 16) {
-            const int32_t *row_idx = idx + (int64_t)r * P.k;
-            const int last = min(p, S - 1);
-            int rows[4];
-            uint32_t ok4 = 0;
-            auto fetch = [&](int i) {  // the 4 cache rows this lane gathers for tile i
-                ok4 = 0;
+    if ((warp == 0 || warp == 3) && n > 0) {
+        // ---------------- producers: gather the selected key rows with cp.async ----------------
+        // Eight lanes cover one 128-byte segment of a row, so a warp instruction
+        // moves four full segments; the 128-byte swizzle of the MMA operand
+        // layout is applied to the 16-byte chunk index.
+        const int pw = warp == 0 ? 0 : 1, c = lane & 7, jr = pw * 4 + (lane >> 3);
+        const int32_t *row_idx = idx + (int64_t)r * P.k;
+        const int last = min(p, S - 1);
+        const uint32_t kv_s = tc::smem_u32(KV);
+        int rows[8];
+        auto fetch = [&](int i) {  // cache rows of this thread's 8 keys of tile i
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int e = e0 + i * BK + 4 * lane + u;
-                    const int s = e < e1 ? __ldg(row_idx + e) : -1;
-                    const bool ok = s >= 0 && s <= last;
-                    rows[u] = kbase + (ok ? s : 0);
-                    ok4 |= (ok ? 1u : 0u) << (8 * u);
-                }
-            };
-            fetch(0);
-            for (int i = 0; i < n; ++i) {
-                const int st = i % NSTAGE;
-                if (!tc::mbar_wait(&bar->kv_empty[st], ((i / NSTAGE) & 1) ^ 1, abort_flag, err, 21)) break;
-                *(uint32_t *)(kvalid + st * BK + 4 * lane) = ok4;
-                tc::mbar_arrive_expect_tx(&bar->kv_full[st], nslab * 4 * 128);
-                uint8_t *dst = KV + st * KV_STAGE + lane * 4 * 128;
-                for (int j = 0; j < nslab; ++j) {
-                    const int g = gslab0 + j;
-                    if (g < 8)
-                        tc::tma_gather4(dst + j * SLAB_K, &tm_c, &bar->kv_full[st], g * 64, rows[0], rows[1], rows[2],
-                                        rows[3]);
-                    else
-                        tc::tma_gather4(dst + j * SLAB_K, &tm_pe, &bar->kv_full[st], 0, rows[0], rows[1], rows[2],
-                                        rows[3]);
-                }
-                ++issued;
-                if (i + 1 < n) fetch(i + 1);  // overlaps the wait for the next free stage
+            for (int ps = 0; ps < 8; ++ps) {
+                const int e = e0 + i * BK + ps * 8 + jr;
+                const int sidx = e < e1 ? __ldg(row_idx + e) : -1;
+                rows[ps] = (sidx >= 0 && sidx <= last) ? sidx : -1;
             }
-            // Drain: every load of this CTA has landed before it may exit.
-            for (int j = max(0, issued - NSTAGE); j < issued; ++j)
-                tc::mbar_wait(&bar->kv_full[j % NSTAGE], (j / NSTAGE) & 1, nv, err, 23);
+        };
+        fetch(0);
+        int issued = 0;
+        for (int i = 0; i < n; ++i) {
+            const int st = i % NSTAGE;
+            if (!tc::mbar_wait(&bar->kv_empty[st], ((i / NSTAGE) & 1) ^ 1, abort_flag, err, 21)) break;
+#pragma unroll
+            for (int ps = 0; ps < 8; ++ps) {
+                const int j = ps * 8 + jr;
+                const int64_t row = kbase + (rows[ps] >= 0 ? rows[ps] : 0);
+                const __nv_bfloat16 *lat = kv + row * ld_kv + c * 8;
+                const uint32_t dst = kv_s + st * KV_STAGE + j * 128 + ((c ^ (j & 7)) << 4);
+                for (int js = 0; js < nslab; ++js) {
+                    const int g = gslab0 + js;
+                    const __nv_bfloat16 *src = g < 8 ? lat + g * 64 : kpe + row * ld_pe + c * 8;
+                    tc::cp_async16(dst + js * SLAB_K, src);
+                }
+                if (c == 0) kvalid[st * BK + j] = rows[ps] >= 0 ? 1 : 0;
+            }
+            tc::cp_async_commit();
+            ++issued;
+            if (i + 1 < n) fetch(i + 1);
+            if (i > 0) {  // the previous tile's copies have landed: publish them to the MMA
+                tc::cp_async_wait<1>();
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&bar->kv_full[(i - 1) % NSTAGE]);
+            }
+        }
+        tc::cp_async_wait<0>();  // nothing may still be copying when the CTA exits
+        if (issued > 0) {
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(&bar->kv_full[(issued - 1) % NSTAGE]);
         }
     } else if (warp == 1 && lane == 0 && n > 0) {
         // ---------------- MMA issuer ----------------
@@ -229,7 +234,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         // ---------------- softmax (one thread per head = TMEM lane) ----------------
         const int q = warp & 3, h = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const uint32_t peer_x_row = tc::map_peer(tc::smem_u32(X) + h * 256, peer);
         const uint32_t peer_xfull = tc::map_peer(tc::smem_u32(&bar->xfull), peer);
         const uint32_t peer_xempty = tc::map_peer(tc::smem_u32(&bar->xempty), peer);
         float m_used = -INFINITY, l = 0.0f;
@@ -254,6 +258,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bar->q_ready);
         }
+        const float sl2 = P.scale_log2;
+        const uint32_t row_sw = (uint32_t)(h & 15);
+        uint8_t *xrow = (uint8_t *)X + h * 256, *yrow = (uint8_t *)Y + h * 256;
+        const uint32_t peer_x_warp = tc::map_peer(tc::smem_u32(X) + q * 32 * 256, peer);
         for (int i = 0; i < n; ++i) {
             const int st = i % NSTAGE;
             if (!tc::mbar_wait(&bar->s_full, i & 1, abort_flag, err, 31)) { done_ok = false; break; }
@@ -273,64 +281,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bar->s_empty);  // the MMA may now compute the next tile's scores
-            // swap partial scores with the peer CTA: st.async into its X, counted on its xfull
+            // --- swap partial scores with the peer: stage locally, one bulk copy per warp ---
             if (threadIdx.x == 4 * 32) tc::mbar_arrive_expect_tx(&bar->xfull, X_BYTES);
-            if (i > 0 && !tc::mbar_wait_cluster(&bar->xempty, (i - 1) & 1, abort_flag, err, 32)) { done_ok = false; break; }
+            if (i > 0 && lane == 0) tc::bulk_wait_read();  // the previous copy has read Y
+            __syncwarp();
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-                tc::st_async_v4(peer_x_row + ((c ^ (h & 15)) << 4),
-                                make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]), peer_xfull);
+                *(float4 *)(yrow + ((c ^ row_sw) << 4)) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // the peer has read what the previous copy put in its X
+                bool ok = i == 0 || tc::mbar_wait_cluster(&bar->xempty, (i - 1) & 1, abort_flag, err, 32);
+                if (ok) tc::bulk_copy_to_peer(peer_x_warp, Y + q * 32 * BK, 32 * BK * 4, peer_xfull);
+            }
             if (!tc::mbar_wait_cluster(&bar->xfull, i & 1, abort_flag, err, 33)) { done_ok = false; break; }
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                const float4 x = *(const float4 *)((const uint8_t *)X + h * 256 + ((c ^ (h & 15)) << 4));
+                const float4 x = *(const float4 *)(xrow + ((c ^ row_sw) << 4));
                 v[4 * c] += x.x;
                 v[4 * c + 1] += x.y;
                 v[4 * c + 2] += x.z;
                 v[4 * c + 3] += x.w;
             }
-            // X may be overwritten by the peer's next tile once every warp has read it.
+            // X may be overwritten by the peer's next copy once every warp has read it
+            // (the values are already in registers, so no ordering fence is needed).
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive_cluster(peer_xempty);
-            // mask (selection entries that are padding, future or outside the sequence)
+            if (lane == 0) tc::mbar_arrive_cluster_relaxed(peer_xempty);
+            // --- mask: entries that are padding, future or outside the sequence ---
             if (!tc::mbar_wait(&bar->kv_full[st], (i / NSTAGE) & 1, abort_flag, err, 34)) { done_ok = false; break; }
-            float mt = -INFINITY;
             {
-                const uint32_t *kvw = (const uint32_t *)(kvalid + st * BK);
+                const uint4 *kv4 = (const uint4 *)(kvalid + st * BK);
+                const uint4 m0 = kv4[0], m1 = kv4[1], m2 = kv4[2], m3 = kv4[3];
+                const uint32_t all = m0.x & m0.y & m0.z & m0.w & m1.x & m1.y & m1.z & m1.w & m2.x & m2.y & m2.z & m2.w &
+                                     m3.x & m3.y & m3.z & m3.w;
+                if (all != 0x01010101u) {
+                    const uint32_t *kvw = (const uint32_t *)(kvalid + st * BK);
 #pragma unroll
-                for (int wd = 0; wd < 16; ++wd) {
-                    const uint32_t bits = kvw[wd];
+                    for (int wd = 0; wd < 16; ++wd) {
+                        const uint32_t bits = kvw[wd];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int j = 4 * wd + u;
-                        v[j] = ((bits >> (8 * u)) & 0xffu) ? v[j] * P.scale_log2 : -INFINITY;
-                        mt = fmaxf(mt, v[j]);
+                        for (int u = 0; u < 4; ++u)
+                            if (!((bits >> (8 * u)) & 0xffu)) v[4 * wd + u] = -INFINITY;
                     }
                 }
             }
+            float mraw = v[0];
+#pragma unroll
+            for (int j = 1; j < 64; ++j) mraw = fmaxf(mraw, v[j]);
+            const float mt = mraw * sl2;  // the scale is positive: max commutes with it
             bool rescale = false;
             float alpha = 1.0f;
             if (mt != -INFINITY) {
                 if (m_used == -INFINITY) {
                     m_used = mt;
                 } else if (mt > m_used + RESCALE_LOG2) {
-                    alpha = exp2f(m_used - mt);
+                    alpha = tc::ex2_approx(m_used - mt);
                     l *= alpha;
                     m_used = mt;
                     rescale = true;
                 }
             }
+            const float neg_m = m_used == -INFINITY ? 0.0f : -m_used;
             uint32_t pk[32];
-            float psum = 0.0f;
+            float psum0 = 0.0f, psum1 = 0.0f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float p0 = v[2 * j] == -INFINITY ? 0.0f : exp2f(v[2 * j] - m_used);
-                const float p1 = v[2 * j + 1] == -INFINITY ? 0.0f : exp2f(v[2 * j + 1] - m_used);
+                const float p0 = tc::ex2_approx(fmaf(v[2 * j], sl2, neg_m));
+                const float p1 = tc::ex2_approx(fmaf(v[2 * j + 1], sl2, neg_m));
                 const __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
-                psum += __low2float(t2) + __high2float(t2);
+                psum0 += __low2float(t2);
+                psum1 += __high2float(t2);
                 pk[j] = *(const uint32_t *)&t2;
             }
-            l += psum;
+            l += psum0 + psum1;
             // the previous PV product must be done before P and O are touched
             if (i > 0 && !tc::mbar_wait(&bar->p_empty, (i - 1) & 1, abort_flag, err, 35)) { done_ok = false; break; }
             tc::tc_fence_after();
@@ -354,6 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bar->p_full);
         }
+        if (lane == 0) tc::bulk_wait_all();  // no copy may still read Y when the CTA exits
         // ---------------- epilogue: normalise and store this CTA's 256 columns ----------------
         const int64_t rh = (int64_t)r * NH + h;
         const bool have = __all_sync(0xffffffffu, n > 0 && done_ok && tc::mbar_wait(&bar->o_done, 0, abort_flag, err, 36));
@@ -494,19 +519,6 @@ cudaError_t launch_mla_tc(const void *qt, const void *kv, int64_t ld_kv, const v
     P.splits = mla_tc_splits(M);
     P.prefix_valid = prefix_valid ? 1 : 0;
     P.scale_log2 = scale * 1.4426950408889634f;
-    CUtensorMap tcm, tpe;
-    {
-        uint64_t dims[2] = {(uint64_t)DC, (uint64_t)std::max<int64_t>(total_k, 1)};
-        uint64_t strides[1] = {(uint64_t)ld_kv * 2};
-        uint32_t box[2] = {64, 1};
-        if (!make_tmap(&tcm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box)) return cudaErrorInvalidValue;
-    }
-    {
-        uint64_t dims[2] = {64, (uint64_t)std::max<int64_t>(total_k, 1)};
-        uint64_t strides[1] = {(uint64_t)ld_pe * 2};
-        uint32_t box[2] = {64, 1};
-        if (!make_tmap(&tpe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kpe, dims, strides, box)) return cudaErrorInvalidValue;
-    }
     float *opart = nullptr, *lpart = nullptr;
     if (P.splits > 1) {
         opart = (float *)part_ws;
@@ -515,8 +527,9 @@ cudaError_t launch_mla_tc(const void *qt, const void *kv, int64_t ld_kv, const v
     cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)M * P.splits * 2;
-    mla_tc_kernel<<<grid, NUM_THREADS, SMEM, s>>>(tcm, tpe, (const __nv_bfloat16 *)qt, idx, P, (__nv_bfloat16 *)olat,
-                                                   lse, opart, lpart);
+    mla_tc_kernel<<<grid, NUM_THREADS, SMEM, s>>>((const __nv_bfloat16 *)kv, ld_kv, (const __nv_bfloat16 *)kpe, ld_pe,
+                                                   (const __nv_bfloat16 *)qt, idx, P, (__nv_bfloat16 *)olat, lse,
+                                                   opart, lpart);
     note_launch(DSA_KERNEL_MLA_TC);
     e = cudaGetLastError();
     if (e != cudaSuccess || P.splits == 1) return e;

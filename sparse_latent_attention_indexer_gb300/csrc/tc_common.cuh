@@ -102,6 +102,16 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only), grouped per thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory, MMA, commit, loads
 // ---------------------------------------------------------------------------
@@ -218,6 +228,30 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint
                      remote_addr),
                  "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
                  : "memory");
+}
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into
+// another CTA's shared memory (both 16-byte aligned), counted on that CTA's
+// mbarrier; the source is free again after bulk_wait_read().
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, const void *src, uint32_t bytes,
+                                                  uint32_t remote_bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(remote_dst),
+        "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Arrive on another CTA's mbarrier without ordering this thread's earlier
+// memory operations (used where the data dependence already orders them).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+// 2^x on the special-function unit (x = -inf gives +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 // Arrive on an mbarrier of another CTA of the cluster, releasing this
 // thread's earlier writes at cluster scope.

@@ -2,8 +2,10 @@
 // M^sel_{t,s} = M_{t,s} for s in top_k(S~^I_t)): a radix select on
 // order-preserving uint32 keys.
 //
-// One CTA per query row.  Only the causal keys 0..p are read.  If there are
-// at most k of them they are all selected.  Otherwise three histogram passes
+// One CTA per query row.  Only the causal keys 0..p are read, once: the first
+// pass converts them to keys and keeps them in shared memory when the row fits
+// the launch's cache (rows longer than that re-read global memory).  If there
+// are at most k causal keys they are all selected.  Otherwise three histogram passes
 // over 11 + 11 + 10 key bits (shared-memory histograms, atomics) find the
 // exact k-th largest key T and how many keys equal to T are needed; a final
 // ordered pass compacts, in increasing key order, every key above T and then
@@ -21,7 +23,8 @@ constexpr int MAX_BINS = 2048;
 
 __global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(const float *__restrict__ scores, int64_t ld,
                                                                 const __grid_constant__ SeqTab st, int k,
-                                                                int32_t *__restrict__ idx) {
+                                                                int32_t *__restrict__ idx, int cache_cap) {
+    extern __shared__ uint32_t cache[];
     __shared__ uint32_t hist[MAX_BINS];
     __shared__ int warp_gt[TK_WARPS], warp_eq[TK_WARPS];
     __shared__ int tot_gt, tot_eq;
@@ -39,6 +42,8 @@ __global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(const float *__r
         return;
     }
 
+    const bool cached = n_live <= cache_cap;
+    auto key_at = [&](int s) -> uint32_t { return cached ? cache[s] : ordered_key(row[s]); };
     uint32_t prefix = 0, pmask = 0;
     int remaining = k;  // keys still to take among those matching the prefix
 #pragma unroll 1
@@ -48,9 +53,17 @@ __global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(const float *__r
         const int nb = 1 << width;
         for (int b = tid; b < nb; b += TK_THREADS) hist[b] = 0;
         __syncthreads();
-        for (int s = tid; s < n_live; s += TK_THREADS) {
-            const uint32_t u = ordered_key(row[s]);
-            if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
+        if (pass == 0) {
+            for (int s = tid; s < n_live; s += TK_THREADS) {
+                const uint32_t u = ordered_key(row[s]);
+                if (cached) cache[s] = u;
+                atomicAdd(&hist[u >> shift], 1u);
+            }
+        } else {
+            for (int s = tid; s < n_live; s += TK_THREADS) {
+                const uint32_t u = key_at(s);
+                if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
+            }
         }
         __syncthreads();
         if (wid == 0) {
@@ -92,7 +105,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(const float *__r
     int base_gt = 0, base_eq = 0;
     for (int s0 = 0; s0 < n_live; s0 += TK_THREADS) {
         const int s = s0 + tid;
-        const uint32_t u = s < n_live ? ordered_key(row[s]) : 0u;
+        const uint32_t u = s < n_live ? key_at(s) : 0u;
         const bool gt = s < n_live && u > T;
         const bool eq = s < n_live && u == T;
         const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
@@ -139,7 +152,17 @@ __global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(const float *__r
 cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int total_q, int k, int32_t *idx,
                         cudaStream_t s) {
     if (total_q == 0) return cudaSuccess;
-    topk_radix_kernel<<<total_q, TK_THREADS, 0, s>>>(scores, ld, st, k, idx);
+    // Shared-memory key cache: the longest causal row of the launch, at most 32768 keys (128 KB).
+    int max_live = 0;
+    for (int b = 0; b < st.B; ++b) {
+        const int T = st.q_off[b + 1] - st.q_off[b];
+        if (T > 0) max_live = max(max_live, min(st.start_pos[b] + T, st.k_len[b]));
+    }
+    const int cap = max_live <= k ? 0 : min(max_live, 32768);
+    const size_t smem = (size_t)cap * sizeof(uint32_t);
+    cudaError_t e = cudaFuncSetAttribute(topk_radix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    topk_radix_kernel<<<total_q, TK_THREADS, smem, s>>>(scores, ld, st, k, idx, cap);
     note_launch(DSA_KERNEL_TOPK);
     return cudaGetLastError();
 }
