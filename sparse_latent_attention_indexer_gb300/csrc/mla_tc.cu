@@ -46,10 +46,11 @@ constexpr int BK = 64;                       // keys per tile (MMA N of QK^T, K 
 constexpr int NSLAB_MAX = 5;                 // 64-column slabs per CTA (CTA 1: 4 latent + rope)
 constexpr int SLAB_K = BK * 128;             // 8 KB: 64 keys x 64 columns, 128-byte swizzle
 constexpr int KV_STAGE = NSLAB_MAX * SLAB_K; // 40 KB
-constexpr int NSTAGE = 3;
+constexpr int NSTAGE = 4;
 constexpr int X_BYTES = NH * BK * 4;         // 32 KB: partial scores (received X, sent Y)
 constexpr int SMEM = 1024 + NSTAGE * KV_STAGE + 2 * X_BYTES + NSTAGE * BK + 256;
-constexpr int NUM_THREADS = 256;             // warps 0-3: TMA, MMA, TMEM; warps 4-7: softmax
+constexpr int NUM_THREADS = 320;             // warps 0, 3, 8, 9: gather; 1: MMA; 2: TMEM; 4-7: softmax
+constexpr int NPROD = 4;                     // gathering warps
 // Tensor-memory columns (512 per CTA): scores, probabilities (bf16 pairs),
 // the resident q~ slice (bf16 pairs, A operand of QK^T) and the context.
 constexpr uint32_t COL_S = 0, COL_P = 64, COL_Q = 96, COL_O = 256;
@@ -121,7 +122,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         tc::mbar_init(&bar->q_ready, 4);
         for (int i = 0; i < NSTAGE; ++i) {
-            tc::mbar_init(&bar->kv_full[i], 64);  // every gathering thread arrives
+            // every gathering thread arrives twice: when its copies land, and to publish the mask bytes
+            tc::mbar_init(&bar->kv_full[i], 2 * NPROD * 32);
             tc::mbar_init(&bar->kv_empty[i], 1);
         }
         tc::mbar_init(&bar->s_full, 1);
@@ -145,32 +147,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tc::cluster_sync();  // both CTAs' barriers exist before any remote arrive
     const uint32_t tmem = *tmem_slot;
 
-    if ((warp == 0 || warp == 3) && n > 0) {
+    if ((warp == 0 || warp == 3 || warp >= 8) && n > 0) {
         // ---------------- producers: gather the selected key rows with cp.async ----------------
         // Eight lanes cover one 128-byte segment of a row, so a warp instruction
         // moves four full segments; the 128-byte swizzle of the MMA operand
         // layout is applied to the 16-byte chunk index.
-        const int pw = warp == 0 ? 0 : 1, c = lane & 7, jr = pw * 4 + (lane >> 3);
+        const int pw = warp == 0 ? 0 : (warp == 3 ? 1 : warp - 6), c = lane & 7, jr = pw * 4 + (lane >> 3);
         const int32_t *row_idx = idx + (int64_t)r * P.k;
         const int last = min(p, S - 1);
         const uint32_t kv_s = tc::smem_u32(KV);
-        int rows[8];
-        auto fetch = [&](int i) {  // cache rows of this thread's 8 keys of tile i
+        constexpr int PASSES = BK / (NPROD * 4);
+        int rows[PASSES];
+        auto fetch = [&](int i) {  // cache rows of this thread's keys of tile i
 #pragma unroll
-            for (int ps = 0; ps < 8; ++ps) {
-                const int e = e0 + i * BK + ps * 8 + jr;
+            for (int ps = 0; ps < PASSES; ++ps) {
+                const int e = e0 + i * BK + ps * NPROD * 4 + jr;
                 const int sidx = e < e1 ? __ldg(row_idx + e) : -1;
                 rows[ps] = (sidx >= 0 && sidx <= last) ? sidx : -1;
             }
         };
         fetch(0);
-        int issued = 0;
         for (int i = 0; i < n; ++i) {
             const int st = i % NSTAGE;
             if (!tc::mbar_wait(&bar->kv_empty[st], ((i / NSTAGE) & 1) ^ 1, abort_flag, err, 21)) break;
 #pragma unroll
-            for (int ps = 0; ps < 8; ++ps) {
-                const int j = ps * 8 + jr;
+            for (int ps = 0; ps < PASSES; ++ps) {
+                const int j = ps * NPROD * 4 + jr;
                 const int64_t row = kbase + (rows[ps] >= 0 ? rows[ps] : 0);
                 const __nv_bfloat16 *lat = kv + row * ld_kv + c * 8;
                 const uint32_t dst = kv_s + st * KV_STAGE + j * 128 + ((c ^ (j & 7)) << 4);
@@ -181,20 +183,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (c == 0) kvalid[st * BK + j] = rows[ps] >= 0 ? 1 : 0;
             }
-            tc::cp_async_commit();
-            ++issued;
+            tc::cp_async_arrive_noinc(&bar->kv_full[st]);  // arrives when this thread's copies have landed
+            tc::mbar_arrive(&bar->kv_full[st]);            // releases the mask bytes
             if (i + 1 < n) fetch(i + 1);
-            if (i > 0) {  // the previous tile's copies have landed: publish them to the MMA
-                tc::cp_async_wait<1>();
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&bar->kv_full[(i - 1) % NSTAGE]);
-            }
         }
         tc::cp_async_wait<0>();  // nothing may still be copying when the CTA exits
-        if (issued > 0) {
-            tc::fence_proxy_async_smem();
-            tc::mbar_arrive(&bar->kv_full[(issued - 1) % NSTAGE]);
-        }
     } else if (warp == 1 && lane == 0 && n > 0) {
         // ---------------- MMA issuer ----------------
         bool ok = tc::mbar_wait(&bar->q_ready, 0, abort_flag, err, 24);
@@ -202,6 +195,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         auto issue_qk = [&](int j) -> bool {
             const int st = j % NSTAGE;
             if (!tc::mbar_wait(&bar->kv_full[st], (j / NSTAGE) & 1, abort_flag, err, 25)) return false;
+            // the gathered rows were written by cp.async (generic proxy); the MMA reads them
+            // through the async proxy
+            tc::fence_proxy_async_smem();
             if (!tc::mbar_wait(&bar->s_empty, (j & 1) ^ 1, abort_flag, err, 26)) return false;
             tc::tc_fence_after();
             for (int js = 0; js < nslab; ++js)
@@ -230,7 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         tc::mma_commit(&bar->o_done);
         tc::mbar_wait(&bar->o_done, 0, nv, err, 28);
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 8) {
         // ---------------- softmax (one thread per head = TMEM lane) ----------------
         const int q = warp & 3, h = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
