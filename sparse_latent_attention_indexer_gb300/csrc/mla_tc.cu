@@ -46,10 +46,10 @@ constexpr int BK = 64;                       // keys per tile (MMA N of QK^T, K 
 constexpr int NSLAB_MAX = 5;                 // 64-column slabs per CTA (CTA 1: 4 latent + rope)
 constexpr int SLAB_K = BK * 128;             // 8 KB: 64 keys x 64 columns, 128-byte swizzle
 constexpr int KV_STAGE = NSLAB_MAX * SLAB_K; // 40 KB
-constexpr int NSTAGE = 4;
+constexpr int NSTAGE = 3;
 constexpr int X_BYTES = NH * BK * 4;         // 32 KB: partial scores (received X, sent Y)
-constexpr int SMEM = 1024 + NSTAGE * KV_STAGE + 2 * X_BYTES + NSTAGE * BK + 256;
-constexpr int NUM_THREADS = 320;             // warps 0, 3, 8, 9: gather; 1: MMA; 2: TMEM; 4-7: softmax
+constexpr int SMEM = 1024 + NSTAGE * KV_STAGE + 2 * X_BYTES + NSTAGE * BK + 3 * 2 * NH * 4 + 256;
+constexpr int NUM_THREADS = 448;             // warps 0, 3, 12, 13: gather; 1: MMA; 2: TMEM; 4-11: softmax
 constexpr int NPROD = 4;                     // gathering warps
 // Tensor-memory columns (512 per CTA): scores, probabilities (bf16 pairs),
 // the resident q~ slice (bf16 pairs, A operand of QK^T) and the context.
@@ -85,7 +85,7 @@ struct Bars {
     uint64_t q_ready, kv_full[NSTAGE], kv_empty[NSTAGE], s_full, s_empty, p_full, p_empty, xfull, xempty, o_done;
 };
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most 4 per SM sub-partition x 128 regs
     mla_tc_kernel(const __nv_bfloat16 *__restrict__ kv, int64_t ld_kv, const __nv_bfloat16 *__restrict__ kpe,
                   int64_t ld_pe, const __nv_bfloat16 *__restrict__ qt, const int32_t *__restrict__ idx,
                   const __grid_constant__ MlaParams P, __nv_bfloat16 *__restrict__ olat, float *__restrict__ lse,
@@ -96,7 +96,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     float *X = (float *)(KV + NSTAGE * KV_STAGE);     // the peer's partial scores land here
     float *Y = X + NH * BK;                            // this CTA's partial scores, staged for the peer
     uint8_t *kvalid = (uint8_t *)(Y + NH * BK);        // [NSTAGE][BK]
-    Bars *bar = (Bars *)(kvalid + NSTAGE * BK);
+    float *pmax = (float *)(kvalid + NSTAGE * BK);     // [2 tiles][2 halves][NH] row-maximum halves
+    float *lsum = pmax + 4 * NH;                       // [2 halves][NH] row-sum halves
+    Bars *bar = (Bars *)(lsum + 2 * NH);
     uint32_t *tmem_slot = (uint32_t *)(bar + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
     __shared__ int never;
@@ -120,18 +122,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int n = e1 > e0 ? (e1 - e0 + BK - 1) / BK : 0;
 
     if (threadIdx.x == 0) {
-        tc::mbar_init(&bar->q_ready, 4);
+        tc::mbar_init(&bar->q_ready, 8);
         for (int i = 0; i < NSTAGE; ++i) {
             // every gathering thread arrives twice: when its copies land, and to publish the mask bytes
             tc::mbar_init(&bar->kv_full[i], 2 * NPROD * 32);
             tc::mbar_init(&bar->kv_empty[i], 1);
         }
         tc::mbar_init(&bar->s_full, 1);
-        tc::mbar_init(&bar->s_empty, 4);
-        tc::mbar_init(&bar->p_full, 4);
+        tc::mbar_init(&bar->s_empty, 8);
+        tc::mbar_init(&bar->p_full, 8);
         tc::mbar_init(&bar->p_empty, 1);
         tc::mbar_init(&bar->xfull, 1);   // armed locally with the 32 KB the peer sends
-        tc::mbar_init(&bar->xempty, 4);  // one arrival per peer softmax warp
+        tc::mbar_init(&bar->xempty, 8);  // one arrival per peer softmax warp
         tc::mbar_init(&bar->o_done, 1);
         *abort_flag = 0;
         never = 0;
@@ -147,12 +149,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     tc::cluster_sync();  // both CTAs' barriers exist before any remote arrive
     const uint32_t tmem = *tmem_slot;
 
-    if ((warp == 0 || warp == 3 || warp >= 8) && n > 0) {
+    if ((warp == 0 || warp == 3 || warp >= 12) && n > 0) {
         // ---------------- producers: gather the selected key rows with cp.async ----------------
         // Eight lanes cover one 128-byte segment of a row, so a warp instruction
         // moves four full segments; the 128-byte swizzle of the MMA operand
         // layout is applied to the 16-byte chunk index.
-        const int pw = warp == 0 ? 0 : (warp == 3 ? 1 : warp - 6), c = lane & 7, jr = pw * 4 + (lane >> 3);
+        const int pw = warp == 0 ? 0 : (warp == 3 ? 1 : warp - 10), c = lane & 7, jr = pw * 4 + (lane >> 3);
         const int32_t *row_idx = idx + (int64_t)r * P.k;
         const int last = min(p, S - 1);
         const uint32_t kv_s = tc::smem_u32(KV);
@@ -226,18 +228,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         tc::mma_commit(&bar->o_done);
         tc::mbar_wait(&bar->o_done, 0, nv, err, 28);
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------- softmax (one thread per head = TMEM lane) ----------------
-        const int q = warp & 3, h = q * 32 + lane;
+    } else if (warp >= 4 && warp < 12) {
+        // ---------------- softmax: two threads per head (TMEM lane), 32 score columns each ----------------
+        const int q = warp & 3, hf = (warp - 4) >> 2, h = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const uint32_t peer_xfull = tc::map_peer(tc::smem_u32(&bar->xfull), peer);
         const uint32_t peer_xempty = tc::map_peer(tc::smem_u32(&bar->xempty), peer);
-        float m_used = -INFINITY, l = 0.0f;
+        float m_used = -INFINITY, l = 0.0f;  // l: this thread's half of the row sum
         bool done_ok = true;
         if (n > 0) {
-            // This CTA's slice of the head's q~ row -> tensor memory (A operand of QK^T).
+            // This CTA's slice of the head's q~ row -> tensor memory (A operand of QK^T);
+            // the two threads of a row split the 64-column slabs.
             const uint4 *src = (const uint4 *)(qt + ((int64_t)r * NH + h) * QW + gslab0 * 64);
-            for (int js = 0; js < nslab; ++js) {
+            for (int js = hf * 2; js < (hf ? nslab : 2); ++js) {
                 uint32_t qv[32];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -255,25 +258,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             if (lane == 0) tc::mbar_arrive(&bar->q_ready);
         }
         const float sl2 = P.scale_log2;
-        const uint32_t row_sw = (uint32_t)(h & 15);
-        uint8_t *xrow = (uint8_t *)X + h * 256, *yrow = (uint8_t *)Y + h * 256;
-        const uint32_t peer_x_warp = tc::map_peer(tc::smem_u32(X) + q * 32 * 256, peer);
+        const uint32_t row_sw = (uint32_t)(h & 7);
+        // X / Y are [half][128 rows][32 floats]: a warp's 32 rows of one half are a contiguous 4 KB block.
+        uint8_t *xrow = (uint8_t *)X + (hf * NH + h) * 128, *yrow = (uint8_t *)Y + (hf * NH + h) * 128;
+        const int wblk = (hf * NH + q * 32) * 128;
+        const uint32_t peer_x_warp = tc::map_peer(tc::smem_u32(X) + wblk, peer);
+        const uint32_t named = 1 + q;  // the two warps of a lane quarter
         for (int i = 0; i < n; ++i) {
             const int st = i % NSTAGE;
             if (!tc::mbar_wait(&bar->s_full, i & 1, abort_flag, err, 31)) { done_ok = false; break; }
             tc::tc_fence_after();
-            float v[64];
-            {
-                float a[32], c[32];
-                tc::tmem_ld32(tmem + lane_off + COL_S, a);
-                tc::tmem_ld32(tmem + lane_off + COL_S + 32, c);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    v[j] = a[j];
-                    v[32 + j] = c[j];
-                }
-            }
+            float v[32];
+            tc::tmem_ld32(tmem + lane_off + COL_S + hf * 32, v);
+            tc::tmem_ld_wait();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bar->s_empty);  // the MMA may now compute the next tile's scores
@@ -282,18 +279,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             if (i > 0 && lane == 0) tc::bulk_wait_read();  // the previous copy has read Y
             __syncwarp();
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
+            for (int c = 0; c < 8; ++c)
                 *(float4 *)(yrow + ((c ^ row_sw) << 4)) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 // the peer has read what the previous copy put in its X
                 bool ok = i == 0 || tc::mbar_wait_cluster(&bar->xempty, (i - 1) & 1, abort_flag, err, 32);
-                if (ok) tc::bulk_copy_to_peer(peer_x_warp, Y + q * 32 * BK, 32 * BK * 4, peer_xfull);
+                if (ok) tc::bulk_copy_to_peer(peer_x_warp, (const uint8_t *)Y + wblk, 32 * 128, peer_xfull);
             }
             if (!tc::mbar_wait_cluster(&bar->xfull, i & 1, abort_flag, err, 33)) { done_ok = false; break; }
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 const float4 x = *(const float4 *)(xrow + ((c ^ row_sw) << 4));
                 v[4 * c] += x.x;
                 v[4 * c + 1] += x.y;
@@ -307,14 +304,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             // --- mask: entries that are padding, future or outside the sequence ---
             if (!tc::mbar_wait(&bar->kv_full[st], (i / NSTAGE) & 1, abort_flag, err, 34)) { done_ok = false; break; }
             {
-                const uint4 *kv4 = (const uint4 *)(kvalid + st * BK);
-                const uint4 m0 = kv4[0], m1 = kv4[1], m2 = kv4[2], m3 = kv4[3];
-                const uint32_t all = m0.x & m0.y & m0.z & m0.w & m1.x & m1.y & m1.z & m1.w & m2.x & m2.y & m2.z & m2.w &
-                                     m3.x & m3.y & m3.z & m3.w;
+                const uint4 *kv4 = (const uint4 *)(kvalid + st * BK + hf * 32);
+                const uint4 m0 = kv4[0], m1 = kv4[1];
+                const uint32_t all = m0.x & m0.y & m0.z & m0.w & m1.x & m1.y & m1.z & m1.w;
                 if (all != 0x01010101u) {
-                    const uint32_t *kvw = (const uint32_t *)(kvalid + st * BK);
+                    const uint32_t *kvw = (const uint32_t *)(kvalid + st * BK + hf * 32);
 #pragma unroll
-                    for (int wd = 0; wd < 16; ++wd) {
+                    for (int wd = 0; wd < 8; ++wd) {
                         const uint32_t bits = kvw[wd];
 #pragma unroll
                         for (int u = 0; u < 4; ++u)
@@ -322,9 +318,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            float mraw = v[0];
+            float mh = v[0];
 #pragma unroll
-            for (int j = 1; j < 64; ++j) mraw = fmaxf(mraw, v[j]);
+            for (int j = 1; j < 32; ++j) mh = fmaxf(mh, v[j]);
+            // row maximum = max of the two halves (double-buffered by tile parity)
+            pmax[(i & 1) * 2 * NH + hf * NH + h] = mh;
+            asm volatile("bar.sync %0, 64;" ::"r"(named) : "memory");
+            const float mraw = fmaxf(mh, pmax[(i & 1) * 2 * NH + (1 - hf) * NH + h]);
             const float mt = mraw * sl2;  // the scale is positive: max commutes with it
             bool rescale = false;
             float alpha = 1.0f;
@@ -339,10 +339,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             const float neg_m = m_used == -INFINITY ? 0.0f : -m_used;
-            uint32_t pk[32];
+            uint32_t pk[16];
             float psum0 = 0.0f, psum1 = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 16; ++j) {
                 const float p0 = tc::ex2_approx(fmaf(v[2 * j], sl2, neg_m));
                 const float p1 = tc::ex2_approx(fmaf(v[2 * j + 1], sl2, neg_m));
                 const __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
@@ -354,11 +354,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             // the previous PV product must be done before P and O are touched
             if (i > 0 && !tc::mbar_wait(&bar->p_empty, (i - 1) & 1, abort_flag, err, 35)) { done_ok = false; break; }
             tc::tc_fence_after();
-            // tcgen05.ld/st are warp-wide: rescale the whole warp's rows when any row needs it
-            // (rows that do not keep alpha = 1).
+            // tcgen05.ld/st are warp-wide: rescale the warp's half of the O columns when any
+            // of its rows needs it (rows that do not keep alpha = 1).
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int cc = hf * 4; cc < hf * 4 + 4; ++cc) {
                     float o[32];
                     uint32_t ob[32];
                     tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
@@ -368,23 +368,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     tc::tmem_st32(tmem + lane_off + COL_O + cc * 32, ob);
                 }
             }
-            tc::tmem_st32(tmem + lane_off + COL_P, pk);  // P row: 64 bf16 as 32 packed columns
+            tc::tmem_st16(tmem + lane_off + COL_P + hf * 16, pk);  // 32 bf16 probabilities as 16 packed columns
             tc::tmem_st_wait();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bar->p_full);
         }
         if (lane == 0) tc::bulk_wait_all();  // no copy may still read Y when the CTA exits
-        // ---------------- epilogue: normalise and store this CTA's 256 columns ----------------
+        // ---------------- epilogue: normalise and store this thread's 128 columns ----------------
+        lsum[hf * NH + h] = l;
+        asm volatile("bar.sync %0, 64;" ::"r"(named) : "memory");
+        const float lrow = l + lsum[(1 - hf) * NH + h];
         const int64_t rh = (int64_t)r * NH + h;
         const bool have = __all_sync(0xffffffffu, n > 0 && done_ok && tc::mbar_wait(&bar->o_done, 0, abort_flag, err, 36));
-        const float inv = (have && l > 0.0f) ? 1.0f / l : 0.0f;
-        const float row_lse = (have && l > 0.0f) ? (m_used + log2f(l)) * LN2 : -INFINITY;
+        const float inv = (have && lrow > 0.0f) ? 1.0f / lrow : 0.0f;
+        const float row_lse = (have && lrow > 0.0f) ? (m_used + log2f(lrow)) * LN2 : -INFINITY;
         if (have) tc::tc_fence_after();
         if (P.splits == 1) {
             __nv_bfloat16 *dst = olat + rh * DC + rank * 256;
 #pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
+            for (int cc = hf * 4; cc < hf * 4 + 4; ++cc) {
                 float o[32];
                 if (have) {
                     tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
@@ -401,12 +404,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pw[4 * e], pw[4 * e + 1], pw[4 * e + 2], pw[4 * e + 3]);
             }
-            if (rank == 0 && lse) lse[rh] = row_lse;
+            if (rank == 0 && hf == 0 && lse) lse[rh] = row_lse;
         } else {
             const int64_t part = ((int64_t)r * P.splits + split) * NH + h;
             float *dst = opart + part * DC + rank * 256;
 #pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
+            for (int cc = hf * 4; cc < hf * 4 + 4; ++cc) {
                 float o[32];
                 if (have) {
                     tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
@@ -418,7 +421,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     d4[e] = have ? make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv)
                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
-            if (rank == 0) lpart[part] = row_lse;
+            if (rank == 0 && hf == 0) lpart[part] = row_lse;
         }
     }
     __syncthreads();
