@@ -45,6 +45,24 @@ def parse():
     return ap.parse_args()
 
 
+def ncu_traffic(stage: str, workload: str):
+    """DRAM bytes per launch of the stage's kernel from the committed ncu
+    capture (profiles/traffic.json), or None when there is no capture for this
+    workload or the kernel's source has changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        entry = json.load(f).get(stage)
+    if not entry or entry.get("workload") != workload:
+        return None
+    src = os.path.join(ROOT, entry["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != entry["sha256"]:
+        return None
+    return float(entry["dram_bytes"])
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -241,7 +259,8 @@ def run_ours(args, world, rank, local):
     achieved = stages[dom]["tflops"]
     peak = peaks["bf16_tflops_sustained"]
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak if achieved else None, "traffic": None,
+                "frac": achieved / peak if achieved else None,
+                "traffic": ncu_traffic(dom, CONFIG_NAMES[args.config]),
                 "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a step)",
                 "algorithmic": f"{flops[dom] / 1e9:.1f} GFLOP per launch"}
 

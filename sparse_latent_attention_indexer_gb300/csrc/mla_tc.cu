@@ -9,28 +9,36 @@
 // and W_UV applied afterwards.)
 //
 // The 128 x 512 fp32 context alone fills a CTA's tensor memory, so a query
-// row is handled by a cluster of two CTAs on two SMs:
-//   * CTA 0 holds latent columns 0..255, CTA 1 latent 256..511 and the rope
-//     part -- of q~ (resident, loaded once by TMA) and of each gathered key
-//     tile (64 keys, rows gathered with cp.async by two producer warps).
-//   * Each CTA computes a partial score tile S_c = Q_c K_c^T (M = 128 heads,
-//     N = 64 keys) over its columns; the softmax warps swap partial tiles
-//     through distributed shared memory and both add them (in the same
-//     order), so both CTAs hold the identical full score tile.
-//   * Both run the same online softmax (identical decisions), write
-//     P (bf16) to shared memory, and accumulate O_c += P V_c for their own 256
-//     latent columns in tensor memory (N = 256, V read MN-major straight from
-//     the gathered tile).
-// The running maximum is only moved (and O rescaled in tensor memory) when
-// a tile's maximum exceeds it by more than 2^8, which after the first tiles
-// almost never happens.  Key tiles are double-buffered in shared memory and
-// score tiles in tensor memory, so the QK^T of tile i+1 overlaps the
-// softmax of tile i.  Waits are bounded; a timeout records its site in the
-// device error word and both CTAs drain and exit.
+// row is handled by a cluster of two CTAs on two SMs.  CTA c owns latent
+// columns 256c..256c+255 and rope columns 32c..32c+31 of q~ and of every key,
+// so both gather the same 576 bytes per key.
+//   * q~ slice: loaded once into tensor memory (the A operand of QK^T, so
+//     the score MMA reads only the key tile from shared memory).
+//   * Key tiles (64 keys): four gathering warps copy the selected rows with
+//     cp.async (8 lanes per 128-byte segment, 128-byte swizzle for the latent
+//     slabs, 64-byte swizzle for the rope half) into a 4-stage ring; a copy's
+//     completion arrives on the stage's barrier by itself.
+//   * One thread issues the MMAs: S_c = Q_c K_c^T (M = 128 heads, N = 64
+//     keys) into tensor memory, and O_c += P V_c (N = 256, V read MN-major
+//     straight from the gathered tile, P from tensor memory).
+//   * Eight softmax warps, two threads per head row (32 scores each): each
+//     CTA rounds its partial scores (log2-scaled) to fp16 and bulk-copies them
+//     into the peer's shared memory; both CTAs then add the same two rounded
+//     halves, so they hold bit-identical scores and take identical softmax
+//     decisions.  The exchange is software-pipelined: tile i is shipped while
+//     tile i-1, whose peer half has arrived, is finished.
+//   * Lazy rescaling: the running maximum moves (and O is rescaled in tensor
+//     memory) only when a tile's maximum exceeds it by more than 2^8.
+// Waits are bounded; a timeout records its site in the device error word and
+// both CTAs drain and exit.
 //
-// Long rows can be split across several clusters (decode: few rows, many
-// keys); each split writes a normalised partial context and its lse, and a
-// small combine kernel merges them.
+// Short batches split each row's keys across up to 8 clusters so that one
+// wave fills the GPU; each split writes a normalised partial context and its
+// lse, and a small combine kernel merges them.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
 #include "tc_common.cuh"
 
 namespace dsa {
@@ -43,12 +51,15 @@ constexpr int NH = 128;                      // heads (MMA M)
 constexpr int DC = 512;                      // latent width
 constexpr int QW = 576;                      // q~ row: [q~ (512) | q_pe (64)]
 constexpr int BK = 64;                       // keys per tile (MMA N of QK^T, K of PV)
-constexpr int NSLAB_MAX = 5;                 // 64-column slabs per CTA (CTA 1: 4 latent + rope)
+// Each CTA of the pair holds 4 latent slabs (64 columns, 128-byte rows) and half of the rope
+// part (32 columns, 64-byte rows) of every key: CTA c owns latent 256c..256c+255, rope 32c..32c+31.
+constexpr int NSLAB = 4;
 constexpr int SLAB_K = BK * 128;             // 8 KB: 64 keys x 64 columns, 128-byte swizzle
-constexpr int KV_STAGE = NSLAB_MAX * SLAB_K; // 40 KB
-constexpr int NSTAGE = 3;
-constexpr int X_BYTES = NH * BK * 4;         // 32 KB: partial scores (received X, sent Y)
-constexpr int SMEM = 1024 + NSTAGE * KV_STAGE + 2 * X_BYTES + NSTAGE * BK + 3 * 2 * NH * 4 + 256;
+constexpr int ROPE_K = BK * 64;              // 4 KB: 64 keys x 32 rope columns, 64-byte swizzle
+constexpr int KV_STAGE = NSLAB * SLAB_K + ROPE_K;  // 36 KB (a multiple of 1 KB: swizzle atoms stay aligned)
+constexpr int NSTAGE = 4;
+constexpr int X_BYTES = NH * BK * 2;         // 16 KB: one tile of fp16 partial scores
+constexpr int SMEM = 1024 + NSTAGE * KV_STAGE + 4 * X_BYTES + NSTAGE * BK + 3 * 2 * NH * 4 + 256;
 constexpr int NUM_THREADS = 448;             // warps 0, 3, 12, 13: gather; 1: MMA; 2: TMEM; 4-11: softmax
 constexpr int NPROD = 4;                     // gathering warps
 // Tensor-memory columns (512 per CTA): scores, probabilities (bf16 pairs),
@@ -82,7 +93,7 @@ __device__ __forceinline__ int find_seq(const MlaParams &P, int r) {
 }
 
 struct Bars {
-    uint64_t q_ready, kv_full[NSTAGE], kv_empty[NSTAGE], s_full, s_empty, p_full, p_empty, xfull, xempty, o_done;
+    uint64_t q_ready, kv_full[NSTAGE], kv_empty[NSTAGE], s_full, s_empty, p_full, p_empty, xfull[2], xempty[2], o_done;
 };
 
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most 4 per SM sub-partition x 128 regs
@@ -93,9 +104,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *KV = base;
-    float *X = (float *)(KV + NSTAGE * KV_STAGE);     // the peer's partial scores land here
-    float *Y = X + NH * BK;                            // this CTA's partial scores, staged for the peer
-    uint8_t *kvalid = (uint8_t *)(Y + NH * BK);        // [NSTAGE][BK]
+    uint8_t *X = KV + NSTAGE * KV_STAGE;               // [2 tiles] the peer's partial scores land here
+    uint8_t *Y = X + 2 * X_BYTES;                      // [2 tiles] this CTA's partial scores, sent from here
+    uint8_t *kvalid = Y + 2 * X_BYTES;                 // [NSTAGE][BK]
     float *pmax = (float *)(kvalid + NSTAGE * BK);     // [2 tiles][2 halves][NH] row-maximum halves
     float *lsum = pmax + 4 * NH;                       // [2 halves][NH] row-sum halves
     Bars *bar = (Bars *)(lsum + 2 * NH);
@@ -107,7 +118,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = tc::cluster_rank(), peer = rank ^ 1u;
-    const int nslab = rank ? 5 : 4, gslab0 = rank ? 4 : 0;
 
     // Work item: heavier rows (later positions) first.
     const int w = (int)(gridDim.x / 2) - 1 - (int)(blockIdx.x / 2);
@@ -132,8 +142,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         tc::mbar_init(&bar->s_empty, 8);
         tc::mbar_init(&bar->p_full, 8);
         tc::mbar_init(&bar->p_empty, 1);
-        tc::mbar_init(&bar->xfull, 1);   // armed locally with the 32 KB the peer sends
-        tc::mbar_init(&bar->xempty, 8);  // one arrival per peer softmax warp
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&bar->xfull[i], 1);   // armed locally with the 32 KB the peer sends
+            tc::mbar_init(&bar->xempty[i], 8);  // one arrival per peer softmax warp
+        }
         tc::mbar_init(&bar->o_done, 1);
         *abort_flag = 0;
         never = 0;
@@ -176,13 +188,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             for (int ps = 0; ps < PASSES; ++ps) {
                 const int j = ps * NPROD * 4 + jr;
                 const int64_t row = kbase + (rows[ps] >= 0 ? rows[ps] : 0);
-                const __nv_bfloat16 *lat = kv + row * ld_kv + c * 8;
+                const __nv_bfloat16 *lat = kv + row * ld_kv + rank * 256 + c * 8;
                 const uint32_t dst = kv_s + st * KV_STAGE + j * 128 + ((c ^ (j & 7)) << 4);
-                for (int js = 0; js < nslab; ++js) {
-                    const int g = gslab0 + js;
-                    const __nv_bfloat16 *src = g < 8 ? lat + g * 64 : kpe + row * ld_pe + c * 8;
-                    tc::cp_async16(dst + js * SLAB_K, src);
-                }
+#pragma unroll
+                for (int js = 0; js < NSLAB; ++js) tc::cp_async16(dst + js * SLAB_K, lat + js * 64);
+                // rope half: 64-byte rows, chunk c of row j at c ^ ((j >> 1) & 3)
+                if (c < 4)
+                    tc::cp_async16(kv_s + st * KV_STAGE + NSLAB * SLAB_K + j * 64 + ((c ^ ((j >> 1) & 3)) << 4),
+                                   kpe + row * ld_pe + rank * 32 + c * 8);
                 if (c == 0) kvalid[st * BK + j] = rows[ps] >= 0 ? 1 : 0;
             }
             tc::cp_async_arrive_noinc(&bar->kv_full[st]);  // arrives when this thread's copies have landed
@@ -202,19 +215,27 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             tc::fence_proxy_async_smem();
             if (!tc::mbar_wait(&bar->s_empty, (j & 1) ^ 1, abort_flag, err, 26)) return false;
             tc::tc_fence_after();
-            for (int js = 0; js < nslab; ++js)
+#pragma unroll
+            for (int js = 0; js < NSLAB; ++js)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t bd = tc::smem_desc(kv0 + st * KV_STAGE + js * SLAB_K + kk * 32, 16, 1024);
                     tc::mma_f16_ts(tmem + COL_S, tmem + COL_Q + js * 32 + kk * 8, bd, IDESC_QK, (js | kk) != 0);
                 }
+            // rope half: K-major, 64-byte swizzle (8-key atoms of 512 bytes)
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                const uint64_t bd = tc::smem_desc(kv0 + st * KV_STAGE + NSLAB * SLAB_K + kk * 32, 16, 512,
+                                                  tc::kSwizzle64B);
+                tc::mma_f16_ts(tmem + COL_S, tmem + COL_Q + NSLAB * 32 + kk * 8, bd, IDESC_QK, true);
+            }
             tc::mma_commit(&bar->s_full);
             return true;
         };
-        if (ok) ok = issue_qk(0);
-        for (int i = 0; ok && i < n; ++i) {
-            if (i + 1 < n && !(ok = issue_qk(i + 1))) break;
-            if (!(ok = tc::mbar_wait(&bar->p_full, i & 1, abort_flag, err, 27))) break;
+        // The softmax warps read the scores of tile j at the start of their iteration j and hand back
+        // P(j-1) at its end, so QK^T(j+1) is issued as soon as S(j) is read, ahead of PV(j-1).
+        auto issue_pv = [&](int i) -> bool {
+            if (!tc::mbar_wait(&bar->p_full, i & 1, abort_flag, err, 27)) return false;
             tc::tc_fence_after();
             const int st = i % NSTAGE;
 #pragma unroll
@@ -225,22 +246,29 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             }
             tc::mma_commit(&bar->kv_empty[st]);
             tc::mma_commit(&bar->p_empty);
+            return true;
+        };
+        if (ok) ok = issue_qk(0);
+        for (int j = 0; ok && j < n; ++j) {
+            if (j + 1 < n && !(ok = issue_qk(j + 1))) break;
+            if (j >= 1 && !(ok = issue_pv(j - 1))) break;
         }
+        if (ok) issue_pv(n - 1);
         tc::mma_commit(&bar->o_done);
         tc::mbar_wait(&bar->o_done, 0, nv, err, 28);
     } else if (warp >= 4 && warp < 12) {
         // ---------------- softmax: two threads per head (TMEM lane), 32 score columns each ----------------
         const int q = warp & 3, hf = (warp - 4) >> 2, h = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const uint32_t peer_xfull = tc::map_peer(tc::smem_u32(&bar->xfull), peer);
-        const uint32_t peer_xempty = tc::map_peer(tc::smem_u32(&bar->xempty), peer);
         float m_used = -INFINITY, l = 0.0f;  // l: this thread's half of the row sum
         bool done_ok = true;
         if (n > 0) {
-            // This CTA's slice of the head's q~ row -> tensor memory (A operand of QK^T);
-            // the two threads of a row split the 64-column slabs.
-            const uint4 *src = (const uint4 *)(qt + ((int64_t)r * NH + h) * QW + gslab0 * 64);
-            for (int js = hf * 2; js < (hf ? nslab : 2); ++js) {
+            // This CTA's slice of the head's q~ row -> tensor memory (A operand of QK^T): latent
+            // columns as 4 slabs of 32 packed columns, then the rope half as 16 more; the two
+            // threads of a row split the slabs and the second one also takes the rope half.
+            const __nv_bfloat16 *qrow = qt + ((int64_t)r * NH + h) * QW;
+            const uint4 *src = (const uint4 *)(qrow + rank * 256);
+            for (int js = hf * 2; js < hf * 2 + 2; ++js) {
                 uint32_t qv[32];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -252,129 +280,176 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                 }
                 tc::tmem_st32(tmem + lane_off + COL_Q + js * 32, qv);
             }
+            if (hf) {
+                const uint4 *rsrc = (const uint4 *)(qrow + DC + rank * 32);
+                uint32_t qv[16];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint4 t4 = __ldg(rsrc + e);
+                    qv[4 * e] = t4.x;
+                    qv[4 * e + 1] = t4.y;
+                    qv[4 * e + 2] = t4.z;
+                    qv[4 * e + 3] = t4.w;
+                }
+                tc::tmem_st16(tmem + lane_off + COL_Q + NSLAB * 32, qv);
+            }
             tc::tmem_st_wait();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bar->q_ready);
         }
         const float sl2 = P.scale_log2;
-        const uint32_t row_sw = (uint32_t)(h & 7);
-        // X / Y are [half][128 rows][32 floats]: a warp's 32 rows of one half are a contiguous 4 KB block.
-        uint8_t *xrow = (uint8_t *)X + (hf * NH + h) * 128, *yrow = (uint8_t *)Y + (hf * NH + h) * 128;
-        const int wblk = (hf * NH + q * 32) * 128;
-        const uint32_t peer_x_warp = tc::map_peer(tc::smem_u32(X) + wblk, peer);
+        const uint32_t row_sw = (uint32_t)((h >> 1) & 3);
+        // The partial scores travel as fp16 of the log2-scaled scores, 64 bytes per half row.
+        // X[2] and Y[2] are [half][128 rows][32 fp16]: a warp's 32 rows of one half form a contiguous
+        // 2 KB block; the 16-byte chunks of a row are rotated by the row to spread the banks.
+        const int roff = (hf * NH + h) * 64, wblk = (hf * NH + q * 32) * 64;
         const uint32_t named = 1 + q;  // the two warps of a lane quarter
-        for (int i = 0; i < n; ++i) {
-            const int st = i % NSTAGE;
-            if (!tc::mbar_wait(&bar->s_full, i & 1, abort_flag, err, 31)) { done_ok = false; break; }
-            tc::tc_fence_after();
-            float v[32];
-            tc::tmem_ld32(tmem + lane_off + COL_S + hf * 32, v);
-            tc::tmem_ld_wait();
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bar->s_empty);  // the MMA may now compute the next tile's scores
-            // --- swap partial scores with the peer: stage locally, one bulk copy per warp ---
-            if (threadIdx.x == 4 * 32) tc::mbar_arrive_expect_tx(&bar->xfull, X_BYTES);
-            if (i > 0 && lane == 0) tc::bulk_wait_read();  // the previous copy has read Y
-            __syncwarp();
+        // Software pipeline: iteration i loads tile i's partial scores and ships them to the
+        // peer, then finishes tile i-1, whose peer half arrived while tile i was being shipped.
+        // Both CTAs sum the same two rounded halves, so they hold bit-identical scores.
+        float prev[32];
+        for (int i = 0; i <= n; ++i) {
+            float cur[32];
+            if (i < n) {
+                if (!tc::mbar_wait(&bar->s_full, i & 1, abort_flag, err, 31)) { done_ok = false; break; }
+                tc::tc_fence_after();
+                tc::tmem_ld32(tmem + lane_off + COL_S + hf * 32, cur);
+                tc::tmem_ld_wait();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bar->s_empty);  // the MMA may now compute the next tile's scores
+                uint32_t hw[16];
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *(float4 *)(yrow + ((c ^ row_sw) << 4)) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                // the peer has read what the previous copy put in its X
-                bool ok = i == 0 || tc::mbar_wait_cluster(&bar->xempty, (i - 1) & 1, abort_flag, err, 32);
-                if (ok) tc::bulk_copy_to_peer(peer_x_warp, (const uint8_t *)Y + wblk, 32 * 128, peer_xfull);
+                for (int j = 0; j < 16; ++j) {
+                    const float a = fminf(fmaxf(cur[2 * j] * sl2, -60000.0f), 60000.0f);
+                    const float b = fminf(fmaxf(cur[2 * j + 1] * sl2, -60000.0f), 60000.0f);
+                    const __half2 h2 = __floats2half2_rn(a, b);
+                    hw[j] = *(const uint32_t *)&h2;
+                    cur[2 * j] = __low2float(h2);
+                    cur[2 * j + 1] = __high2float(h2);
+                }
+                const int xb = i & 1;
+                if (threadIdx.x == 4 * 32) tc::mbar_arrive_expect_tx(&bar->xfull[xb], X_BYTES);
+                // Once the peer has read tile i-2 from its X[xb], the copy that delivered it has also
+                // finished reading Y[xb]: both buffers of this parity are free again.
+                bool ok = true;
+                if (lane == 0 && i >= 2)
+                    ok = tc::mbar_wait_cluster(&bar->xempty[xb], ((i >> 1) & 1) ^ 1, abort_flag, err, 32);
+                __syncwarp();
+                if (!__shfl_sync(0xffffffffu, ok, 0)) { done_ok = false; break; }
+                uint8_t *yrow = Y + xb * X_BYTES + roff;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *(uint4 *)(yrow + ((c ^ row_sw) << 4)) = make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+                tc::fence_proxy_async_smem();  // the stores are read by the bulk copy (async proxy)
+                __syncwarp();
+                if (lane == 0)
+                    tc::bulk_copy_to_peer(tc::map_peer(tc::smem_u32(X + xb * X_BYTES) + wblk, peer),
+                                          Y + xb * X_BYTES + wblk, 32 * 64,
+                                          tc::map_peer(tc::smem_u32(&bar->xfull[xb]), peer));
             }
-            if (!tc::mbar_wait_cluster(&bar->xfull, i & 1, abort_flag, err, 33)) { done_ok = false; break; }
+            if (i > 0) {
+                // ---------------- finish tile t = i - 1 ----------------
+                const int t = i - 1, xb = t & 1, st = t % NSTAGE;
+                float *v = prev;
+                if (!tc::mbar_wait_cluster(&bar->xfull[xb], (t >> 1) & 1, abort_flag, err, 33)) { done_ok = false; break; }
+                const uint8_t *xrow = X + xb * X_BYTES + roff;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 x = *(const float4 *)(xrow + ((c ^ row_sw) << 4));
-                v[4 * c] += x.x;
-                v[4 * c + 1] += x.y;
-                v[4 * c + 2] += x.z;
-                v[4 * c + 3] += x.w;
-            }
-            // X may be overwritten by the peer's next copy once every warp has read it
-            // (the values are already in registers, so no ordering fence is needed).
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive_cluster_relaxed(peer_xempty);
-            // --- mask: entries that are padding, future or outside the sequence ---
-            if (!tc::mbar_wait(&bar->kv_full[st], (i / NSTAGE) & 1, abort_flag, err, 34)) { done_ok = false; break; }
-            {
-                const uint4 *kv4 = (const uint4 *)(kvalid + st * BK + hf * 32);
-                const uint4 m0 = kv4[0], m1 = kv4[1];
-                const uint32_t all = m0.x & m0.y & m0.z & m0.w & m1.x & m1.y & m1.z & m1.w;
-                if (all != 0x01010101u) {
-                    const uint32_t *kvw = (const uint32_t *)(kvalid + st * BK + hf * 32);
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 x = *(const uint4 *)(xrow + ((c ^ row_sw) << 4));
+                    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                    for (int wd = 0; wd < 8; ++wd) {
-                        const uint32_t bits = kvw[wd];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            if (!((bits >> (8 * u)) & 0xffu)) v[4 * wd + u] = -INFINITY;
+                    for (int e = 0; e < 4; ++e) {
+                        const __half2 h2 = *(const __half2 *)&xs[e];
+                        v[8 * c + 2 * e] += __low2float(h2);
+                        v[8 * c + 2 * e + 1] += __high2float(h2);
                     }
                 }
-            }
-            float mh = v[0];
+                // X[xb] may be overwritten by the peer's copy of tile t+2 once every lane of every warp
+                // has read it.  The warp barrier orders the lanes' loads before lane 0's arrive, and the
+                // arrive's release (CTA scope: the loads are of this CTA's own shared memory) keeps them
+                // ahead of the peer's view of the arrival.
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive_remote(tc::map_peer(tc::smem_u32(&bar->xempty[xb]), peer));
+                // --- mask: entries that are padding, future or outside the sequence ---
+                if (!tc::mbar_wait(&bar->kv_full[st], (t / NSTAGE) & 1, abort_flag, err, 34)) { done_ok = false; break; }
+                {
+                    const uint4 *kv4 = (const uint4 *)(kvalid + st * BK + hf * 32);
+                    const uint4 m0 = kv4[0], m1 = kv4[1];
+                    const uint32_t all = m0.x & m0.y & m0.z & m0.w & m1.x & m1.y & m1.z & m1.w;
+                    if (all != 0x01010101u) {
+                        const uint32_t *kvw = (const uint32_t *)(kvalid + st * BK + hf * 32);
 #pragma unroll
-            for (int j = 1; j < 32; ++j) mh = fmaxf(mh, v[j]);
-            // row maximum = max of the two halves (double-buffered by tile parity)
-            pmax[(i & 1) * 2 * NH + hf * NH + h] = mh;
-            asm volatile("bar.sync %0, 64;" ::"r"(named) : "memory");
-            const float mraw = fmaxf(mh, pmax[(i & 1) * 2 * NH + (1 - hf) * NH + h]);
-            const float mt = mraw * sl2;  // the scale is positive: max commutes with it
-            bool rescale = false;
-            float alpha = 1.0f;
-            if (mt != -INFINITY) {
-                if (m_used == -INFINITY) {
-                    m_used = mt;
-                } else if (mt > m_used + RESCALE_LOG2) {
-                    alpha = tc::ex2_approx(m_used - mt);
-                    l *= alpha;
-                    m_used = mt;
-                    rescale = true;
+                        for (int wd = 0; wd < 8; ++wd) {
+                            const uint32_t bits = kvw[wd];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                if (!((bits >> (8 * u)) & 0xffu)) v[4 * wd + u] = -INFINITY;
+                        }
+                    }
                 }
-            }
-            const float neg_m = m_used == -INFINITY ? 0.0f : -m_used;
-            uint32_t pk[16];
-            float psum0 = 0.0f, psum1 = 0.0f;
+                float mh = v[0];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float p0 = tc::ex2_approx(fmaf(v[2 * j], sl2, neg_m));
-                const float p1 = tc::ex2_approx(fmaf(v[2 * j + 1], sl2, neg_m));
-                const __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
-                psum0 += __low2float(t2);
-                psum1 += __high2float(t2);
-                pk[j] = *(const uint32_t *)&t2;
-            }
-            l += psum0 + psum1;
-            // the previous PV product must be done before P and O are touched
-            if (i > 0 && !tc::mbar_wait(&bar->p_empty, (i - 1) & 1, abort_flag, err, 35)) { done_ok = false; break; }
-            tc::tc_fence_after();
-            // tcgen05.ld/st are warp-wide: rescale the warp's half of the O columns when any
-            // of its rows needs it (rows that do not keep alpha = 1).
-            if (__any_sync(0xffffffffu, rescale)) {
+                for (int j = 1; j < 32; ++j) mh = fmaxf(mh, v[j]);
+                // row maximum = max of the two halves (double-buffered by tile parity)
+                pmax[(t & 1) * 2 * NH + hf * NH + h] = mh;
+                asm volatile("bar.sync %0, 64;" ::"r"(named) : "memory");
+                const float mraw = fmaxf(mh, pmax[(t & 1) * 2 * NH + (1 - hf) * NH + h]);
+                const float mt = mraw;  // the scores are already in log2 units
+                bool rescale = false;
+                float alpha = 1.0f;
+                if (mt != -INFINITY) {
+                    if (m_used == -INFINITY) {
+                        m_used = mt;
+                    } else if (mt > m_used + RESCALE_LOG2) {
+                        alpha = tc::ex2_approx(m_used - mt);
+                        l *= alpha;
+                        m_used = mt;
+                        rescale = true;
+                    }
+                }
+                const float neg_m = m_used == -INFINITY ? 0.0f : -m_used;
+                uint32_t pk[16];
+                float psum0 = 0.0f, psum1 = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float p0 = tc::ex2_approx(v[2 * j] + neg_m);
+                    const float p1 = tc::ex2_approx(v[2 * j + 1] + neg_m);
+                    const __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
+                    psum0 += __low2float(t2);
+                    psum1 += __high2float(t2);
+                    pk[j] = *(const uint32_t *)&t2;
+                }
+                l += psum0 + psum1;
+                // the previous PV product must be done before P and O are touched
+                if (t > 0 && !tc::mbar_wait(&bar->p_empty, (t - 1) & 1, abort_flag, err, 35)) { done_ok = false; break; }
+                tc::tc_fence_after();
+                // tcgen05.ld/st are warp-wide: rescale the warp's half of the O columns when any
+                // of its rows needs it (rows that do not keep alpha = 1).
+                if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-                for (int cc = hf * 4; cc < hf * 4 + 4; ++cc) {
-                    float o[32];
-                    uint32_t ob[32];
-                    tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
-                    tc::tmem_ld_wait();
+                    for (int cc = hf * 4; cc < hf * 4 + 4; ++cc) {
+                        float o[32];
+                        uint32_t ob[32];
+                        tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
+                        tc::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) ob[j] = __float_as_uint(o[j] * alpha);
-                    tc::tmem_st32(tmem + lane_off + COL_O + cc * 32, ob);
+                        for (int j = 0; j < 32; ++j) ob[j] = __float_as_uint(o[j] * alpha);
+                        tc::tmem_st32(tmem + lane_off + COL_O + cc * 32, ob);
+                    }
                 }
+                tc::tmem_st16(tmem + lane_off + COL_P + hf * 16, pk);  // 32 bf16 probabilities as 16 packed columns
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bar->p_full);
             }
-            tc::tmem_st16(tmem + lane_off + COL_P + hf * 16, pk);  // 32 bf16 probabilities as 16 packed columns
-            tc::tmem_st_wait();
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bar->p_full);
+            if (i < n) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) prev[j] = cur[j];
+            }
         }
-        if (lane == 0) tc::bulk_wait_all();  // no copy may still read Y when the CTA exits
         // ---------------- epilogue: normalise and store this thread's 128 columns ----------------
         lsum[hf * NH + h] = l;
         asm volatile("bar.sync %0, 64;" ::"r"(named) : "memory");
@@ -487,11 +562,11 @@ bool mla_tc_supported(int dtype, int H, int d_n, int d_r, int d_c, int d_v) {
 // Clusters per row: enough rows fill the GPU on their own; a few long rows
 // (decode) are split so that about two clusters per SM pair run.
 int mla_tc_splits(int M) {
-    if (M >= 152) return 1;
-    const int want = (152 + M - 1) / M;
-    int s = 1;
-    while (s < want && s < 8) s *= 2;
-    return s;
+    // One CTA per SM (shared memory) and two per cluster: 76 clusters run at once.  Splitting a
+    // row's keys pays only while the clusters still fit one wave; beyond that it adds waves of
+    // proportionally shorter work plus a pipeline fill per wave.
+    const int wave = 152 / 2;
+    return M >= wave ? 1 : std::min(8, std::max(1, wave / M));
 }
 
 size_t mla_tc_partial_bytes(int M) {

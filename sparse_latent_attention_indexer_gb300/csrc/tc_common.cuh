@@ -88,16 +88,6 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
-// Four rows (row coordinates r0..r3, same column x) of a 2-D tensor whose
-// box is one row high; the rows land consecutively at dst.
-__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int r0, int r1,
-                                            int r2, int r3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-        : "memory");
-}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -229,48 +219,28 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t local_addr, uint32_t rank)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
-                 "f"(v.w)
-                 : "memory");
-}
-// Asynchronous 16-byte store into another CTA's shared memory that counts
-// its bytes on that CTA's mbarrier (complete_tx): no fence is needed, the
-// receiver sees the data once the barrier phase completes.
-__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                     remote_addr),
-                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
-                 : "memory");
-}
-// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory into
 // another CTA's shared memory (both 16-byte aligned), counted on that CTA's
-// mbarrier; the source is free again after bulk_wait_read().
+// mbarrier.  This direction completes only through that mbarrier: it joins no
+// bulk async-group, so the sender learns that the source may be reused only
+// from a message the receiver sends back after its barrier phase completed.
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, const void *src, uint32_t bytes,
                                                   uint32_t remote_bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(remote_dst),
         "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
         : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// Arrive on another CTA's mbarrier without ordering this thread's earlier
-// memory operations (used where the data dependence already orders them).
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+// Arrive on a barrier in another CTA of the cluster with the instruction's default semantics
+// (release at CTA scope): orders this thread's earlier accesses to its own CTA's shared memory.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 // 2^x on the special-function unit (x = -inf gives +0).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-// Arrive on an mbarrier of another CTA of the cluster, releasing this
-// thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t addr, uint32_t parity) {
     uint32_t ok;
@@ -305,8 +275,9 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
 // ---------------------------------------------------------------------------
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), descriptor version 1 at bit 46, and the
-// swizzle mode in bits 61..63 (2 = 128-byte swizzle).
+// swizzle mode in bits 61..63 (2 = 128-byte, 4 = 64-byte swizzle).
 constexpr uint64_t kSwizzle128B = 2;
+constexpr uint64_t kSwizzle64B = 4;
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                               uint64_t swizzle = kSwizzle128B) {
     uint64_t d = 0;

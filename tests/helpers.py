@@ -24,6 +24,12 @@ import sparse_latent_attention_indexer_gb300 as dsa
 SCORE_RTOL = 1e-3
 OUT_ATOL_BF16 = 2e-2
 OUT_ATOL_F32 = 1e-4
+# The stated tolerances bound the outputs only; the lse (natural log) bound is derived from the
+# rounding the bf16 path performs: q~ rounded to bf16 (relative 2^-9 per element) perturbs a
+# unit-scale logit by a few 1e-3, and the fp16 exchange of the log2-scaled partial scores between
+# the two CTAs of a cluster (relative 2^-11 of scores below about 8) adds about 3e-3 more.
+LSE_ATOL_BF16 = 1e-2
+LSE_ATOL_F32 = 1e-4
 
 
 def seqs_of(wl) -> dsa.Seqs:

@@ -166,7 +166,7 @@ def test_sparse_mla_given_selection(name):
                                             H.f32np(T["W_UV"]), sel[q0:q1].numpy(), pos, sh.softmax_scale)
         err = np.abs(out[q0:q1] - ro).max()
         assert err <= out_atol(wl), f"seq {b}: max abs err {err:.3e}"
-        assert np.allclose(lse[q0:q1], rl, rtol=0, atol=5e-3 if sh.dtype == "bf16" else 1e-4)
+        assert np.allclose(lse[q0:q1], rl, rtol=0, atol=H.LSE_ATOL_BF16 if sh.dtype == "bf16" else H.LSE_ATOL_F32)
 
 
 def test_sparse_mla_masked_rows_and_out_of_window_indices():
@@ -246,6 +246,37 @@ def test_forward_deterministic():
     assert torch.equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("rows", [256, 24])
+def test_sparse_mla_repeatable_over_runs(rows):
+    """Long selections (about 32 key tiles per row) run eight times in a row:
+    every run is bit-identical and sampled rows match the oracle.  The two
+    CTAs of a row exchange partial scores through double-buffered shared
+    memory every tile, so a buffer reused before its transfer finished shows
+    up as run-to-run differences in a few rows.  24 rows take the split path
+    (several clusters per row plus the merge kernel)."""
+    wl = di.generate("repeat", di.FULL, 17, [rows], [4096], [4096 - rows])
+    t = H.to_device(wl)
+    sh = wl.shape
+    sel = di.random_selection(wl, seed=5, density=0.7)
+    seqs = H.seqs_of(wl)
+    sel_d = sel.cuda()
+    runs = [dsa.dsa_sparse_mla_fwd(t["q_nope"], t["q_pe"], t["ckv"], t["kpe"], t["W_UK"], t["W_UV"], sel_d, seqs,
+                                   sh.softmax_scale) for _ in range(8)]
+    for k, (o, l) in enumerate(runs[1:], 1):
+        bad = (o != runs[0][0]).flatten(1).any(1).nonzero().flatten().tolist()
+        assert not bad and torch.equal(l, runs[0][1]), f"run {k} differs from run 0 in rows {bad[:8]}"
+    sample = sorted({0, rows // 3, rows // 2, rows - 1})
+    T = wl.tensors
+    pos = np.array([wl.start_pos[0] + r for r in sample], np.int64)
+    cache = H.f32np(T["kv_cache"])
+    ro, rl = oracle.sparse_mla_absorbed(H.f32np(T["q_nope"][sample]), H.f32np(T["q_pe"][sample]), cache[:, :sh.d_c],
+                                        cache[:, sh.d_c:], H.f32np(T["W_UK"]), H.f32np(T["W_UV"]),
+                                        sel[sample].numpy(), pos, sh.softmax_scale)
+    out = runs[0][0].float().cpu().numpy()[sample]
+    assert np.abs(out - ro).max() <= H.OUT_ATOL_BF16
+    assert np.abs(runs[0][1].cpu().numpy()[sample] - rl).max() <= H.LSE_ATOL_BF16
+
+
 @pytest.mark.parametrize("name", ["bf16-ragged", "bf16-k64", "fp8-ragged"])
 def test_indexer_tensor_core_matches_generic(name, monkeypatch):
     """The tcgen05 indexer and the CUDA-core indexer on the same inputs agree
@@ -286,4 +317,4 @@ def test_attention_stage_tensor_core_matches_generic(name, monkeypatch):
     assert "absorb_simt" in dsa.last_kernels()
     monkeypatch.delenv("DSA_FORCE_GENERIC")
     assert (fast.float() - gen.float()).abs().max().item() <= H.OUT_ATOL_BF16
-    assert (lf - lg).abs().max().item() <= 5e-3
+    assert (lf - lg).abs().max().item() <= H.LSE_ATOL_BF16
