@@ -308,27 +308,20 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         // Software pipeline: iteration i loads tile i's partial scores and ships them to the
         // peer, then finishes tile i-1, whose peer half arrived while tile i was being shipped.
         // Both CTAs sum the same two rounded halves, so they hold bit-identical scores.
-        float prev[32];
+        uint32_t prev[16];  // the previous tile's own partial scores (packed fp16 pairs)
         for (int i = 0; i <= n; ++i) {
-            float cur[32];
+            uint32_t cur[16];
             if (i < n) {
                 if (!tc::mbar_wait(&bar->s_full, i & 1, abort_flag, err, 31)) { done_ok = false; break; }
                 tc::tc_fence_after();
-                tc::tmem_ld32(tmem + lane_off + COL_S + hf * 32, cur);
+                float sc[32];
+                tc::tmem_ld32(tmem + lane_off + COL_S + hf * 32, sc);
                 tc::tmem_ld_wait();
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&bar->s_empty);  // the MMA may now compute the next tile's scores
-                uint32_t hw[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float a = fminf(fmaxf(cur[2 * j] * sl2, -60000.0f), 60000.0f);
-                    const float b = fminf(fmaxf(cur[2 * j + 1] * sl2, -60000.0f), 60000.0f);
-                    const __half2 h2 = __floats2half2_rn(a, b);
-                    hw[j] = *(const uint32_t *)&h2;
-                    cur[2 * j] = __low2float(h2);
-                    cur[2 * j + 1] = __high2float(h2);
-                }
+                for (int j = 0; j < 16; ++j) cur[j] = tc::f16x2_satfinite(sc[2 * j] * sl2, sc[2 * j + 1] * sl2);
                 const int xb = i & 1;
                 if (threadIdx.x == 4 * 32) tc::mbar_arrive_expect_tx(&bar->xfull[xb], X_BYTES);
                 // Once the peer has read tile i-2 from its X[xb], the copy that delivered it has also
@@ -341,7 +334,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                 uint8_t *yrow = Y + xb * X_BYTES + roff;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    *(uint4 *)(yrow + ((c ^ row_sw) << 4)) = make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+                    *(uint4 *)(yrow + ((c ^ row_sw) << 4)) = make_uint4(cur[4 * c], cur[4 * c + 1], cur[4 * c + 2], cur[4 * c + 3]);
                 tc::fence_proxy_async_smem();  // the stores are read by the bulk copy (async proxy)
                 __syncwarp();
                 if (lane == 0)
@@ -352,7 +345,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             if (i > 0) {
                 // ---------------- finish tile t = i - 1 ----------------
                 const int t = i - 1, xb = t & 1, st = t % NSTAGE;
-                float *v = prev;
+                float v[32];
                 if (!tc::mbar_wait_cluster(&bar->xfull[xb], (t >> 1) & 1, abort_flag, err, 33)) { done_ok = false; break; }
                 const uint8_t *xrow = X + xb * X_BYTES + roff;
 #pragma unroll
@@ -361,9 +354,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const __half2 h2 = *(const __half2 *)&xs[e];
-                        v[8 * c + 2 * e] += __low2float(h2);
-                        v[8 * c + 2 * e + 1] += __high2float(h2);
+                        // peer half + own half in fp32 (addition commutes: both CTAs get the same sum)
+                        const uint32_t own = prev[4 * c + e];
+                        v[8 * c + 2 * e] = tc::add_f16_f32((uint16_t)(xs[e] & 0xffffu), tc::f16_to_f32((uint16_t)(own & 0xffffu)));
+                        v[8 * c + 2 * e + 1] = tc::add_f16_f32((uint16_t)(xs[e] >> 16), tc::f16_to_f32((uint16_t)(own >> 16)));
                     }
                 }
                 // X[xb] may be overwritten by the peer's copy of tile t+2 once every lane of every warp
@@ -389,9 +383,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                         }
                     }
                 }
-                float mh = v[0];
+                float mh = tc::max3(v[0], v[1], v[2]);
 #pragma unroll
-                for (int j = 1; j < 32; ++j) mh = fmaxf(mh, v[j]);
+                for (int j = 3; j < 31; j += 2) mh = tc::max3(mh, v[j], v[j + 1]);
+                mh = fmaxf(mh, v[31]);
                 // row maximum = max of the two halves (double-buffered by tile parity)
                 pmax[(t & 1) * 2 * NH + hf * NH + h] = mh;
                 asm volatile("bar.sync %0, 64;" ::"r"(named) : "memory");
@@ -417,9 +412,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                     const float p0 = tc::ex2_approx(v[2 * j] + neg_m);
                     const float p1 = tc::ex2_approx(v[2 * j + 1] + neg_m);
                     const __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
-                    psum0 += __low2float(t2);
-                    psum1 += __high2float(t2);
                     pk[j] = *(const uint32_t *)&t2;
+                    // the row sum takes the rounded probabilities that the PV product uses
+                    psum0 = tc::add_bf16_f32((uint16_t)(pk[j] & 0xffffu), psum0);
+                    psum1 = tc::add_bf16_f32((uint16_t)(pk[j] >> 16), psum1);
                 }
                 l += psum0 + psum1;
                 // the previous PV product must be done before P and O are touched
@@ -447,7 +443,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             }
             if (i < n) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) prev[j] = cur[j];
+                for (int j = 0; j < 16; ++j) prev[j] = cur[j];
             }
         }
         // ---------------- epilogue: normalise and store this thread's 128 columns ----------------

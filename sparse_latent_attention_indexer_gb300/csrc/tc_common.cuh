@@ -236,6 +236,35 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, const voi
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
+// {lo, hi} -> packed f16 pair (lo in the low half), rounded to nearest and
+// saturated to the finite range (+-65504).
+__device__ __forceinline__ uint32_t f16x2_satfinite(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// f16 a (as its 16 bits) + f32 c, one rounding to f32.
+__device__ __forceinline__ float add_f16_f32(uint16_t a, float c) {
+    float d;
+    asm("add.rn.f32.f16 %0, %1, %2;" : "=f"(d) : "h"(a), "f"(c));
+    return d;
+}
+// bf16 a (as its 16 bits) + f32 c, one rounding to f32.
+__device__ __forceinline__ float add_bf16_f32(uint16_t a, float c) {
+    float d;
+    asm("add.rn.f32.bf16 %0, %1, %2;" : "=f"(d) : "h"(a), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float f16_to_f32(uint16_t a) {
+    float d;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(d) : "h"(a));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 // 2^x on the special-function unit (x = -inf gives +0).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
