@@ -45,11 +45,20 @@ def parse():
     return ap.parse_args()
 
 
+def source_digest(paths):
+    """sha256 over the given repository files, in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def ncu_traffic(stage: str, workload: str):
     """DRAM bytes per launch of the stage's kernel from the committed ncu
     capture (profiles/traffic.json), or None when there is no capture for this
-    workload or the kernel's source has changed since it was taken."""
-    import hashlib
+    workload or the kernel's sources have changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -57,8 +66,8 @@ def ncu_traffic(stage: str, workload: str):
         entry = json.load(f).get(stage)
     if not entry or entry.get("workload") != workload:
         return None
-    src = os.path.join(ROOT, entry["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != entry["sha256"]:
+    srcs = entry["sources"]
+    if not all(os.path.exists(os.path.join(ROOT, p)) for p in srcs) or source_digest(srcs) != entry["sha256"]:
         return None
     return float(entry["dram_bytes"])
 
@@ -70,6 +79,65 @@ def load_peaks():
             d = json.load(f)
         return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (read-only queries)
+    every 5 ms on a thread, so that a timed region of a few tens of
+    milliseconds still gets samples.  Raises on construction if NVML cannot be
+    loaded; ClockSampler (nvidia-smi) is the fallback."""
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, uuid: str | None):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        if uuid:
+            rc = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev))
+        else:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.dev))
+        if rc != 0:
+            raise RuntimeError("NVML device handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx)) == 0 else None
+
+    def _run(self):
+        ct = self.ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop_flag.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(clk)) == 0 and \
+                    self.reasons_fn(self.dev, ct.byref(rs)) == 0:
+                self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(0.005)
+
+    def start(self):
+        self.thread.start()
+
+    def stop(self):
+        self.stop_flag.set()
+        self.thread.join(timeout=2)
+        self.lib.nvmlShutdown()
+        if not self.samples:
+            return None
+        reasons = sorted({n for _, r in self.samples for bit, n in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples), "source": "NVML, 5 ms"}
+
+
+def clock_sampler(uuid):
+    try:
+        return NvmlClockSampler(uuid)
+    except Exception:
+        return ClockSampler(uuid)
 
 
 class ClockSampler:
@@ -222,7 +290,7 @@ def run_ours(args, world, rank, local):
 
     nst = dsa._abi.DSA_STAGE_EVENTS
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(args.steps)]
-    clocks = ClockSampler(_gpu_uuid(local))
+    clocks = clock_sampler(_gpu_uuid(local))
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
@@ -242,27 +310,49 @@ def run_ours(args, world, rank, local):
     ms = max_over_ranks(statistics.mean(step_ms), world)
     value = wl.total_q * world / (ms / 1e3)
 
-    # roofline of the dominant stage (each stage below is one kernel on this path)
+    # roofline of the dominant stage: flops and compulsory HBM bytes per stage; the stage is
+    # tensor-bound when its intensity is above the measured ridge point, else HBM-bound
     peaks, peak_src = load_peaks()
     pairs_sel, pairs_causal = wl.selected_pairs(), wl.causal_pairs()
+    elt = 4 if sh.dtype == "f32" else 2
+    ki_elt = 1 if sh.idx_fp8 else elt
     flops = {
         "indexer+topk": 2.0 * sh.H_I * sh.D_I * pairs_causal,
         "absorb_q": 2.0 * M * sh.H * sh.d_n * sh.d_c,
         "sparse_mla": 2.0 * sh.H * (2 * sh.d_c + sh.d_r) * pairs_sel,
         "absorb_v": 2.0 * M * sh.H * sh.d_c * sh.d_v,
     }
+    hbm_bytes = {
+        # k^I once, q^I, w, the fp32 scores written and read back, the selection written
+        "indexer+topk": wl.total_k * sh.D_I * ki_elt + M * sh.H_I * (sh.D_I * ki_elt + 4) + 8 * pairs_causal
+                        + 4 * M * sh.k,
+        "absorb_q": sh.H * sh.d_n * sh.d_c * elt + M * sh.H * (sh.d_n + sh.d_r) * elt
+                    + M * sh.H * (sh.d_c + sh.d_r) * elt,
+        # each distinct selected latent row once, q~ rows in, latent context out
+        "sparse_mla": min(pairs_sel, wl.total_k) * (sh.d_c + sh.d_r) * elt + M * sh.H * (sh.d_c + sh.d_r) * elt
+                      + M * sh.H * sh.d_c * elt + 4 * M * sh.k,
+        "absorb_v": sh.H * sh.d_c * sh.d_v * elt + M * sh.H * (sh.d_c + sh.d_v) * elt,
+    }
     names = ["quant", "indexer+topk", "absorb_q", "sparse_mla", "absorb_v"]
     stages = {n: {"ms": stage_ms[j]} for j, n in enumerate(names)}
     for n, f in flops.items():
-        stages[n]["tflops"] = f / (stages[n]["ms"] * 1e9) if stages[n]["ms"] > 0 else None
+        ok = stages[n]["ms"] > 0
+        stages[n]["tflops"] = f / (stages[n]["ms"] * 1e9) if ok else None
+        stages[n]["gbs"] = hbm_bytes[n] / (stages[n]["ms"] * 1e6) if ok else None
     dom = max(["sparse_mla", "indexer+topk", "absorb_q", "absorb_v"], key=lambda n: stages[n]["ms"])
-    achieved = stages[dom]["tflops"]
-    peak = peaks["bf16_tflops_sustained"]
-    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if flops[dom] / hbm_bytes[dom] >= ridge:
+        achieved, peak, unit, bound = stages[dom]["tflops"], peaks["bf16_tflops_sustained"], "TFLOP/s", "tensor"
+        psrc = f"{peak_src} bf16 sustained (kernel timed inside a step)"
+        alg = f"{flops[dom] / 1e9:.1f} GFLOP per launch"
+    else:
+        achieved, peak, unit, bound = stages[dom]["gbs"], peaks["hbm_gbs"], "GB/s", "hbm"
+        psrc = f"{peak_src} HBM copy bandwidth"
+        alg = f"{hbm_bytes[dom] / 1e6:.1f} MB per launch"
+    roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak if achieved else None,
                 "traffic": ncu_traffic(dom, CONFIG_NAMES[args.config]),
-                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a step)",
-                "algorithmic": f"{flops[dom] / 1e9:.1f} GFLOP per launch"}
+                "peak_source": psrc, "algorithmic": alg}
 
     e2e = None if args.no_e2e else measure_e2e(args, dsa, torch, dev, wl, host, t, seqs, out, lse, idx, ws)
     cpu = None
