@@ -1,25 +1,35 @@
 // Exact per-row top-k of the indexer scores (DeepSeek-V3.2-Exp atlas page,
 // M^sel_{t,s} = M_{t,s} for s in top_k(S~^I_t)): a radix select on
-// order-preserving uint32 keys.
+// order-preserving uint32 keys, one CTA per query row.
 //
-// One CTA per query row.  Only the causal keys 0..p are read, once: the first
-// pass converts them to keys and keeps them in shared memory when the row fits
-// the launch's cache (rows longer than that re-read global memory).  If there
-// are at most k causal keys they are all selected.  Otherwise three histogram passes
-// over 11 + 11 + 10 key bits (shared-memory histograms, atomics) find the
-// exact k-th largest key T and how many keys equal to T are needed; a final
-// ordered pass compacts, in increasing key order, every key above T and then
-// the first `need` keys equal to T (warp ballots + a block-wide prefix sum),
-// so equal scores resolve to the lower key index and the output is
+// Only the causal keys 0..p are read: the first pass converts them to keys
+// and keeps them in shared memory when the row fits the launch's cache
+// (longer rows re-read global memory).  If there are at most k causal keys
+// they are all selected.  Otherwise three histogram passes over 11 + 11 + 10
+// key bits (shared-memory histograms, atomics) find the exact k-th largest key
+// T and how many keys equal to T are needed; a final ordered pass compacts, in
+// increasing key order, every key above T and then the first `need` keys equal
+// to T, so equal scores resolve to the lower key index and the output is
 // deterministic.
+//
+// Two kernels for two regimes:
+//   * topk_radix_kernel (many rows, e.g. prefill): 512 threads, one key per
+//     thread per step, warp ballots + a block scan per 512 keys; four CTAs per
+//     SM hide each other's latency.
+//   * topk_radix_wide_kernel (few long rows, e.g. decode: fewer CTAs than
+//     SMs): 1024 threads, eight loads in flight per thread in the histogram
+//     passes, eight consecutive keys per thread in the ordered pass (one block
+//     scan per 8192 keys), the output row assembled in shared memory and
+//     written out coalesced.
 #include "dsa_common.cuh"
 
 namespace dsa {
 namespace {
 
+constexpr int MAX_BINS = 2048;
+
 constexpr int TK_THREADS = 512;
 constexpr int TK_WARPS = TK_THREADS / 32;
-constexpr int MAX_BINS = 2048;
 
 __global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(const float *__restrict__ scores, int64_t ld,
                                                                 const __grid_constant__ SeqTab st, int k,
@@ -147,22 +157,206 @@ __global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(const float *__r
     }
 }
 
+
+constexpr int KPT = 8;                // consecutive keys per thread in the ordered pass
+constexpr int CACHE_MAX = 48 * 1024;  // keys kept in shared memory (192 KB)
+
+constexpr int WIDE_THREADS = 1024;         // threads per row of the wide kernel
+constexpr int HB = 8;                 // keys per thread per iteration of a histogram pass
+
+__global__ void __launch_bounds__(WIDE_THREADS, 1) topk_radix_wide_kernel(const float *__restrict__ scores, int64_t ld,
+                                                             const __grid_constant__ SeqTab st, int k,
+                                                             int32_t *__restrict__ idx, int cache_cap) {
+    constexpr int WARPS = WIDE_THREADS / 32;
+    extern __shared__ uint32_t cache[];  // [cache_cap] keys, then [k] staged output indices
+    __shared__ uint32_t hist[MAX_BINS];
+    __shared__ uint32_t warp_tot[2][WARPS];
+    __shared__ int sel_bin, sel_above;
+
+    const int r = blockIdx.x;
+    const RowInfo ri = row_info(st, r);
+    const int n_live = min(ri.p + 1, ri.S);
+    const float *row = scores + (int64_t)r * ld;
+    int32_t *out = idx + (int64_t)r * k;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
+    if (n_live <= k) {
+        for (int j = tid; j < k; j += WIDE_THREADS) out[j] = j < n_live ? j : -1;
+        return;
+    }
+
+    const bool cached = n_live <= cache_cap;
+    auto key_at = [&](int s) -> uint32_t { return cached ? cache[s] : ordered_key(row[s]); };
+    uint32_t prefix = 0, pmask = 0;
+    int remaining = k;  // keys still to take among those matching the prefix
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int width = pass == 2 ? 10 : 11;
+        const uint32_t nb = 1u << width;
+        for (int b = tid; b < (int)nb; b += WIDE_THREADS) hist[b] = 0;
+        __syncthreads();
+        // HB loads in flight per thread before their atomics: uncached rows read global memory,
+        // and one dependent round trip per key would bound the pass by latency.
+#pragma unroll 1
+        for (int s0 = 0; s0 < n_live; s0 += HB * WIDE_THREADS) {
+            uint32_t u[HB];
+#pragma unroll
+            for (int j = 0; j < HB; ++j) {
+                const int s = s0 + j * WIDE_THREADS + tid;
+                u[j] = 0;
+                if (s < n_live) {
+                    if (pass == 0) {
+                        u[j] = ordered_key(row[s]);
+                        if (cached) cache[s] = u[j];
+                    } else {
+                        u[j] = key_at(s);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < HB; ++j) {
+                const int s = s0 + j * WIDE_THREADS + tid;
+                if (s < n_live && (u[j] & pmask) == prefix) atomicAdd(&hist[(u[j] >> shift) & (nb - 1)], 1u);
+            }
+        }
+        __syncthreads();
+        if (wid == 0) {
+            // Lane l owns the bins [nb - (l+1)*per, nb - l*per), scanned from the top.
+            const int per = (int)nb / 32;
+            const int hi = (int)nb - lane * per;
+            int mine = 0;
+            for (int b = hi - 1; b >= hi - per; --b) mine += (int)hist[b];
+            int incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const int excl = incl - mine;
+            if (excl < remaining && remaining <= incl) {
+                int cum = excl;
+                for (int b = hi - 1; b >= hi - per; --b) {
+                    const int h = (int)hist[b];
+                    if (cum + h >= remaining) {
+                        sel_bin = b;
+                        sel_above = cum;
+                        break;
+                    }
+                    cum += h;
+                }
+            }
+        }
+        __syncthreads();
+        remaining -= sel_above;
+        prefix |= (uint32_t)sel_bin << shift;
+        pmask |= (nb - 1) << shift;
+        __syncthreads();  // sel_* are rewritten by the next pass
+    }
+
+    // prefix is now the k-th largest key T; (k - remaining) keys are above it.
+    const uint32_t T = prefix;
+    const int n_gt = k - remaining;
+    // Rows that are not cached stage each chunk of keys in the (unused) cache
+    // so that a thread can read 8 consecutive ones.  The output row is
+    // assembled in shared memory and written out coalesced at the end.
+    uint32_t *stage = cache;
+    int32_t *out_s = (int32_t *)(cache + cache_cap);
+    int base_gt = 0, base_eq = 0;
+#pragma unroll 1
+    for (int c = 0, s0 = 0; s0 < n_live; ++c, s0 += KPT * WIDE_THREADS) {
+        if (!cached) {
+            __syncthreads();  // the previous chunk's reads of the staging area are done
+            for (int j = 0; j < KPT; ++j) {
+                const int s = s0 + j * WIDE_THREADS + tid;
+                stage[j * WIDE_THREADS + tid] = s < n_live ? ordered_key(row[s]) : 0u;
+            }
+            __syncthreads();
+        }
+        const int first = s0 + tid * KPT;
+        const uint32_t *src = cached ? cache + first : stage + tid * KPT;  // 32-byte aligned
+        uint32_t u[KPT];
+        if (first + KPT <= n_live) {
+            const uint4 a = ((const uint4 *)src)[0], b = ((const uint4 *)src)[1];
+            u[0] = a.x, u[1] = a.y, u[2] = a.z, u[3] = a.w, u[4] = b.x, u[5] = b.y, u[6] = b.z, u[7] = b.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < KPT; ++j) u[j] = first + j < n_live ? src[j] : 0u;
+        }
+        int g = 0, e = 0;
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+            const bool valid = first + j < n_live;
+            g += valid && u[j] > T;
+            e += valid && u[j] == T;
+        }
+        // block-wide exclusive prefix of (g, e), packed as g + e * 2^16
+        const uint32_t mine = (uint32_t)g | ((uint32_t)e << 16);
+        uint32_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        uint32_t *wt = warp_tot[c & 1];
+        if (lane == 31) wt[wid] = incl;
+        __syncthreads();
+        uint32_t before = 0, total = 0;
+        for (int w = 0; w < WARPS; ++w) {
+            const uint32_t v = wt[w];
+            before += w < wid ? v : 0u;
+            total += v;
+        }
+        const uint32_t excl = before + incl - mine;
+        int rg = base_gt + (int)(excl & 0xffffu), re = base_eq + (int)(excl >> 16);
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+            const int s = first + j;
+            if (s < n_live && u[j] > T) {
+                if (rg < n_gt) out_s[rg] = s;
+                ++rg;
+            } else if (s < n_live && u[j] == T) {
+                if (re < remaining) out_s[n_gt + re] = s;
+                ++re;
+            }
+        }
+        base_gt += (int)(total & 0xffffu);
+        base_eq += (int)(total >> 16);
+        if (base_gt >= n_gt && base_eq >= remaining) break;  // block-uniform: every slot is written
+    }
+    __syncthreads();
+    for (int j = tid; j < k; j += WIDE_THREADS) out[j] = out_s[j];
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int total_q, int k, int32_t *idx,
                         cudaStream_t s) {
     if (total_q == 0) return cudaSuccess;
-    // Shared-memory key cache: the longest causal row of the launch, at most 32768 keys (128 KB).
-    int max_live = 0;
+    int max_live = 0;  // the longest causal row of the launch
     for (int b = 0; b < st.B; ++b) {
         const int T = st.q_off[b + 1] - st.q_off[b];
         if (T > 0) max_live = max(max_live, min(st.start_pos[b] + T, st.k_len[b]));
     }
-    const int cap = max_live <= k ? 0 : min(max_live, 32768);
-    const size_t smem = (size_t)cap * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_radix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e;
+    if (total_q < 2 * 152) {
+        // Few rows: the wide kernel.  Its dynamic shared memory (200 KB) holds the key cache (at
+        // least one chunk: it is also the staging area of the ordered pass for longer rows) and
+        // the staged output row.
+        constexpr int words = 50 * 1024, chunk = KPT * WIDE_THREADS;
+        if (max_live > k && k + chunk > words) return cudaErrorInvalidValue;
+        const int cap = max_live <= k ? 0 : max(min(max_live, min(CACHE_MAX, words - k)), chunk);
+        const size_t smem = ((size_t)cap + (size_t)k) * sizeof(uint32_t);
+        e = cudaFuncSetAttribute(topk_radix_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) topk_radix_wide_kernel<<<total_q, WIDE_THREADS, smem, s>>>(scores, ld, st, k, idx, cap);
+    } else {
+        // Many rows: the cache is the longest causal row, at most 32768 keys (128 KB).
+        const int cap = max_live <= k ? 0 : min(max_live, 32768);
+        const size_t smem = (size_t)cap * sizeof(uint32_t);
+        e = cudaFuncSetAttribute(topk_radix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) topk_radix_kernel<<<total_q, TK_THREADS, smem, s>>>(scores, ld, st, k, idx, cap);
+    }
     if (e != cudaSuccess) return e;
-    topk_radix_kernel<<<total_q, TK_THREADS, smem, s>>>(scores, ld, st, k, idx, cap);
     note_launch(DSA_KERNEL_TOPK);
     return cudaGetLastError();
 }

@@ -111,28 +111,32 @@ def test_topk(name):
         H.check_selection_row(idx[r], o["scores"], o["absterm"], p, k)
 
 
+# A launch with fewer than 2 x 152 rows takes the wide top-k kernel (decode); more rows take the
+# many-rows kernel (prefill).  The cases below run on both sides of that switch.
+@pytest.mark.parametrize("T", [700, 100])
 @pytest.mark.parametrize("fill", [1.0, 0.0, -3.5])
-def test_topk_all_equal_scores(fill):
+def test_topk_all_equal_scores(fill, T):
     """Every score equal: the lowest key indices win."""
-    T = S = 700
+    S = 700
     k = 100
-    seqs = dsa.Seqs.from_lengths([T], [S], [0])
-    scores = torch.full((T, 700), fill, dtype=torch.float32, device="cuda")
+    seqs = dsa.Seqs.from_lengths([T], [S], [S - T])
+    scores = torch.full((T, S), fill, dtype=torch.float32, device="cuda")
     if fill == 0.0:
         scores[:, ::2] = -0.0  # -0 and +0 are the same score
     idx = dsa.dsa_topk_select(scores, seqs, k).cpu().numpy()
     for r in range(T):
-        n = min(k, r + 1)
+        n = min(k, S - T + r + 1)
         assert sorted(idx[r, :n].tolist()) == list(range(n))
         assert np.all(idx[r, n:] == -1)
 
 
-def test_topk_threshold_ties_and_large_rows():
+@pytest.mark.parametrize("rows", [24, 320])
+def test_topk_threshold_ties_and_large_rows(rows):
     """Scores on a coarse grid (many exact ties at the threshold), rows up to
-    65536 keys; exact equality with the CPU top-k of the same buffer."""
+    65536 keys (beyond either kernel's shared-memory key cache); exact equality
+    with the CPU top-k of the same buffer."""
     g = torch.Generator().manual_seed(5)
     S = 65536
-    rows = 24
     seqs = dsa.Seqs([0, rows], [0, S], [S - rows])
     scores = torch.randint(-40, 40, (rows, S), generator=g).float() / 8
     idx = dsa.dsa_topk_select(scores.cuda(), seqs, 2048).cpu().numpy()
