@@ -326,9 +326,9 @@ def run_ours(args, world, rank, local):
         # k^I once, q^I, w, the fp32 scores written and read back, the selection written
         "indexer+topk": wl.total_k * sh.D_I * ki_elt + M * sh.H_I * (sh.D_I * ki_elt + 4) + 8 * pairs_causal
                         + 4 * M * sh.k,
-        "absorb_q": sh.H * sh.d_n * sh.d_c * elt + M * sh.H * (sh.d_n + sh.d_r) * elt
-                    + M * sh.H * (sh.d_c + sh.d_r) * elt,
-        # each distinct selected latent row once, q~ rows in, latent context out
+        # W_UK, q_nope in, q~ out (the attention reads q_pe in place)
+        "absorb_q": sh.H * sh.d_n * sh.d_c * elt + M * sh.H * sh.d_n * elt + M * sh.H * sh.d_c * elt,
+        # each distinct selected latent row once, q~ and q_pe rows in, latent context out
         "sparse_mla": min(pairs_sel, wl.total_k) * (sh.d_c + sh.d_r) * elt + M * sh.H * (sh.d_c + sh.d_r) * elt
                       + M * sh.H * sh.d_c * elt + 4 * M * sh.k,
         "absorb_v": sh.H * sh.d_c * sh.d_v * elt + M * sh.H * (sh.d_c + sh.d_v) * elt,

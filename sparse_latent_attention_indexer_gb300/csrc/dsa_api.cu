@@ -124,8 +124,8 @@ namespace dsa {
 // both fp32 [M, H, d_c] on the generic path.
 MlaWs mla_ws_layout(int H, int d_c, int64_t total_q) {
     // Generic path: q~ and the latent context in fp32.  Tensor-core path: the
-    // bf16 [q~ | q_pe] rows and bf16 context fit in the same two regions, plus
-    // the split partials of short batches.
+    // bf16 q~ rows and bf16 context fit in the same two regions, plus the split
+    // partials of short batches.
     MlaWs w;
     const size_t per = align_up((size_t)total_q * H * d_c * sizeof(float));
     w.qt = 0;
@@ -145,19 +145,18 @@ int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int
     const bool fast = !force_generic() && absorb_tc_supported(dtype, H, d_n, d_r, d_c, d_v) && aligned(q_nope, 16) &&
                       aligned(q_pe, 16) && aligned(W_UK, 16) && aligned(W_UV, 16) && aligned(out, 16);
     if (fast) {
-        // q~ rows [M, H, d_c + d_r] bf16 = [q_nope W_UK | q_pe]; latent context bf16 [M, H, d_c].
+        // q~ rows [M, H, d_c] bf16 = q_nope W_UK (q_pe is read in place); latent context bf16 [M, H, d_c].
         __nv_bfloat16 *qt = (__nv_bfloat16 *)(ws + L.qt);
         __nv_bfloat16 *olat = (__nv_bfloat16 *)(ws + L.olat);
-        const int W = d_c + d_r;
-        e = launch_absorb_q_tc(q_nope, W_UK, q_pe, qt, M, H, d_r, s);
+        e = launch_absorb_q_tc(q_nope, W_UK, qt, M, H, s);
         if (e != cudaSuccess) return fail_cuda(e);
         if (mark) stage_mark(3, s);
         if (mla_tc_supported(dtype, H, d_n, d_r, d_c, d_v) && aligned(kv, 16) && aligned(k_pe, 16) && ld_kv % 8 == 0 &&
             ld_pe % 8 == 0)
-            e = launch_mla_tc(qt, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, bt.total_k, M, scale, prefix_valid, olat, lse,
-                              ws + L.part, s);
+            e = launch_mla_tc(qt, q_pe, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, bt.total_k, M, scale, prefix_valid, olat,
+                              lse, ws + L.part, s);
         else
-            e = launch_mla_simt(qt, DSA_BF16, W, qt + d_c, W, dtype, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, M, H, d_r,
+            e = launch_mla_simt(qt, DSA_BF16, d_c, q_pe, d_r, dtype, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, M, H, d_r,
                                 d_c, scale, olat, DSA_BF16, lse, s);
         if (e != cudaSuccess) return fail_cuda(e);
         if (mark) stage_mark(4, s);

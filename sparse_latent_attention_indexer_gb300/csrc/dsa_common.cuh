@@ -137,21 +137,20 @@ cudaError_t launch_mla_simt(const void *qt, int qt_dtype, int qt_ld, const void 
                             int olat_dtype, float *lse, cudaStream_t s);
 
 // tcgen05 absorption GEMMs (bf16, d_n = 128, d_c = 512, d_v = 128):
-// qt [M, H, 512 + d_r] = [q_nope W_UK | q_pe];  out [M, H, 128] = olat W_UV.
+// qt [M, H, 512] = q_nope W_UK;  out [M, H, 128] = olat W_UV.
 bool absorb_tc_supported(int dtype, int H, int d_n, int d_r, int d_c, int d_v);
-cudaError_t launch_absorb_q_tc(const void *q_nope, const void *W_UK, const void *q_pe, void *qt, int M, int H,
-                               int d_r, cudaStream_t s);
+cudaError_t launch_absorb_q_tc(const void *q_nope, const void *W_UK, void *qt, int M, int H, cudaStream_t s);
 cudaError_t launch_absorb_v_tc(const void *olat, const void *W_UV, void *out, int M, int H, cudaStream_t s);
 int absorb_tc_read_error(int *site);
 
-// tcgen05 sparse latent attention (bf16, H = 128, d_c = 512, d_r = 64): qt rows
-// [M, 128, 576] = [q~ | q_pe] -> olat [M, 128, 512] bf16 and lse.  Rows with
+// tcgen05 sparse latent attention (bf16, H = 128, d_c = 512, d_r = 64): q~ rows
+// [M, 128, 512] and q_pe rows [M, 128, 64] -> olat [M, 128, 512] bf16 and lse.  Rows with
 // few entries per split write fp32 partials to part_ws (mla_tc_partial_bytes)
 // and a combine kernel merges them.
 bool mla_tc_supported(int dtype, int H, int d_n, int d_r, int d_c, int d_v);
 int mla_tc_splits(int M);
 size_t mla_tc_partial_bytes(int M);
-cudaError_t launch_mla_tc(const void *qt, const void *kv, int64_t ld_kv, const void *kpe, int64_t ld_pe,
+cudaError_t launch_mla_tc(const void *qt, const void *qpe, const void *kv, int64_t ld_kv, const void *kpe, int64_t ld_pe,
                           const int32_t *idx, int k, const SeqTab &st, int64_t total_k, int M, float scale,
                           bool prefix_valid, void *olat, float *lse, void *part_ws, cudaStream_t s);
 int mla_tc_read_error(int *site);

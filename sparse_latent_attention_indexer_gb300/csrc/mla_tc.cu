@@ -12,8 +12,8 @@
 // row is handled by a cluster of two CTAs on two SMs.  CTA c owns latent
 // columns 256c..256c+255 and rope columns 32c..32c+31 of q~ and of every key,
 // so both gather the same 576 bytes per key.
-//   * q~ slice: loaded once into tensor memory (the A operand of QK^T, so
-//     the score MMA reads only the key tile from shared memory).
+//   * q~ and q_pe slices: loaded once into tensor memory (the A operand of
+//     QK^T, so the score MMA reads only the key tile from shared memory).
 //   * Key tiles (64 keys): four gathering warps copy the selected rows with
 //     cp.async (8 lanes per 128-byte segment, 128-byte swizzle for the latent
 //     slabs, 64-byte swizzle for the rope half) into a 4-stage ring; a copy's
@@ -49,7 +49,7 @@ namespace {
 
 constexpr int NH = 128;                      // heads (MMA M)
 constexpr int DC = 512;                      // latent width
-constexpr int QW = 576;                      // q~ row: [q~ (512) | q_pe (64)]
+constexpr int DR = 64;                       // rope width (q_pe rows)
 constexpr int BK = 64;                       // keys per tile (MMA N of QK^T, K of PV)
 // Each CTA of the pair holds 4 latent slabs (64 columns, 128-byte rows) and half of the rope
 // part (32 columns, 64-byte rows) of every key: CTA c owns latent 256c..256c+255, rope 32c..32c+31.
@@ -98,7 +98,8 @@ struct Bars {
 
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most 4 per SM sub-partition x 128 regs
     mla_tc_kernel(const __nv_bfloat16 *__restrict__ kv, int64_t ld_kv, const __nv_bfloat16 *__restrict__ kpe,
-                  int64_t ld_pe, const __nv_bfloat16 *__restrict__ qt, const int32_t *__restrict__ idx,
+                  int64_t ld_pe, const __nv_bfloat16 *__restrict__ qt, const __nv_bfloat16 *__restrict__ qpe,
+                  const int32_t *__restrict__ idx,
                   const __grid_constant__ MlaParams P, __nv_bfloat16 *__restrict__ olat, float *__restrict__ lse,
                   float *__restrict__ opart, float *__restrict__ lpart) {
     extern __shared__ uint8_t smem_raw[];
@@ -266,7 +267,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             // This CTA's slice of the head's q~ row -> tensor memory (A operand of QK^T): latent
             // columns as 4 slabs of 32 packed columns, then the rope half as 16 more; the two
             // threads of a row split the slabs and the second one also takes the rope half.
-            const __nv_bfloat16 *qrow = qt + ((int64_t)r * NH + h) * QW;
+            const __nv_bfloat16 *qrow = qt + ((int64_t)r * NH + h) * DC;
             const uint4 *src = (const uint4 *)(qrow + rank * 256);
             for (int js = hf * 2; js < hf * 2 + 2; ++js) {
                 uint32_t qv[32];
@@ -281,7 +282,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                 tc::tmem_st32(tmem + lane_off + COL_Q + js * 32, qv);
             }
             if (hf) {
-                const uint4 *rsrc = (const uint4 *)(qrow + DC + rank * 32);
+                const uint4 *rsrc = (const uint4 *)(qpe + ((int64_t)r * NH + h) * DR + rank * 32);
                 uint32_t qv[16];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -571,7 +572,7 @@ size_t mla_tc_partial_bytes(int M) {
     return (size_t)M * s * NH * DC * sizeof(float) + 256 + (size_t)M * s * NH * sizeof(float);
 }
 
-cudaError_t launch_mla_tc(const void *qt, const void *kv, int64_t ld_kv, const void *kpe, int64_t ld_pe,
+cudaError_t launch_mla_tc(const void *qt, const void *qpe, const void *kv, int64_t ld_kv, const void *kpe, int64_t ld_pe,
                           const int32_t *idx, int k, const SeqTab &st, int64_t total_k, int M, float scale,
                           bool prefix_valid, void *olat, float *lse, void *part_ws, cudaStream_t s) {
     if (M == 0) return cudaSuccess;
@@ -598,7 +599,8 @@ cudaError_t launch_mla_tc(const void *qt, const void *kv, int64_t ld_kv, const v
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)M * P.splits * 2;
     mla_tc_kernel<<<grid, NUM_THREADS, SMEM, s>>>((const __nv_bfloat16 *)kv, ld_kv, (const __nv_bfloat16 *)kpe, ld_pe,
-                                                   (const __nv_bfloat16 *)qt, idx, P, (__nv_bfloat16 *)olat, lse,
+                                                   (const __nv_bfloat16 *)qt, (const __nv_bfloat16 *)qpe, idx, P,
+                                                   (__nv_bfloat16 *)olat, lse,
                                                    opart, lpart);
     note_launch(DSA_KERNEL_MLA_TC);
     e = cudaGetLastError();
