@@ -328,6 +328,229 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1) topk_radix_wide_kernel(const 
     for (int j = tid; j < k; j += WIDE_THREADS) out[j] = out_s[j];
 }
 
+// ---------------------------------------------------------------------------
+// Few long rows (decode): a cluster of CL CTAs per row.  CTA c takes the c-th
+// contiguous slice of the row's causal keys and keeps its keys in shared
+// memory.  Each radix pass builds a per-CTA histogram; after a cluster
+// barrier every CTA sums the CL histograms through distributed shared memory
+// and makes the same bin decision.  The final pass counts each slice's keys
+// above / equal to the threshold, exchanges the counts, and every CTA writes
+// its own keys at their ranks in index order: the output is the same as the
+// one-CTA kernels'.
+// ---------------------------------------------------------------------------
+constexpr int CL = 8;              // CTAs per row
+constexpr int CT = 256;            // threads per CTA
+constexpr int CT_WARPS = CT / 32;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t peer_addr(const void *local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(r)
+                 : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint4 ld_peer_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(CT)
+    topk_cluster_kernel(const float *__restrict__ scores, int64_t ld, const __grid_constant__ SeqTab st, int k,
+                        int32_t *__restrict__ idx) {
+    extern __shared__ __align__(16) uint32_t slice[];  // this CTA's keys
+    __shared__ __align__(16) uint32_t hist[2][MAX_BINS];
+    __shared__ __align__(16) uint32_t merged[MAX_BINS];
+    __shared__ __align__(16) uint32_t counts[4];       // (above, equal) of this slice
+    __shared__ uint32_t warp_tot[2][CT_WARPS];
+    __shared__ int sel_bin, sel_above;
+
+    const int r = blockIdx.x / CL;
+    const uint32_t c = cluster_ctarank();
+    const RowInfo ri = row_info(st, r);
+    const int n_live = min(ri.p + 1, ri.S);
+    const float *row = scores + (int64_t)r * ld;
+    int32_t *out = idx + (int64_t)r * k;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid < 4) counts[tid] = 0;  // ordered before the final pass's atomics by the passes' barriers
+
+    if (n_live <= k) {  // the whole cluster takes this branch: no cluster barrier is pending
+        if (c == 0)
+            for (int j = tid; j < k; j += CT) out[j] = j < n_live ? j : -1;
+        return;
+    }
+    const int s_lo = (int)((int64_t)c * n_live / CL), n = (int)((int64_t)(c + 1) * n_live / CL) - s_lo;
+
+    uint32_t prefix = 0, pmask = 0;
+    int remaining = k;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int width = pass == 2 ? 10 : 11;
+        const uint32_t nb = 1u << width;
+        uint32_t *h = hist[pass & 1];
+        for (int b = tid; b < (int)nb; b += CT) h[b] = 0;
+        __syncthreads();
+        if (pass == 0) {
+#pragma unroll 1
+            for (int s0 = 0; s0 < n; s0 += HB * CT) {
+                uint32_t u[HB];
+#pragma unroll
+                for (int j = 0; j < HB; ++j) {
+                    const int s = s0 + j * CT + tid;
+                    u[j] = s < n ? ordered_key(row[s_lo + s]) : 0u;
+                }
+#pragma unroll
+                for (int j = 0; j < HB; ++j) {
+                    const int s = s0 + j * CT + tid;
+                    if (s < n) {
+                        slice[s] = u[j];
+                        atomicAdd(&h[u[j] >> shift], 1u);
+                    }
+                }
+            }
+        } else {
+            for (int s = tid; s < n; s += CT) {
+                const uint32_t u = slice[s];
+                if ((u & pmask) == prefix) atomicAdd(&h[(u >> shift) & (nb - 1)], 1u);
+            }
+        }
+        // Every CTA's histogram of this pass is complete (and the previous pass's reads of
+        // the other buffer are done) once the whole cluster has arrived.
+        cluster_barrier();
+        for (int q4 = tid; q4 < (int)nb / 4; q4 += CT) {
+            uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int cc = 0; cc < CL; ++cc) {
+                const uint4 v = ld_peer_v4(peer_addr(h + 4 * q4, (uint32_t)cc));
+                acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+            }
+            *(uint4 *)(merged + 4 * q4) = acc;
+        }
+        __syncthreads();
+        if (wid == 0) {
+            // Lane l owns the bins [nb - (l+1)*per, nb - l*per), scanned from the top.
+            const int per = (int)nb / 32;
+            const int hi = (int)nb - lane * per;
+            int mine = 0;
+            for (int b = hi - 1; b >= hi - per; --b) mine += (int)merged[b];
+            int incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const int excl = incl - mine;
+            if (excl < remaining && remaining <= incl) {
+                int cum = excl;
+                for (int b = hi - 1; b >= hi - per; --b) {
+                    const int hb = (int)merged[b];
+                    if (cum + hb >= remaining) {
+                        sel_bin = b;
+                        sel_above = cum;
+                        break;
+                    }
+                    cum += hb;
+                }
+            }
+        }
+        __syncthreads();
+        remaining -= sel_above;
+        prefix |= (uint32_t)sel_bin << shift;
+        pmask |= (nb - 1) << shift;
+        __syncthreads();  // sel_* and merged[] are rewritten by the next pass
+    }
+
+    // prefix is now the k-th largest key T of the row; (k - remaining) keys are above it.
+    const uint32_t T = prefix;
+    const int n_gt = k - remaining;
+    {
+        uint32_t g = 0, e = 0;
+        for (int s = tid; s < n; s += CT) {
+            g += slice[s] > T;
+            e += slice[s] == T;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            e += __shfl_xor_sync(0xffffffffu, e, o);
+        }
+        if (lane == 0) {
+            atomicAdd(&counts[0], g);
+            atomicAdd(&counts[1], e);
+        }
+    }
+    __syncthreads();
+    cluster_barrier();
+    // ranks of this slice's first key above / equal to T among the row's keys
+    int base_gt = 0, base_eq = 0;
+    for (uint32_t cc = 0; cc < c; ++cc) {
+        const uint4 v = ld_peer_v4(peer_addr(counts, cc));
+        base_gt += (int)v.x;
+        base_eq += (int)v.y;
+    }
+    // No CTA may leave while another can still read its counts.
+    cluster_barrier();
+#pragma unroll 1
+    for (int ch = 0, s0 = 0; s0 < n; ++ch, s0 += KPT * CT) {
+        if (base_gt >= n_gt && base_eq >= remaining) break;  // block-uniform: nothing left to place
+        const int first = s0 + tid * KPT;
+        uint32_t u[KPT];
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) u[j] = first + j < n ? slice[first + j] : 0u;
+        int g = 0, e = 0;
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+            const bool valid = first + j < n;
+            g += valid && u[j] > T;
+            e += valid && u[j] == T;
+        }
+        // block-wide exclusive prefix of (g, e), packed as g + e * 2^16
+        const uint32_t mine = (uint32_t)g | ((uint32_t)e << 16);
+        uint32_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        uint32_t *wt = warp_tot[ch & 1];
+        if (lane == 31) wt[wid] = incl;
+        __syncthreads();
+        uint32_t before = 0, total = 0;
+        for (int w = 0; w < CT_WARPS; ++w) {
+            const uint32_t v = wt[w];
+            before += w < wid ? v : 0u;
+            total += v;
+        }
+        const uint32_t excl = before + incl - mine;
+        int rg = base_gt + (int)(excl & 0xffffu), re = base_eq + (int)(excl >> 16);
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+            const int s = first + j;
+            if (s < n && u[j] > T) {
+                if (rg < n_gt) out[rg] = s_lo + s;
+                ++rg;
+            } else if (s < n && u[j] == T) {
+                if (re < remaining) out[n_gt + re] = s_lo + s;
+                ++re;
+            }
+        }
+        base_gt += (int)(total & 0xffffu);
+        base_eq += (int)(total >> 16);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int total_q, int k, int32_t *idx,
@@ -339,7 +562,13 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int t
         if (T > 0) max_live = max(max_live, min(st.start_pos[b] + T, st.k_len[b]));
     }
     cudaError_t e;
-    if (total_q < 2 * 152) {
+    // Few long rows: a cluster of CTAs per row when each CTA's slice fits its shared memory.
+    const int slice_cap = (max_live + CL - 1) / CL;
+    if (total_q < 2 * 152 && max_live > k && slice_cap <= 48 * 1024) {
+        const size_t smem = (size_t)slice_cap * sizeof(uint32_t);
+        e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) topk_cluster_kernel<<<total_q * CL, CT, smem, s>>>(scores, ld, st, k, idx);
+    } else if (total_q < 2 * 152) {
         // Few rows: the wide kernel.  Its dynamic shared memory (200 KB) holds the key cache (at
         // least one chunk: it is also the staging area of the ordered pass for longer rows) and
         // the staged output row.

@@ -111,8 +111,9 @@ def test_topk(name):
         H.check_selection_row(idx[r], o["scores"], o["absterm"], p, k)
 
 
-# A launch with fewer than 2 x 152 rows takes the wide top-k kernel (decode); more rows take the
-# many-rows kernel (prefill).  The cases below run on both sides of that switch.
+# A launch with fewer than 2 x 152 rows takes the cluster top-k kernel (decode: eight CTAs per row),
+# or the wide one-CTA-per-row kernel when a row's slices would not fit the CTAs' shared memory; more
+# rows take the many-rows kernel (prefill).  The cases below run on every side of those switches.
 @pytest.mark.parametrize("T", [700, 100])
 @pytest.mark.parametrize("fill", [1.0, 0.0, -3.5])
 def test_topk_all_equal_scores(fill, T):
@@ -133,8 +134,8 @@ def test_topk_all_equal_scores(fill, T):
 @pytest.mark.parametrize("rows", [24, 320])
 def test_topk_threshold_ties_and_large_rows(rows):
     """Scores on a coarse grid (many exact ties at the threshold), rows up to
-    65536 keys (beyond either kernel's shared-memory key cache); exact equality
-    with the CPU top-k of the same buffer."""
+    65536 keys (cluster kernel for 24 rows, beyond the many-rows kernel's key
+    cache for 320 rows); exact equality with the CPU top-k of the same buffer."""
     g = torch.Generator().manual_seed(5)
     S = 65536
     seqs = dsa.Seqs([0, rows], [0, S], [S - rows])
@@ -144,6 +145,21 @@ def test_topk_threshold_ties_and_large_rows(rows):
     for r in range(rows):
         p = S - rows + r
         want = H.cpu_topk_same_buffer(sc[r], p, 2048)
+        assert sorted(idx[r].tolist()) == sorted(want.tolist())
+
+
+def test_topk_rows_longer_than_the_cluster_cache():
+    """Two rows of 400,000 causal keys (beyond eight CTAs' shared memory: the
+    wide kernel, which re-reads global memory); exact equality with the CPU
+    top-k of the same buffer, ties included."""
+    g = torch.Generator().manual_seed(6)
+    rows, S, k = 2, 400_000, 2048
+    seqs = dsa.Seqs([0, rows], [0, S], [S - rows])
+    scores = torch.randint(-400, 400, (rows, S), generator=g).float() / 16
+    idx = dsa.dsa_topk_select(scores.cuda(), seqs, k).cpu().numpy()
+    sc = scores.numpy()
+    for r in range(rows):
+        want = H.cpu_topk_same_buffer(sc[r], S - rows + r, k)
         assert sorted(idx[r].tolist()) == sorted(want.tolist())
 
 
