@@ -42,6 +42,7 @@ constexpr int DI = 128;         // indexer head dim
 constexpr int BN = TOK * HI;    // 256 (MMA N)
 constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
+constexpr int SPLIT_TAB = 2 * 152;  // launches with fewer query groups split each group's key blocks
 
 template <bool FP8>
 struct Cfg {
@@ -53,8 +54,6 @@ struct Cfg {
     static constexpr int A_HALF = BM * 128;
     static constexpr int STAGES = FP8 ? 6 : 4;
     static constexpr int KSTEPS = FP8 ? 4 : 8;              // MMAs per block (K = 32 / 16 each)
-    static constexpr uint32_t IDESC =
-        FP8 ? tc::instr_desc(tc::kFmtE4M3, tc::kFmtE4M3, BM, BN, 0, 0) : tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, BM, BN, 0, 0);
     static constexpr int SMEM = 1024 /*align slack*/ + B_BYTES + STAGES * A_BYTES + TOK * HI * 4 + 256;
 };
 
@@ -66,7 +65,13 @@ struct IdxParams {
     int start_pos[DSA_MAX_SEQS];
     int g_off[DSA_MAX_SEQS + 1];  // cumulative query groups
     int total_groups;
-    int splits;                    // CTAs per group (strided key blocks)
+    int splits;                    // CTAs per group (strided key blocks) when every group gets the same
+    // Few groups (decode): group g_of[i] gets s_off[i+1] - s_off[i] CTAs, about one per `target`
+    // key blocks, and the table lists groups by decreasing blocks per CTA (heaviest CTAs first).
+    int balanced;
+    int n_tab;
+    int s_off[SPLIT_TAB + 1];
+    int g_of[SPLIT_TAB];
     int fill_future;
     int64_t ld;
     float c;
@@ -93,8 +98,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Heavier groups (later tokens of a sequence see more keys) start first.
-    const int lin = P.total_groups * P.splits - 1 - (int)blockIdx.x;
-    const int g = lin / P.splits, split = lin % P.splits;
+    int g, split, splits;
+    if (P.balanced) {
+        int lo = 0, hi = P.n_tab - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (P.s_off[mid] <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+        }
+        g = P.g_of[lo];
+        split = (int)blockIdx.x - P.s_off[lo];
+        splits = P.s_off[lo + 1] - P.s_off[lo];
+    } else {
+        const int lin = P.total_groups * P.splits - 1 - (int)blockIdx.x;
+        g = lin / P.splits;
+        split = lin % P.splits;
+        splits = P.splits;
+    }
     int b = 0;
     {
         int lo = 0, hi = P.B - 1;
@@ -111,7 +130,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int p0 = P.start_pos[b] + t0;
     const int S = P.k_len[b], kbase = P.k_base[b];
     const int nblk = (p0 + ntok - 1) / BM + 1;  // blocks holding keys 0 .. last position
-    const int mine = split < nblk ? (nblk - split + P.splits - 1) / P.splits : 0;
+    const int mine = split < nblk ? (nblk - split + splits - 1) / splits : 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::STAGES; ++i) {
@@ -159,7 +178,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int i = 0; i < mine; ++i) {
                 const int st = i % C::STAGES;
                 if (!tc::mbar_wait(&empty[st], ((i / C::STAGES) & 1) ^ 1, abort_flag, &g_indexer_tc_error, 1)) break;
-                const int row = kbase + (split + i * P.splits) * BM;
+                const int row = kbase + (split + i * splits) * BM;
                 tc::mbar_arrive_expect_tx(&full[st], C::A_BYTES);
                 for (int h = 0; h < C::HALVES; ++h)
                     tc::tma_load_2d(As + st * C::A_BYTES + h * C::A_HALF, &tm_k, &full[st], h * 64, row);
@@ -172,6 +191,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else if (warp == 1 && lane == 0) {
             // ---------------- MMA issuer ----------------
             bool ok = tc::mbar_wait(bfull, 0, abort_flag, &g_indexer_tc_error, 4);
+            // Only the group's valid tokens are multiplied: N = 64 heads x ntok.
+            const uint32_t idesc = FP8 ? tc::instr_desc(tc::kFmtE4M3, tc::kFmtE4M3, BM, HI * ntok, 0, 0)
+                                       : tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, BM, HI * ntok, 0, 0);
             int issued = 0;
             for (int i = 0; ok && i < mine; ++i) {
                 const int st = i % C::STAGES, acc = i & 1;
@@ -186,8 +208,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int slab = FP8 ? 0 : kk / 4, off = (FP8 ? kk : kk % 4) * 32;
                     const uint64_t ad = tc::smem_desc(a0 + slab * C::A_HALF + off, 16, 1024);
                     const uint64_t bd = tc::smem_desc(b0 + slab * C::B_HALF + off, 16, 1024);
-                    if (FP8) tc::mma_f8(d, ad, bd, C::IDESC, kk > 0);
-                    else tc::mma_f16(d, ad, bd, C::IDESC, kk > 0);
+                    if (FP8) tc::mma_f8(d, ad, bd, idesc, kk > 0);
+                    else tc::mma_f16(d, ad, bd, idesc, kk > 0);
                 }
                 tc::mma_commit(&empty[st]);
                 tc::mma_commit(&tfull[acc]);
@@ -206,11 +228,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int acc = i & 1;
                 if (!tc::mbar_wait(&tfull[acc], (i >> 1) & 1, abort_flag, &g_indexer_tc_error, 8)) break;
                 tc::tc_fence_after();
-                const int key = (split + i * P.splits) * BM + q * 32 + lane;
+                const int key = (split + i * splits) * BM + q * 32 + lane;
                 const float ks = (FP8 && key < S) ? k_scale[kbase + key] : 1.0f;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int tt = 2 * hf + j;
+                // The two warps of a lane quarter take alternate tokens; absent tokens are skipped.
+#pragma unroll 1
+                for (int tt = hf; tt < ntok; tt += 2) {
                     const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + tt * HI;
                     float v0[32], v1[32];
                     tc::tmem_ld32(taddr, v0);
@@ -230,8 +252,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         s0 = fmaf(a.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
                         s1 = fmaf(c.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
                     }
-                    if (tt < ntok && key < S)
-                        out_base[(int64_t)tt * P.ld + key] = (key <= p0 + tt) ? (s0 + s1) * ks : -INFINITY;
+                    if (key < S) out_base[(int64_t)tt * P.ld + key] = (key <= p0 + tt) ? (s0 + s1) * ks : -INFINITY;
                 }
                 tc::tc_fence_before();
                 __syncwarp();
@@ -290,8 +311,39 @@ cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k
     P.q_off[st.B] = st.q_off[st.B];
     P.total_groups = P.g_off[st.B];
     if (P.total_groups == 0) return cudaSuccess;
-    const int want = 2 * 152;
-    P.splits = P.total_groups >= want ? 1 : std::min(16, (want + P.total_groups - 1) / P.total_groups);
+    P.splits = 1;
+    P.balanced = 0;
+    P.n_tab = 0;
+    unsigned grid = (unsigned)P.total_groups;
+    if (P.total_groups < SPLIT_TAB) {
+        // Few groups of (possibly very) different lengths: about SPLIT_TAB CTAs of `target` key
+        // blocks each, so that no CTA carries a long row's blocks alone.
+        int nblk[SPLIT_TAB], order[SPLIT_TAB];
+        int64_t total_blocks = 0;
+        for (int b = 0; b < st.B; ++b)
+            for (int g = P.g_off[b]; g < P.g_off[b + 1]; ++g) {
+                const int t0 = (g - P.g_off[b]) * TOK;
+                const int ntok = std::min(TOK, st.q_off[b + 1] - st.q_off[b] - t0);
+                nblk[g] = (st.start_pos[b] + t0 + ntok - 1) / BM + 1;
+                total_blocks += nblk[g];
+            }
+        const int target = (int)std::max<int64_t>(1, (total_blocks + SPLIT_TAB - 1) / SPLIT_TAB);
+        int per_cta[SPLIT_TAB], sp[SPLIT_TAB];
+        for (int g = 0; g < P.total_groups; ++g) {
+            sp[g] = std::max(1, std::min(nblk[g], (nblk[g] + target - 1) / target));
+            per_cta[g] = (nblk[g] + sp[g] - 1) / sp[g];
+            order[g] = g;
+        }
+        std::stable_sort(order, order + P.total_groups, [&](int a, int b) { return per_cta[a] > per_cta[b]; });
+        P.balanced = 1;
+        P.n_tab = P.total_groups;
+        P.s_off[0] = 0;
+        for (int i = 0; i < P.total_groups; ++i) {
+            P.g_of[i] = order[i];
+            P.s_off[i + 1] = P.s_off[i] + sp[order[i]];
+        }
+        grid = (unsigned)P.s_off[P.total_groups];
+    }
     P.fill_future = fill_future ? 1 : 0;
     P.ld = ld;
     P.c = 1.0f / sqrtf((float)(HI * DI));
@@ -313,7 +365,6 @@ cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k
         uint32_t box[2] = {inner, (uint32_t)BM};
         if (!make_tmap(&tk, ty, 2, k, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    const unsigned grid = (unsigned)P.total_groups * P.splits;
     cudaError_t e;
     if (fp8) {
         e = cudaFuncSetAttribute(indexer_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true>::SMEM);
