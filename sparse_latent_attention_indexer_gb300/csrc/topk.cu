@@ -1,26 +1,27 @@
 // Exact per-row top-k of the indexer scores (DeepSeek-V3.2-Exp atlas page,
 // M^sel_{t,s} = M_{t,s} for s in top_k(S~^I_t)): a radix select on
-// order-preserving uint32 keys, one CTA per query row.
+// order-preserving uint32 keys.
 //
-// Only the causal keys 0..p are read: the first pass converts them to keys
-// and keeps them in shared memory when the row fits the launch's cache
-// (longer rows re-read global memory).  If there are at most k causal keys
+// Only the causal keys 0..p are read.  If there are at most k causal keys
 // they are all selected.  Otherwise three histogram passes over 11 + 11 + 10
-// key bits (shared-memory histograms, atomics) find the exact k-th largest key
-// T and how many keys equal to T are needed; a final ordered pass compacts, in
-// increasing key order, every key above T and then the first `need` keys equal
-// to T, so equal scores resolve to the lower key index and the output is
-// deterministic.
+// key bits (shared-memory histograms) find the exact k-th largest key T and
+// how many keys equal to T are needed; a final ordered pass writes every key
+// above T and then the first `need` keys equal to T, each in increasing key
+// index, so equal scores resolve to the lower key index and the output is
+// deterministic.  Every kernel below writes the same output.
 //
-// Two kernels for two regimes:
-//   * topk_radix_kernel (many rows, e.g. prefill): 512 threads, one key per
-//     thread per step, warp ballots + a block scan per 512 keys; four CTAs per
-//     SM hide each other's latency.
-//   * topk_radix_wide_kernel (few long rows, e.g. decode: fewer CTAs than
-//     SMs): 1024 threads, eight loads in flight per thread in the histogram
-//     passes, eight consecutive keys per thread in the ordered pass (one block
-//     scan per 8192 keys), the output row assembled in shared memory and
-//     written out coalesced.
+// Three kernels for three regimes:
+//   * topk_filter_kernel (many rows, e.g. prefill): one CTA per row, two
+//     streaming passes (a histogram of the top 11 bits, then a compaction of
+//     every key in or above the threshold bin into a shared-memory candidate
+//     list); the radix select runs on the candidates.
+//   * topk_cluster_kernel (few long rows, e.g. decode): a cluster of eight
+//     CTAs per row, each holding a slice of the row's keys in shared memory,
+//     histograms merged through distributed shared memory.
+//   * topk_radix_wide_kernel (few rows too long for the cluster's shared
+//     memory): 1024 threads per row, eight loads in flight per thread in the
+//     histogram passes, eight consecutive keys per thread in the ordered pass,
+//     the output row assembled in shared memory and written out coalesced.
 #include "dsa_common.cuh"
 
 namespace dsa {
@@ -28,17 +29,162 @@ namespace {
 
 constexpr int MAX_BINS = 2048;
 
-constexpr int TK_THREADS = 512;
-constexpr int TK_WARPS = TK_THREADS / 32;
+// ---------------------------------------------------------------------------
+// Many rows (prefill): one CTA per row, two streaming passes over the row.
+//   A. 16 consecutive scores per thread per step (vector loads), an 11-bit
+//      histogram of the keys' top bits (warp-aggregated shared atomics: a
+//      row's scores crowd into a few exponent bins).  The bin B holding the
+//      k-th largest key follows from a scan from the top.
+//   B. every key whose top bits are >= B (all keys of the top k are among
+//      them) is compacted, in index order, into a shared-memory candidate
+//      list with its index.
+// The exact radix select then runs on the candidates only.  A row whose
+// candidates overflow the list (massive ties at the threshold) runs it on the
+// global row instead.
+// ---------------------------------------------------------------------------
+constexpr int TF_THREADS = 256;
+constexpr int TF_WARPS = TF_THREADS / 32;
+constexpr int CAND_CAP = 8192;  // candidates per row kept in shared memory (64 KB)
+constexpr int SPT = 16;         // consecutive scores per thread per streaming step
 
-__global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(const float *__restrict__ scores, int64_t ld,
-                                                                const __grid_constant__ SeqTab st, int k,
-                                                                int32_t *__restrict__ idx, int cache_cap) {
-    extern __shared__ uint32_t cache[];
+// Scores s0 .. s0+15 of a row (keys of absent positions are 0 and masked by `valid`).
+__device__ __forceinline__ void load_keys16(const float *__restrict__ row, int s0, int n, bool vec,
+                                            uint32_t (&u)[SPT], uint32_t &valid) {
+    if (vec && s0 + SPT <= n) {
+        const float4 *p = (const float4 *)(row + s0);
+#pragma unroll
+        for (int j = 0; j < SPT / 4; ++j) {
+            const float4 f = __ldg(p + j);
+            u[4 * j] = ordered_key(f.x);
+            u[4 * j + 1] = ordered_key(f.y);
+            u[4 * j + 2] = ordered_key(f.z);
+            u[4 * j + 3] = ordered_key(f.w);
+        }
+        valid = 0xffffu;
+    } else {
+        valid = 0;
+#pragma unroll
+        for (int j = 0; j < SPT; ++j) {
+            const bool ok = s0 + j < n;
+            u[j] = ok ? ordered_key(__ldg(row + s0 + j)) : 0u;
+            valid |= ok ? (1u << j) : 0u;
+        }
+    }
+}
+
+// The bin b of hist[0..nb) (nb a multiple of TF_THREADS) holding the need-th
+// largest key, counted from the top: keys in bins above b number `above` <
+// need <= above + hist[b].  Every thread of the CTA calls it and receives
+// {b, above, above + hist[b]} in res[0..2].  Thread t owns nb / TF_THREADS
+// consecutive bins from the top, so the search is one block-wide scan.
+__device__ __forceinline__ void find_bin_from_top(const uint32_t *hist, int nb, int need, int *res, int *warp_sum) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int per = nb / TF_THREADS, hi = nb - tid * per;
+    int mine = 0;
+    for (int b = hi - 1; b >= hi - per; --b) mine += (int)hist[b];
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sum[wid] = incl;
+    __syncthreads();
+    int before = 0;
+#pragma unroll
+    for (int w = 0; w < TF_WARPS; ++w) before += w < wid ? warp_sum[w] : 0;
+    const int excl = before + incl - mine;
+    if (excl < need && need <= excl + mine) {
+        int cum = excl;
+        for (int b = hi - 1; b >= hi - per; --b) {
+            const int h = (int)hist[b];
+            if (cum + h >= need) {
+                res[0] = b;
+                res[1] = cum;
+                res[2] = cum + h;
+                break;
+            }
+            cum += h;
+        }
+    }
+    __syncthreads();
+}
+
+// Exact top-k of n keys (key_at(j), j in index order), written as
+// [keys above the k-th key T, in order][the first keys equal to T, in order];
+// out_at(j) is the row index stored for entry j.  All threads of the CTA call it.
+template <class KeyAt, class IdxAt>
+__device__ __forceinline__ void radix_select_write(KeyAt key_at, IdxAt idx_at, int n, int k, int32_t *__restrict__ out,
+                                                   uint32_t *hist, int *warp_gt, int *warp_eq, int *shared3) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int &sel_bin = shared3[0], &sel_above = shared3[1];
+    uint32_t prefix = 0, pmask = 0;
+    int remaining = k;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int width = pass == 2 ? 10 : 11;
+        const int nb = 1 << width;
+        for (int b = tid; b < nb; b += TF_THREADS) hist[b] = 0;
+        __syncthreads();
+        for (int s = tid; s < n; s += TF_THREADS) {
+            const uint32_t u = key_at(s);
+            if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
+        }
+        __syncthreads();
+        find_bin_from_top(hist, nb, remaining, shared3, warp_eq);
+        remaining -= sel_above;
+        prefix |= (uint32_t)sel_bin << shift;
+        pmask |= (uint32_t)(nb - 1) << shift;
+        __syncthreads();  // sel_* are rewritten by the next pass
+    }
+    // prefix is now the k-th largest key T; (k - remaining) keys are above it.
+    const uint32_t T = prefix;
+    const int n_gt = k - remaining;
+    int base_gt = 0, base_eq = 0;
+    for (int s0 = 0; s0 < n; s0 += TF_THREADS) {
+        if (base_gt >= n_gt && base_eq >= remaining) break;  // block-uniform: every slot is written
+        const int s = s0 + tid;
+        const uint32_t u = s < n ? key_at(s) : 0u;
+        const bool gt = s < n && u > T;
+        const bool eq = s < n && u == T;
+        const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
+        const uint32_t lt_mask = (1u << lane) - 1u;
+        if (lane == 0) {
+            warp_gt[wid] = __popc(bg);
+            warp_eq[wid] = __popc(be);
+        }
+        __syncthreads();
+        int off_gt = 0, off_eq = 0, tot_gt = 0, tot_eq = 0;
+#pragma unroll
+        for (int w = 0; w < TF_WARPS; ++w) {
+            off_gt += w < wid ? warp_gt[w] : 0;
+            off_eq += w < wid ? warp_eq[w] : 0;
+            tot_gt += warp_gt[w];
+            tot_eq += warp_eq[w];
+        }
+        if (gt) {
+            const int rank = base_gt + off_gt + __popc(bg & lt_mask);
+            if (rank < n_gt) out[rank] = idx_at(s);
+        }
+        if (eq) {
+            const int rank = base_eq + off_eq + __popc(be & lt_mask);
+            if (rank < remaining) out[n_gt + rank] = idx_at(s);
+        }
+        base_gt += tot_gt;
+        base_eq += tot_eq;
+        __syncthreads();  // warp_gt / warp_eq are rewritten by the next chunk
+    }
+}
+
+__global__ void __launch_bounds__(TF_THREADS) topk_filter_kernel(const float *__restrict__ scores, int64_t ld,
+                                                                 const __grid_constant__ SeqTab st, int k,
+                                                                 int32_t *__restrict__ idx, int vec, int cap) {
+    extern __shared__ __align__(16) uint32_t cand[];  // [cap] keys, then [cap] row indices
     __shared__ uint32_t hist[MAX_BINS];
-    __shared__ int warp_gt[TK_WARPS], warp_eq[TK_WARPS];
-    __shared__ int tot_gt, tot_eq;
-    __shared__ int sel_bin, sel_above;
+    __shared__ int warp_gt[TF_WARPS], warp_eq[TF_WARPS];
+    __shared__ int shared3[3];
+    int32_t *cand_idx = (int32_t *)(cand + cap);
 
     const int r = blockIdx.x;
     const RowInfo ri = row_info(st, r);
@@ -48,115 +194,75 @@ __global__ void __launch_bounds__(TK_THREADS) topk_radix_kernel(const float *__r
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
 
     if (n_live <= k) {
-        for (int j = tid; j < k; j += TK_THREADS) out[j] = j < n_live ? j : -1;
+        for (int j = tid; j < k; j += TF_THREADS) out[j] = j < n_live ? j : -1;
         return;
     }
 
-    const bool cached = n_live <= cache_cap;
-    auto key_at = [&](int s) -> uint32_t { return cached ? cache[s] : ordered_key(row[s]); };
-    uint32_t prefix = 0, pmask = 0;
-    int remaining = k;  // keys still to take among those matching the prefix
+    // ---- A: histogram of the top 11 key bits ----
+    for (int b = tid; b < MAX_BINS; b += TF_THREADS) hist[b] = 0;
+    __syncthreads();
+    // The loop bounds are block-uniform: every lane reaches each __match_any_sync.
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const int width = pass == 2 ? 10 : 11;
-        const int nb = 1 << width;
-        for (int b = tid; b < nb; b += TK_THREADS) hist[b] = 0;
-        __syncthreads();
-        if (pass == 0) {
-            for (int s = tid; s < n_live; s += TK_THREADS) {
-                const uint32_t u = ordered_key(row[s]);
-                if (cached) cache[s] = u;
-                atomicAdd(&hist[u >> shift], 1u);
-            }
-        } else {
-            for (int s = tid; s < n_live; s += TK_THREADS) {
-                const uint32_t u = key_at(s);
-                if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
-            }
+    for (int base = 0; base < n_live; base += TF_THREADS * SPT) {
+        uint32_t u[SPT], valid;
+        load_keys16(row, base + tid * SPT, n_live, vec != 0, u, valid);
+#pragma unroll
+        for (int j = 0; j < SPT; ++j) {
+            const uint32_t bin = (valid >> j) & 1u ? (u[j] >> 21) : 0xffffffffu;
+            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+            if (bin != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
         }
-        __syncthreads();
-        if (wid == 0) {
-            // Lane l owns the bins [nb - (l+1)*per, nb - l*per), scanned from the top.
-            const int per = nb / 32;
-            const int hi = nb - lane * per;
-            int mine = 0;
-            for (int b = hi - 1; b >= hi - per; --b) mine += (int)hist[b];
-            int incl = mine;
+    }
+    __syncthreads();
+    find_bin_from_top(hist, MAX_BINS, k, shared3, warp_eq);
+    const uint32_t bsel = (uint32_t)shared3[0];
+    const int n_cand = shared3[2];  // keys in the threshold bin or above
+    __syncthreads();  // shared3 is reused by the select
+
+    if (n_cand <= cap) {
+        // ---- B: compact the candidates (top bits >= bsel) in index order ----
+        int base = 0;
+#pragma unroll 1
+        for (int s0 = 0; s0 < n_live; s0 += TF_THREADS * SPT) {
+            const int first = s0 + tid * SPT;
+            uint32_t u[SPT], valid = 0;
+            if (first < n_live) load_keys16(row, first, n_live, vec != 0, u, valid);
+            uint32_t take = 0;
+#pragma unroll
+            for (int j = 0; j < SPT; ++j) take |= (((valid >> j) & 1u) && (u[j] >> 21) >= bsel) ? (1u << j) : 0u;
+            const int c = __popc(take);
+            int incl = c;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int v = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += v;
             }
-            const int excl = incl - mine;
-            if (excl < remaining && remaining <= incl) {
-                int cum = excl;
-                for (int b = hi - 1; b >= hi - per; --b) {
-                    const int h = (int)hist[b];
-                    if (cum + h >= remaining) {
-                        sel_bin = b;
-                        sel_above = cum;
-                        break;
-                    }
-                    cum += h;
-                }
-            }
-        }
-        __syncthreads();
-        remaining -= sel_above;
-        prefix |= (uint32_t)sel_bin << shift;
-        pmask |= (uint32_t)(nb - 1) << shift;
-        __syncthreads();  // sel_* are rewritten by the next pass
-    }
-
-    // prefix is now the k-th largest key T; (k - remaining) keys are above it.
-    const uint32_t T = prefix;
-    const int n_gt = k - remaining;
-    int base_gt = 0, base_eq = 0;
-    for (int s0 = 0; s0 < n_live; s0 += TK_THREADS) {
-        const int s = s0 + tid;
-        const uint32_t u = s < n_live ? key_at(s) : 0u;
-        const bool gt = s < n_live && u > T;
-        const bool eq = s < n_live && u == T;
-        const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
-        const uint32_t lt_mask = (1u << lane) - 1u;
-        if (lane == 0) {
-            warp_gt[wid] = __popc(bg);
-            warp_eq[wid] = __popc(be);
-        }
-        __syncthreads();
-        if (wid == 0) {
-            int g = lane < TK_WARPS ? warp_gt[lane] : 0, e = lane < TK_WARPS ? warp_eq[lane] : 0;
-            int gi = g, ei = e;
+            if (lane == 31) warp_gt[wid] = incl;
+            __syncthreads();
+            int before = 0, total = 0;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int vg = __shfl_up_sync(0xffffffffu, gi, o), ve = __shfl_up_sync(0xffffffffu, ei, o);
-                if (lane >= o) { gi += vg; ei += ve; }
+            for (int w = 0; w < TF_WARPS; ++w) {
+                before += w < wid ? warp_gt[w] : 0;
+                total += warp_gt[w];
             }
-            if (lane < TK_WARPS) {
-                warp_gt[lane] = gi - g;
-                warp_eq[lane] = ei - e;
-            }
-            if (lane == 31) {
-                tot_gt = gi;
-                tot_eq = ei;
-            }
+            int pos = base + before + incl - c;
+#pragma unroll
+            for (int j = 0; j < SPT; ++j)
+                if ((take >> j) & 1u) {
+                    cand[pos] = u[j];
+                    cand_idx[pos] = first + j;
+                    ++pos;
+                }
+            base += total;
+            __syncthreads();  // warp_gt is rewritten by the next step
         }
-        __syncthreads();
-        if (gt) {
-            const int rank = base_gt + warp_gt[wid] + __popc(bg & lt_mask);
-            if (rank < n_gt) out[rank] = s;
-        }
-        if (eq) {
-            const int rank = base_eq + warp_eq[wid] + __popc(be & lt_mask);
-            if (rank < remaining) out[n_gt + rank] = s;
-        }
-        base_gt += tot_gt;
-        base_eq += tot_eq;
-        __syncthreads();
+        radix_select_write([&](int j) { return cand[j]; }, [&](int j) { return cand_idx[j]; }, n_cand, k, out, hist,
+                           warp_gt, warp_eq, shared3);
+    } else {
+        radix_select_write([&](int j) { return ordered_key(__ldg(row + j)); }, [&](int j) { return j; }, n_live, k,
+                           out, hist, warp_gt, warp_eq, shared3);
     }
 }
-
 
 constexpr int KPT = 8;                // consecutive keys per thread in the ordered pass
 constexpr int CACHE_MAX = 48 * 1024;  // keys kept in shared memory (192 KB)
@@ -579,11 +685,13 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int t
         e = cudaFuncSetAttribute(topk_radix_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess) topk_radix_wide_kernel<<<total_q, WIDE_THREADS, smem, s>>>(scores, ld, st, k, idx, cap);
     } else {
-        // Many rows: the cache is the longest causal row, at most 32768 keys (128 KB).
-        const int cap = max_live <= k ? 0 : min(max_live, 32768);
-        const size_t smem = (size_t)cap * sizeof(uint32_t);
-        e = cudaFuncSetAttribute(topk_radix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) topk_radix_kernel<<<total_q, TK_THREADS, smem, s>>>(scores, ld, st, k, idx, cap);
+        // Many rows: two streaming passes per row and a shared-memory candidate list as long as
+        // the longest row (at most CAND_CAP), so that short rows keep more CTAs per SM.
+        const int cap = std::max(64, std::min(CAND_CAP, (max_live + 63) / 64 * 64));
+        const size_t smem = (size_t)cap * 2 * sizeof(uint32_t);
+        const int vec = ((uintptr_t)scores % 16 == 0 && ld % 4 == 0) ? 1 : 0;
+        e = cudaFuncSetAttribute(topk_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess) topk_filter_kernel<<<total_q, TF_THREADS, smem, s>>>(scores, ld, st, k, idx, vec, cap);
     }
     if (e != cudaSuccess) return e;
     note_launch(DSA_KERNEL_TOPK);

@@ -113,7 +113,8 @@ def test_topk(name):
 
 # A launch with fewer than 2 x 152 rows takes the cluster top-k kernel (decode: eight CTAs per row),
 # or the wide one-CTA-per-row kernel when a row's slices would not fit the CTAs' shared memory; more
-# rows take the many-rows kernel (prefill).  The cases below run on every side of those switches.
+# rows take the many-rows kernel (prefill: a candidate list, or the global row when the list would
+# overflow).  The cases below run on every side of those switches.
 @pytest.mark.parametrize("T", [700, 100])
 @pytest.mark.parametrize("fill", [1.0, 0.0, -3.5])
 def test_topk_all_equal_scores(fill, T):
@@ -145,6 +146,24 @@ def test_topk_threshold_ties_and_large_rows(rows):
     for r in range(rows):
         p = S - rows + r
         want = H.cpu_topk_same_buffer(sc[r], p, 2048)
+        assert sorted(idx[r].tolist()) == sorted(want.tolist())
+
+
+def test_topk_candidate_overflow_falls_back_to_the_global_row():
+    """Many rows (the many-rows kernel) whose threshold bin holds more keys
+    than its shared-memory candidate list: almost every score ties at 1.0 and
+    a few keys score 2.0, so the select runs on the global row; exact equality
+    with the CPU top-k of the same buffer (lowest indices win the ties)."""
+    g = torch.Generator().manual_seed(7)
+    rows, S, k = 320, 12000, 2048
+    seqs = dsa.Seqs([0, rows], [0, S], [S - rows])
+    scores = torch.ones((rows, S))
+    hot = torch.randint(0, S, (rows, 300), generator=g)
+    scores.scatter_(1, hot, 2.0)
+    idx = dsa.dsa_topk_select(scores.cuda(), seqs, k).cpu().numpy()
+    sc = scores.numpy()
+    for r in range(rows):
+        want = H.cpu_topk_same_buffer(sc[r], S - rows + r, k)
         assert sorted(idx[r].tolist()) == sorted(want.tolist())
 
 
