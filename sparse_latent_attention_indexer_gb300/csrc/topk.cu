@@ -207,11 +207,8 @@ __global__ void __launch_bounds__(TF_THREADS) topk_filter_kernel(const float *__
         uint32_t u[SPT], valid;
         load_keys16(row, base + tid * SPT, n_live, vec != 0, u, valid);
 #pragma unroll
-        for (int j = 0; j < SPT; ++j) {
-            const uint32_t bin = (valid >> j) & 1u ? (u[j] >> 21) : 0xffffffffu;
-            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-            if (bin != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-        }
+        for (int j = 0; j < SPT; ++j)
+            if ((valid >> j) & 1u) atomicAdd(&hist[u[j] >> 21], 1u);
     }
     __syncthreads();
     find_bin_from_top(hist, MAX_BINS, k, shared3, warp_eq);

@@ -167,6 +167,23 @@ def test_topk_candidate_overflow_falls_back_to_the_global_row():
         assert sorted(idx[r].tolist()) == sorted(want.tolist())
 
 
+@pytest.mark.parametrize("rows", [24, 320])
+def test_topk_odd_row_stride(rows):
+    """A score buffer whose rows are not 16-byte aligned (odd row stride): the
+    kernels take their scalar loads; exact equality with the CPU top-k."""
+    g = torch.Generator().manual_seed(8)
+    S, k = 9001, 512
+    seqs = dsa.Seqs([0, rows], [0, S], [S - rows])
+    full = torch.randn((rows, S + 1), generator=g)
+    scores = full.cuda()[:, 1:]
+    assert scores.stride(0) % 4 != 0 or scores.data_ptr() % 16 != 0
+    idx = dsa.dsa_topk_select(scores, seqs, k).cpu().numpy()
+    sc = full[:, 1:].numpy()
+    for r in range(rows):
+        want = H.cpu_topk_same_buffer(sc[r], S - rows + r, k)
+        assert sorted(idx[r].tolist()) == sorted(want.tolist())
+
+
 def test_topk_rows_longer_than_the_cluster_cache():
     """Two rows of 400,000 causal keys (beyond eight CTAs' shared memory: the
     wide kernel, which re-reads global memory); exact equality with the CPU
