@@ -203,10 +203,11 @@ namespace {
 
 int run_indexer(const void *q, const float *q_scale, const void *k, const float *k_scale, int idx_dtype,
                 const float *w, int H_I, int D_I, const SeqTab &st, int rows, int max_S, int64_t total_k,
-                float *scores, int64_t ld, bool fill_future, cudaStream_t s) {
+                float *scores, int64_t ld, bool fill_future, cudaStream_t s, int dense_k = 0) {
     cudaError_t e;
     if (!force_generic() && indexer_tc_supported(idx_dtype, H_I, D_I) && aligned(q, 16) && aligned(k, 16))
-        e = launch_indexer_tc(q, q_scale, k, k_scale, idx_dtype, w, st, total_k, scores, ld, fill_future, s);
+        e = launch_indexer_tc(q, q_scale, k, k_scale, idx_dtype, w, st, total_k, scores, ld, fill_future, s,
+                              dense_k);
     else
         e = launch_indexer_simt(q, q_scale, k, k_scale, idx_dtype, w, H_I, D_I, st, rows, max_S, scores, ld, s);
     return e == cudaSuccess ? DSA_OK : fail_cuda(e);
@@ -417,7 +418,7 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
         sub_batch(seqs, r0, r1, st, max_S);
         rc = run_indexer((const char *)q_idx + qrow * r0, q_scale ? q_scale + (size_t)r0 * p->H_I : nullptr, k_idx,
                          k_scale, idx_dtype, p->w + (size_t)r0 * p->H_I, p->H_I, p->D_I, st, r1 - r0, max_S,
-                         bt.total_k, scores, L.ld, false, s);
+                         bt.total_k, scores, L.ld, false, s, p->top_k);
         if (rc) return rc;
         e = launch_topk(scores, L.ld, st, r1 - r0, p->top_k, idx + (size_t)r0 * p->top_k, s);
         if (e != cudaSuccess) return fail_cuda(e);

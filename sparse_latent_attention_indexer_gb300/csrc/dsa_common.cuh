@@ -113,7 +113,7 @@ cudaError_t launch_indexer_simt(const void *q, const float *q_scale, const void 
 bool indexer_tc_supported(int dtype, int H_I, int D_I);
 cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k, const float *k_scale, int dtype,
                               const float *w, const SeqTab &st, int64_t total_k, float *scores, int64_t ld,
-                              bool fill_future, cudaStream_t s);
+                              bool fill_future, cudaStream_t s, int dense_k = 0);
 int indexer_tc_read_error(int *site);
 
 // DSA_FORCE_GENERIC=1 in the environment routes every stage to the generic

@@ -73,6 +73,7 @@ struct IdxParams {
     int s_off[SPLIT_TAB + 1];
     int g_of[SPLIT_TAB];
     int fill_future;
+    int dense_k;  // > 0: skip groups whose rows all see at most dense_k keys (they select every causal key)
     int64_t ld;
     float c;
 };
@@ -130,7 +131,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int p0 = P.start_pos[b] + t0;
     const int S = P.k_len[b], kbase = P.k_base[b];
     const int nblk = (p0 + ntok - 1) / BM + 1;  // blocks holding keys 0 .. last position
-    const int mine = split < nblk ? (nblk - split + splits - 1) / splits : 0;
+    // A group whose last row sits at position < dense_k needs no scores: every row of it selects all
+    // of its causal keys, and the top-k does not read them.
+    const bool dense = P.dense_k > 0 && p0 + ntok - 1 < P.dense_k;
+    const int mine = (split < nblk && !dense) ? (nblk - split + splits - 1) / splits : 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::STAGES; ++i) {
@@ -295,7 +299,7 @@ int indexer_tc_read_error(int *site) {
 
 cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k, const float *k_scale, int dtype,
                               const float *w, const SeqTab &st, int64_t total_k, float *scores, int64_t ld,
-                              bool fill_future, cudaStream_t s) {
+                              bool fill_future, cudaStream_t s, int dense_k) {
     const bool fp8 = dtype == DSA_E4M3;
     static thread_local IdxParams P;  // ~10 KB: keep it off the host stack
     P.B = st.B;
@@ -345,6 +349,7 @@ cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k
         grid = (unsigned)P.s_off[P.total_groups];
     }
     P.fill_future = fill_future ? 1 : 0;
+    P.dense_k = dense_k;
     P.ld = ld;
     P.c = 1.0f / sqrtf((float)(HI * DI));
 
