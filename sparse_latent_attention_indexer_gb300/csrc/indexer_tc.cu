@@ -234,19 +234,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc::tc_fence_after();
                 const int key = (split + i * splits) * BM + q * 32 + lane;
                 const float ks = (FP8 && key < S) ? k_scale[kbase + key] : 1.0f;
-                // The two warps of a lane quarter take alternate tokens; absent tokens are skipped.
+                // The two warps of a lane quarter take alternate tokens (hf and hf + 2); absent tokens are
+                // skipped.  bf16: both tokens' 64 head columns are loaded before a single wait, the
+                // accumulator is handed back to the MMA at once, and the two reductions run as four
+                // independent chains.
+                const int tt0 = hf, tt1 = hf + 2;
+                if (FP8) {
+                    // FP8 variant: one token at a time (the two-token form raises register pressure
+                    // past the limit and measured slower here).
 #pragma unroll 1
-                for (int tt = hf; tt < ntok; tt += 2) {
-                    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + tt * HI;
-                    float v0[32], v1[32];
-                    tc::tmem_ld32(taddr, v0);
-                    tc::tmem_ld32(taddr + 32, v1);
+                    for (int tt = hf; tt < ntok; tt += 2) {
+                        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + tt * HI;
+                        float v0[32], v1[32];
+                        tc::tmem_ld32(taddr, v0);
+                        tc::tmem_ld32(taddr + 32, v1);
+                        tc::tmem_ld_wait();
+                        const float4 *wv = (const float4 *)(wsm + tt * HI);
+                        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+                        for (int h4 = 0; h4 < 8; ++h4) {
+                            const float4 a = wv[h4], c = wv[8 + h4];
+                            s0 = fmaf(a.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
+                            s1 = fmaf(c.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
+                            s0 = fmaf(a.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
+                            s1 = fmaf(c.y, fmaxf(v1[4 * h4 + 1], 0.0f), s1);
+                            s0 = fmaf(a.z, fmaxf(v0[4 * h4 + 2], 0.0f), s0);
+                            s1 = fmaf(c.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
+                            s0 = fmaf(a.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
+                            s1 = fmaf(c.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
+                        }
+                        if (key < S) out_base[(int64_t)tt * P.ld + key] = (key <= p0 + tt) ? (s0 + s1) * ks : -INFINITY;
+                    }
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+                } else if (tt0 < ntok) {
+                    const bool two = tt1 < ntok;  // warp-uniform
+                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+                    float v0[32], v1[32], v2[32], v3[32];
+                    tc::tmem_ld32(ta + tt0 * HI, v0);
+                    tc::tmem_ld32(ta + tt0 * HI + 32, v1);
+                    if (two) {
+                        tc::tmem_ld32(ta + tt1 * HI, v2);
+                        tc::tmem_ld32(ta + tt1 * HI + 32, v3);
+                    }
                     tc::tmem_ld_wait();
-                    const float4 *wv = (const float4 *)(wsm + tt * HI);
-                    float s0 = 0.0f, s1 = 0.0f;
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+                    const float4 *wa = (const float4 *)(wsm + tt0 * HI), *wb = (const float4 *)(wsm + tt1 * HI);
+                    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
 #pragma unroll
                     for (int h4 = 0; h4 < 8; ++h4) {
-                        const float4 a = wv[h4], c = wv[8 + h4];
+                        const float4 a = wa[h4], c = wa[8 + h4];
                         s0 = fmaf(a.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
                         s1 = fmaf(c.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
                         s0 = fmaf(a.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
@@ -255,12 +295,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         s1 = fmaf(c.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
                         s0 = fmaf(a.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
                         s1 = fmaf(c.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
+                        if (two) {
+                            const float4 b = wb[h4], d = wb[8 + h4];
+                            s2 = fmaf(b.x, fmaxf(v2[4 * h4 + 0], 0.0f), s2);
+                            s3 = fmaf(d.x, fmaxf(v3[4 * h4 + 0], 0.0f), s3);
+                            s2 = fmaf(b.y, fmaxf(v2[4 * h4 + 1], 0.0f), s2);
+                            s3 = fmaf(d.y, fmaxf(v3[4 * h4 + 1], 0.0f), s3);
+                            s2 = fmaf(b.z, fmaxf(v2[4 * h4 + 2], 0.0f), s2);
+                            s3 = fmaf(d.z, fmaxf(v3[4 * h4 + 2], 0.0f), s3);
+                            s2 = fmaf(b.w, fmaxf(v2[4 * h4 + 3], 0.0f), s2);
+                            s3 = fmaf(d.w, fmaxf(v3[4 * h4 + 3], 0.0f), s3);
+                        }
                     }
-                    if (key < S) out_base[(int64_t)tt * P.ld + key] = (key <= p0 + tt) ? (s0 + s1) * ks : -INFINITY;
+                    if (key < S) {
+                        out_base[(int64_t)tt0 * P.ld + key] = (key <= p0 + tt0) ? (s0 + s1) * ks : -INFINITY;
+                        if (two) out_base[(int64_t)tt1 * P.ld + key] = (key <= p0 + tt1) ? (s2 + s3) * ks : -INFINITY;
+                    }
+                } else {
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&tempty[acc]);
                 }
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&tempty[acc]);
             }
         }
     }
