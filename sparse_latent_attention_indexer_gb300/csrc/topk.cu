@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1) topk_radix_wide_kernel(const 
 constexpr int CL = 8;              // CTAs per row
 constexpr int CT = 256;            // threads per CTA
 constexpr int CT_WARPS = CT / 32;
+static_assert(CT == TF_THREADS, "find_bin_from_top assumes the filter kernel's block size");
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -477,7 +478,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(CT)
     __shared__ __align__(16) uint32_t merged[MAX_BINS];
     __shared__ __align__(16) uint32_t counts[4];       // (above, equal) of this slice
     __shared__ uint32_t warp_tot[2][CT_WARPS];
-    __shared__ int sel_bin, sel_above;
+    __shared__ int sel[3], warp_sum[CT_WARPS];
 
     const int r = blockIdx.x / CL;
     const uint32_t c = cluster_ctarank();
@@ -507,15 +508,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(CT)
         __syncthreads();
         if (pass == 0) {
 #pragma unroll 1
-            for (int s0 = 0; s0 < n; s0 += HB * CT) {
-                uint32_t u[HB];
+            for (int s0 = 0; s0 < n; s0 += 2 * HB * CT) {
+                uint32_t u[2 * HB];
 #pragma unroll
-                for (int j = 0; j < HB; ++j) {
+                for (int j = 0; j < 2 * HB; ++j) {
                     const int s = s0 + j * CT + tid;
                     u[j] = s < n ? ordered_key(row[s_lo + s]) : 0u;
                 }
 #pragma unroll
-                for (int j = 0; j < HB; ++j) {
+                for (int j = 0; j < 2 * HB; ++j) {
                     const int s = s0 + j * CT + tid;
                     if (s < n) {
                         slice[s] = u[j];
@@ -542,37 +543,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(CT)
             *(uint4 *)(merged + 4 * q4) = acc;
         }
         __syncthreads();
-        if (wid == 0) {
-            // Lane l owns the bins [nb - (l+1)*per, nb - l*per), scanned from the top.
-            const int per = (int)nb / 32;
-            const int hi = (int)nb - lane * per;
-            int mine = 0;
-            for (int b = hi - 1; b >= hi - per; --b) mine += (int)merged[b];
-            int incl = mine;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            const int excl = incl - mine;
-            if (excl < remaining && remaining <= incl) {
-                int cum = excl;
-                for (int b = hi - 1; b >= hi - per; --b) {
-                    const int hb = (int)merged[b];
-                    if (cum + hb >= remaining) {
-                        sel_bin = b;
-                        sel_above = cum;
-                        break;
-                    }
-                    cum += hb;
-                }
-            }
-        }
-        __syncthreads();
-        remaining -= sel_above;
-        prefix |= (uint32_t)sel_bin << shift;
+        find_bin_from_top(merged, (int)nb, remaining, sel, warp_sum);
+        remaining -= sel[1];
+        prefix |= (uint32_t)sel[0] << shift;
         pmask |= (nb - 1) << shift;
-        __syncthreads();  // sel_* and merged[] are rewritten by the next pass
+        __syncthreads();  // sel[] and merged[] are rewritten by the next pass
     }
 
     // prefix is now the k-th largest key T of the row; (k - remaining) keys are above it.
