@@ -59,8 +59,12 @@ constexpr int ROPE_K = BK * 64;              // 4 KB: 64 keys x 32 rope columns,
 constexpr int KV_STAGE = NSLAB * SLAB_K + ROPE_K;  // 36 KB (a multiple of 1 KB: swizzle atoms stay aligned)
 constexpr int NSTAGE = 4;
 constexpr int X_BYTES = NH * BK * 2;         // 16 KB: one tile of fp16 partial scores
+constexpr int Q_BOX = NH * 128;              // 16 KB: 128 heads x 64 bf16 columns (one TMA box of q~ or o_lat)
+static_assert(4 * Q_BOX <= 4 * X_BYTES, "the q~ slice is staged in the four exchange buffers");
+static_assert(4 * Q_BOX <= NSTAGE * KV_STAGE, "the context is staged in the key stages");
 constexpr int SMEM = 1024 + NSTAGE * KV_STAGE + 4 * X_BYTES + NSTAGE * BK + 3 * 2 * NH * 4 + 256;
-constexpr int NUM_THREADS = 448;             // warps 0, 3, 12, 13: gather; 1: MMA; 2: TMEM; 4-11: softmax
+constexpr int NUM_THREADS = 448;
+constexpr uint32_t SOFT_BAR = 5;             // named barrier of the eight softmax warps (ids 1-4: warp pairs)             // warps 0, 3, 12, 13: gather; 1: MMA; 2: TMEM; 4-11: softmax
 constexpr int NPROD = 4;                     // gathering warps
 // Tensor-memory columns (512 per CTA): scores, probabilities (bf16 pairs),
 // the resident q~ slice (bf16 pairs, A operand of QK^T) and the context.
@@ -93,11 +97,13 @@ __device__ __forceinline__ int find_seq(const MlaParams &P, int r) {
 }
 
 struct Bars {
-    uint64_t q_ready, kv_full[NSTAGE], kv_empty[NSTAGE], s_full, s_empty, p_full, p_empty, xfull[2], xempty[2], o_done;
+    uint64_t q_stage, q_ready, kv_full[NSTAGE], kv_empty[NSTAGE], s_full, s_empty, p_full, p_empty, xfull[2], xempty[2],
+        o_done;
 };
 
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most 4 per SM sub-partition x 128 regs
-    mla_tc_kernel(const __nv_bfloat16 *__restrict__ kv, int64_t ld_kv, const __nv_bfloat16 *__restrict__ kpe,
+    mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+                  const __nv_bfloat16 *__restrict__ kv, int64_t ld_kv, const __nv_bfloat16 *__restrict__ kpe,
                   int64_t ld_pe, const __nv_bfloat16 *__restrict__ qt, const __nv_bfloat16 *__restrict__ qpe,
                   const int32_t *__restrict__ idx,
                   const __grid_constant__ MlaParams P, __nv_bfloat16 *__restrict__ olat, float *__restrict__ lse,
@@ -133,6 +139,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
     const int n = e1 > e0 ? (e1 - e0 + BK - 1) / BK : 0;
 
     if (threadIdx.x == 0) {
+        tc::mbar_init(&bar->q_stage, 1);
         tc::mbar_init(&bar->q_ready, 8);
         for (int i = 0; i < NSTAGE; ++i) {
             // every gathering thread arrives twice: when its copies land, and to publish the mask bytes
@@ -145,7 +152,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         tc::mbar_init(&bar->p_empty, 1);
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&bar->xfull[i], 1);   // armed locally with the 32 KB the peer sends
-            tc::mbar_init(&bar->xempty[i], 8);  // one arrival per peer softmax warp
+            // one arrival per peer softmax warp; phase 0 = the peer's q~ staging (below) has been read
+            tc::mbar_init(&bar->xempty[i], 8);
         }
         tc::mbar_init(&bar->o_done, 1);
         *abort_flag = 0;
@@ -161,6 +169,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
     tc::tc_fence_after();
     tc::cluster_sync();  // both CTAs' barriers exist before any remote arrive
     const uint32_t tmem = *tmem_slot;
+    // This CTA's q~ slice (128 heads x 256 latent columns) comes in by TMA as four 128-byte-swizzled
+    // boxes of 64 columns, staged in the exchange buffers, which carry no scores yet.
+    if (warp == 2 && lane == 0 && n > 0) {
+        tc::prefetch_tmap(&tm_q);
+        tc::mbar_arrive_expect_tx(&bar->q_stage, 4 * Q_BOX);
+        for (int js = 0; js < 4; ++js) tc::tma_load_3d(X + js * Q_BOX, &tm_q, &bar->q_stage, rank * 256 + js * 64, 0, r);
+    }
 
     if ((warp == 0 || warp == 3 || warp >= 12) && n > 0) {
         // ---------------- producers: gather the selected key rows with cp.async ----------------
@@ -265,39 +280,52 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         bool done_ok = true;
         if (n > 0) {
             // This CTA's slice of the head's q~ row -> tensor memory (A operand of QK^T): latent
-            // columns as 4 slabs of 32 packed columns, then the rope half as 16 more; the two
-            // threads of a row split the slabs and the second one also takes the rope half.
-            const __nv_bfloat16 *qrow = qt + ((int64_t)r * NH + h) * DC;
-            const uint4 *src = (const uint4 *)(qrow + rank * 256);
-            for (int js = hf * 2; js < hf * 2 + 2; ++js) {
-                uint32_t qv[32];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint4 t4 = __ldg(src + js * 8 + e);
-                    qv[4 * e] = t4.x;
-                    qv[4 * e + 1] = t4.y;
-                    qv[4 * e + 2] = t4.z;
-                    qv[4 * e + 3] = t4.w;
-                }
-                tc::tmem_st32(tmem + lane_off + COL_Q + js * 32, qv);
-            }
+            // columns as 4 slabs of 32 packed columns (from the TMA staging; chunk e of row h sits at
+            // e ^ (h & 7)), then the rope half as 16 more; the two threads of a row split the slabs
+            // and the second one also takes the rope half (read in place).
+            uint4 rq[4];
             if (hf) {
                 const uint4 *rsrc = (const uint4 *)(qpe + ((int64_t)r * NH + h) * DR + rank * 32);
-                uint32_t qv[16];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint4 t4 = __ldg(rsrc + e);
-                    qv[4 * e] = t4.x;
-                    qv[4 * e + 1] = t4.y;
-                    qv[4 * e + 2] = t4.z;
-                    qv[4 * e + 3] = t4.w;
-                }
-                tc::tmem_st16(tmem + lane_off + COL_Q + NSLAB * 32, qv);
+                for (int e = 0; e < 4; ++e) rq[e] = __ldg(rsrc + e);
             }
-            tc::tmem_st_wait();
+            if (!tc::mbar_wait(&bar->q_stage, 0, abort_flag, err, 23)) done_ok = false;
+            if (done_ok) {
+                for (int js = hf * 2; js < hf * 2 + 2; ++js) {
+                    const uint8_t *srow = X + js * Q_BOX + h * 128;
+                    uint32_t qv[32];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint4 t4 = *(const uint4 *)(srow + ((e ^ (h & 7)) << 4));
+                        qv[4 * e] = t4.x;
+                        qv[4 * e + 1] = t4.y;
+                        qv[4 * e + 2] = t4.z;
+                        qv[4 * e + 3] = t4.w;
+                    }
+                    tc::tmem_st32(tmem + lane_off + COL_Q + js * 32, qv);
+                }
+                if (hf) {
+                    uint32_t qv[16];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        qv[4 * e] = rq[e].x;
+                        qv[4 * e + 1] = rq[e].y;
+                        qv[4 * e + 2] = rq[e].z;
+                        qv[4 * e + 3] = rq[e].w;
+                    }
+                    tc::tmem_st16(tmem + lane_off + COL_Q + NSLAB * 32, qv);
+                }
+                tc::tmem_st_wait();
+            }
             tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bar->q_ready);
+            // Every softmax warp has read its part of the staging before any of them writes a score
+            // tile into Y, and then tells the peer that this CTA's X buffers may receive scores.
+            asm volatile("bar.sync %0, %1;" ::"r"(SOFT_BAR), "r"(8 * 32) : "memory");
+            if (lane == 0) {
+                tc::mbar_arrive(&bar->q_ready);
+                tc::mbar_arrive_remote(tc::map_peer(tc::smem_u32(&bar->xempty[0]), peer));
+                tc::mbar_arrive_remote(tc::map_peer(tc::smem_u32(&bar->xempty[1]), peer));
+            }
         }
         const float sl2 = P.scale_log2;
         const uint32_t row_sw = (uint32_t)((h >> 1) & 3);
@@ -325,11 +353,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                 for (int j = 0; j < 16; ++j) cur[j] = tc::f16x2_satfinite(sc[2 * j] * sl2, sc[2 * j + 1] * sl2);
                 const int xb = i & 1;
                 if (threadIdx.x == 4 * 32) tc::mbar_arrive_expect_tx(&bar->xfull[xb], X_BYTES);
-                // Once the peer has read tile i-2 from its X[xb], the copy that delivered it has also
-                // finished reading Y[xb]: both buffers of this parity are free again.
+                // The peer's X[xb] is free once the peer has read its q~ staging (tiles 0, 1) or tile
+                // i-2 from it (then the copy that delivered tile i-2 has also finished reading Y[xb]).
                 bool ok = true;
-                if (lane == 0 && i >= 2)
-                    ok = tc::mbar_wait_cluster(&bar->xempty[xb], ((i >> 1) & 1) ^ 1, abort_flag, err, 32);
+                if (lane == 0) ok = tc::mbar_wait_cluster(&bar->xempty[xb], (i >> 1) & 1, abort_flag, err, 32);
                 __syncwarp();
                 if (!__shfl_sync(0xffffffffu, ok, 0)) { done_ok = false; break; }
                 uint8_t *yrow = Y + xb * X_BYTES + roff;
@@ -457,7 +484,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         const float row_lse = (have && lrow > 0.0f) ? (m_used + log2f(lrow)) * LN2 : -INFINITY;
         if (have) tc::tc_fence_after();
         if (P.splits == 1) {
-            __nv_bfloat16 *dst = olat + rh * DC + rank * 256;
+            // bf16 context -> the key stages (free: every PV product is done), as four 128-byte-
+            // swizzled boxes of 64 columns, then out by TMA tensor stores.
 #pragma unroll 1
             for (int cc = hf * 4; cc < hf * 4 + 4; ++cc) {
                 float o[32];
@@ -472,9 +500,19 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                                                    : __floats2bfloat162_rn(0.0f, 0.0f);
                     pw[e] = *(const uint32_t *)&t2;
                 }
-                uint4 *d4 = (uint4 *)(dst + cc * 32);
+                uint8_t *srow = KV + (cc >> 1) * Q_BOX + h * 128;
+                const int j0 = (cc & 1) * 4;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pw[4 * e], pw[4 * e + 1], pw[4 * e + 2], pw[4 * e + 3]);
+                for (int e = 0; e < 4; ++e)
+                    *(uint4 *)(srow + (((j0 + e) ^ (h & 7)) << 4)) =
+                        make_uint4(pw[4 * e], pw[4 * e + 1], pw[4 * e + 2], pw[4 * e + 3]);
+            }
+            tc::fence_proxy_async_smem();  // the staging is read by the TMA stores (async proxy)
+            asm volatile("bar.sync %0, %1;" ::"r"(SOFT_BAR), "r"(8 * 32) : "memory");
+            if (threadIdx.x == 4 * 32) {
+                for (int cb = 0; cb < 4; ++cb) tc::tma_store_3d(&tm_o, KV + cb * Q_BOX, rank * 256 + cb * 64, 0, r);
+                tc::bulk_commit_group();
+                tc::bulk_wait_all();  // the staging must outlive the stores' reads (the CTA exits next)
             }
             if (rank == 0 && hf == 0 && lse) lse[rh] = row_lse;
         } else {
@@ -595,10 +633,20 @@ cudaError_t launch_mla_tc(const void *qt, const void *qpe, const void *kv, int64
         opart = (float *)part_ws;
         lpart = (float *)((char *)part_ws + (((size_t)M * P.splits * NH * DC * sizeof(float) + 255) / 256) * 256);
     }
+    // q~ rows [M, 128, 512] (loaded) and the latent context [M, 128, 512] (stored): boxes of
+    // 64 columns x 128 heads x 1 row, 128-byte swizzle.
+    CUtensorMap tq, to;
+    {
+        const uint64_t dims[3] = {(uint64_t)DC, (uint64_t)NH, (uint64_t)M};
+        const uint64_t strides[2] = {(uint64_t)DC * 2, (uint64_t)NH * DC * 2};
+        const uint32_t box[3] = {64, (uint32_t)NH, 1};
+        if (!make_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, qt, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!make_tmap(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, olat, dims, strides, box)) return cudaErrorInvalidValue;
+    }
     cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)M * P.splits * 2;
-    mla_tc_kernel<<<grid, NUM_THREADS, SMEM, s>>>((const __nv_bfloat16 *)kv, ld_kv, (const __nv_bfloat16 *)kpe, ld_pe,
+    mla_tc_kernel<<<grid, NUM_THREADS, SMEM, s>>>(tq, to, (const __nv_bfloat16 *)kv, ld_kv, (const __nv_bfloat16 *)kpe, ld_pe,
                                                    (const __nv_bfloat16 *)qt, (const __nv_bfloat16 *)qpe, idx, P,
                                                    (__nv_bfloat16 *)olat, lse,
                                                    opart, lpart);
