@@ -512,7 +512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             if (threadIdx.x == 4 * 32) {
                 for (int cb = 0; cb < 4; ++cb) tc::tma_store_3d(&tm_o, KV + cb * Q_BOX, rank * 256 + cb * 64, 0, r);
                 tc::bulk_commit_group();
-                tc::bulk_wait_all();  // the staging must outlive the stores' reads (the CTA exits next)
+                tc::bulk_wait_read_all();  // the staging must outlive the stores' reads (the CTA exits next)
             }
             if (rank == 0 && hf == 0 && lse) lse[rh] = row_lse;
         } else {
