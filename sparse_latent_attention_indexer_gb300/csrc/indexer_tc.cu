@@ -40,8 +40,12 @@ constexpr int TOK = 4;          // query tokens per group
 constexpr int HI = 64;          // indexer heads
 constexpr int DI = 128;         // indexer head dim
 constexpr int BN = TOK * HI;    // 256 (MMA N)
-constexpr int NUM_THREADS = 384;
+// Warps 0-3: TMA producer, MMA issuer, tensor-memory owner, idle; then the epilogue warps.  bf16:
+// 16 of them, one per (TMEM lane quarter, token) pair, four per SM sub-partition.  FP8: 8, each
+// taking two tokens of its lane quarter (measured faster for the shorter FP8 MMA).
 constexpr int EPI_WARP0 = 4;
+template <bool FP8> constexpr int num_epi() { return FP8 ? 8 : 16; }
+template <bool FP8> constexpr int num_threads() { return (EPI_WARP0 + num_epi<FP8>()) * 32; }
 constexpr int SPLIT_TAB = 2 * 152;  // launches with fewer query groups split each group's key blocks
 
 template <bool FP8>
@@ -79,7 +83,7 @@ struct IdxParams {
 };
 
 template <bool FP8>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(num_threads<FP8>(), 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const float *__restrict__ w, const float *__restrict__ q_scale,
                       const float *__restrict__ k_scale, const __grid_constant__ IdxParams P,
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc::mbar_init(bfull, 1);
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&tfull[i], 1);
-            tc::mbar_init(&tempty[i], 8);
+            tc::mbar_init(&tempty[i], num_epi<FP8>());
         }
         tc::mbar_init(mmadone, 1);
         *abort_flag = 0;
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc::tmem_relinquish();
     }
     if (warp >= EPI_WARP0) {
-        for (int i = threadIdx.x - EPI_WARP0 * 32; i < TOK * HI; i += (NUM_THREADS - EPI_WARP0 * 32)) {
+        for (int i = threadIdx.x - EPI_WARP0 * 32; i < TOK * HI; i += (num_threads<FP8>() - EPI_WARP0 * 32)) {
             const int tt = i / HI, h = i % HI;
             float v = 0.0f;
             if (tt < ntok) {
@@ -226,7 +230,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         } else if (warp >= EPI_WARP0) {
             // ---------------- epilogue ----------------
-            const int q = warp & 3, hf = (warp - EPI_WARP0) >> 2;
+            // bf16: warp (q, tt) reduces token tt for the keys of lane quarter q.  FP8: the two
+            // warps of lane quarter q take tokens hf and hf + 2.  Absent tokens are skipped.
+            const int q = warp & 3, t_first = (warp - EPI_WARP0) >> 2, t_step = FP8 ? 2 : 4;
             float *out_base = scores + (int64_t)r0 * P.ld;
             for (int i = 0; i < mine; ++i) {
                 const int acc = i & 1;
@@ -234,59 +240,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc::tc_fence_after();
                 const int key = (split + i * splits) * BM + q * 32 + lane;
                 const float ks = (FP8 && key < S) ? k_scale[kbase + key] : 1.0f;
-                // The two warps of a lane quarter take alternate tokens (hf and hf + 2); absent tokens are
-                // skipped.  bf16: both tokens' 64 head columns are loaded before a single wait, the
-                // accumulator is handed back to the MMA at once, and the two reductions run as four
-                // independent chains.
-                const int tt0 = hf, tt1 = hf + 2;
-                if (FP8) {
-                    // FP8 variant: one token at a time (the two-token form raises register pressure
-                    // past the limit and measured slower here).
 #pragma unroll 1
-                    for (int tt = hf; tt < ntok; tt += 2) {
-                        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + tt * HI;
-                        float v0[32], v1[32];
-                        tc::tmem_ld32(taddr, v0);
-                        tc::tmem_ld32(taddr + 32, v1);
-                        tc::tmem_ld_wait();
-                        const float4 *wv = (const float4 *)(wsm + tt * HI);
-                        float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-                        for (int h4 = 0; h4 < 8; ++h4) {
-                            const float4 a = wv[h4], c = wv[8 + h4];
-                            s0 = fmaf(a.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
-                            s1 = fmaf(c.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
-                            s0 = fmaf(a.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
-                            s1 = fmaf(c.y, fmaxf(v1[4 * h4 + 1], 0.0f), s1);
-                            s0 = fmaf(a.z, fmaxf(v0[4 * h4 + 2], 0.0f), s0);
-                            s1 = fmaf(c.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
-                            s0 = fmaf(a.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
-                            s1 = fmaf(c.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
-                        }
-                        if (key < S) out_base[(int64_t)tt * P.ld + key] = (key <= p0 + tt) ? (s0 + s1) * ks : -INFINITY;
-                    }
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&tempty[acc]);
-                } else if (tt0 < ntok) {
-                    const bool two = tt1 < ntok;  // warp-uniform
-                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
-                    float v0[32], v1[32], v2[32], v3[32];
-                    tc::tmem_ld32(ta + tt0 * HI, v0);
-                    tc::tmem_ld32(ta + tt0 * HI + 32, v1);
-                    if (two) {
-                        tc::tmem_ld32(ta + tt1 * HI, v2);
-                        tc::tmem_ld32(ta + tt1 * HI + 32, v3);
-                    }
+                for (int tt = t_first; tt < ntok; tt += t_step) {
+                    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + tt * HI;
+                    float v0[32], v1[32];
+                    tc::tmem_ld32(taddr, v0);
+                    tc::tmem_ld32(taddr + 32, v1);
                     tc::tmem_ld_wait();
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&tempty[acc]);
-                    const float4 *wa = (const float4 *)(wsm + tt0 * HI), *wb = (const float4 *)(wsm + tt1 * HI);
-                    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+                    if (!FP8) {  // bf16: one token per warp, so the accumulator can go back at once
+                        tc::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+                    }
+                    const float4 *wv = (const float4 *)(wsm + tt * HI);
+                    float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
                     for (int h4 = 0; h4 < 8; ++h4) {
-                        const float4 a = wa[h4], c = wa[8 + h4];
+                        const float4 a = wv[h4], c = wv[8 + h4];
                         s0 = fmaf(a.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
                         s1 = fmaf(c.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
                         s0 = fmaf(a.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
@@ -295,23 +265,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         s1 = fmaf(c.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
                         s0 = fmaf(a.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
                         s1 = fmaf(c.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
-                        if (two) {
-                            const float4 b = wb[h4], d = wb[8 + h4];
-                            s2 = fmaf(b.x, fmaxf(v2[4 * h4 + 0], 0.0f), s2);
-                            s3 = fmaf(d.x, fmaxf(v3[4 * h4 + 0], 0.0f), s3);
-                            s2 = fmaf(b.y, fmaxf(v2[4 * h4 + 1], 0.0f), s2);
-                            s3 = fmaf(d.y, fmaxf(v3[4 * h4 + 1], 0.0f), s3);
-                            s2 = fmaf(b.z, fmaxf(v2[4 * h4 + 2], 0.0f), s2);
-                            s3 = fmaf(d.z, fmaxf(v3[4 * h4 + 2], 0.0f), s3);
-                            s2 = fmaf(b.w, fmaxf(v2[4 * h4 + 3], 0.0f), s2);
-                            s3 = fmaf(d.w, fmaxf(v3[4 * h4 + 3], 0.0f), s3);
-                        }
                     }
-                    if (key < S) {
-                        out_base[(int64_t)tt0 * P.ld + key] = (key <= p0 + tt0) ? (s0 + s1) * ks : -INFINITY;
-                        if (two) out_base[(int64_t)tt1 * P.ld + key] = (key <= p0 + tt1) ? (s2 + s3) * ks : -INFINITY;
-                    }
-                } else {
+                    if (key < S) out_base[(int64_t)tt * P.ld + key] = (key <= p0 + tt) ? (s0 + s1) * ks : -INFINITY;
+                }
+                if (FP8 || t_first >= ntok) {
                     tc::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(&tempty[acc]);
@@ -324,7 +281,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (P.fill_future && split == 0 && warp >= EPI_WARP0) {
         const int start = nblk * BM;
         for (int tt = 0; tt < ntok; ++tt)
-            for (int s = start + threadIdx.x - EPI_WARP0 * 32; s < S; s += NUM_THREADS - EPI_WARP0 * 32)
+            for (int s = start + threadIdx.x - EPI_WARP0 * 32; s < S; s += num_threads<FP8>() - EPI_WARP0 * 32)
                 scores[(int64_t)(r0 + tt) * P.ld + s] = -INFINITY;
     }
     if (warp == 2) {
@@ -429,13 +386,13 @@ cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k
     if (fp8) {
         e = cudaFuncSetAttribute(indexer_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true>::SMEM);
         if (e != cudaSuccess) return e;
-        indexer_tc_kernel<true><<<grid, NUM_THREADS, Cfg<true>::SMEM, s>>>(tq, tk, w, q_scale, k_scale, P, scores);
+        indexer_tc_kernel<true><<<grid, num_threads<true>(), Cfg<true>::SMEM, s>>>(tq, tk, w, q_scale, k_scale, P, scores);
         note_launch(DSA_KERNEL_INDEXER_FP8);
     } else {
         e = cudaFuncSetAttribute(indexer_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg<false>::SMEM);
         if (e != cudaSuccess) return e;
-        indexer_tc_kernel<false><<<grid, NUM_THREADS, Cfg<false>::SMEM, s>>>(tq, tk, w, nullptr, nullptr, P, scores);
+        indexer_tc_kernel<false><<<grid, num_threads<false>(), Cfg<false>::SMEM, s>>>(tq, tk, w, nullptr, nullptr, P, scores);
         note_launch(DSA_KERNEL_INDEXER_TC);
     }
     return cudaGetLastError();
