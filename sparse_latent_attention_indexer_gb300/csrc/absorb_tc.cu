@@ -33,7 +33,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
-constexpr int EPI_THREADS = 256;
+constexpr int HALF_THREADS = 128;  // the four epilogue warps of one column half
 constexpr int STAGES = 4;
 constexpr int SLAB = BM * 128;  // one 64-column bf16 slab of a 128-row block: 16 KB
 
@@ -54,7 +54,7 @@ struct ACfg {
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
 
-// All EPI_THREADS epilogue threads arrive; returns the AND of `v` over them.
+// The HALF_THREADS threads of one column half arrive; returns the AND of `v` over them.
 __device__ __forceinline__ bool epi_bar_and(uint32_t id, bool v) {
     uint32_t r;
     asm volatile(
@@ -63,12 +63,12 @@ __device__ __forceinline__ bool epi_bar_and(uint32_t id, bool v) {
         "bar.red.and.pred p, %2, %3, q;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"((uint32_t)EPI_THREADS)
+        : "r"((uint32_t)v), "r"(id), "r"((uint32_t)HALF_THREADS)
         : "memory");
     return r != 0;
 }
 __device__ __forceinline__ void epi_bar(uint32_t id) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"((uint32_t)EPI_THREADS) : "memory");
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"((uint32_t)HALF_THREADS) : "memory");
 }
 
 struct Unit {
@@ -207,16 +207,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         } else if (warp >= EPI_WARP0) {
             // ---------------- epilogue ----------------
+            // The two column halves (four warps each) run independently: each stages its half of
+            // the tile and one of its threads stores that half, so neither waits for the other.
             const int q = warp & 3, half = (warp - EPI_WARP0) >> 2;
             const int row = q * 32 + lane;
-            const bool leader = threadIdx.x == EPI_WARP0 * 32;
+            const bool leader = lane == 0 && q == 0;  // warp 4 (half 0) or warp 8 (half 1)
+            const uint32_t bar_free = 1 + 2 * half, bar_done = 2 + 2 * half;
             constexpr int COLS = N_TILE / 2;  // columns per epilogue thread
             for (int i = 0; i < mine; ++i) {
                 const int acc = i & 1;
                 bool ok = tc::mbar_wait(&tfull[acc], (i >> 1) & 1, abort_flag, err, 19);
                 // The previous unit's TMA stores must have read the staging tile before it is rewritten.
                 if (leader) tc::bulk_wait_read_all();
-                if (!epi_bar_and(1, ok)) break;
+                if (!epi_bar_and(bar_free, ok)) break;
                 tc::tc_fence_after();
 #pragma unroll 1
                 for (int c0 = 0; c0 < COLS; c0 += 32) {
@@ -241,10 +244,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&tempty[acc]);
                 tc::fence_proxy_async_smem();  // the staging tile is read by the TMA store (async proxy)
-                epi_bar(2);
+                epi_bar(bar_done);
                 if (leader) {
                     const Unit x = unit_of<N_TILE>(P, u0 + i);
-                    for (int cb = 0; cb < N_TILE / 64; ++cb)
+                    for (int cb = half * (COLS / 64); cb < (half + 1) * (COLS / 64); ++cb)
                         tc::tma_store_3d(&tm_c, Cs + cb * (BM * 128), x.n0 + cb * 64, x.h, x.m0);
                     tc::bulk_commit_group();
                 }
