@@ -442,6 +442,7 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1) topk_radix_wide_kernel(const 
 // one-CTA kernels'.
 // ---------------------------------------------------------------------------
 constexpr int CL = 8;              // CTAs per row
+constexpr int LONG_ROW = 8192;     // causal keys from which a few rows take the cluster kernel
 constexpr int CT = 256;            // threads per CTA
 constexpr int CT_WARPS = CT / 32;
 static_assert(CT == TF_THREADS, "find_bin_from_top assumes the filter kernel's block size");
@@ -640,14 +641,17 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int t
         if (T > 0) max_live = max(max_live, min(st.start_pos[b] + T, st.k_len[b]));
     }
     cudaError_t e;
-    // Few long rows: a cluster of CTAs per row when each CTA's slice fits its shared memory.
+    // Few long rows (decode): a cluster of CTAs per row when each CTA's slice fits its shared
+    // memory; rows too long for that take the wide kernel.  Many rows, or short ones (where a
+    // cluster's barriers cost more than they save), take the filter kernel.
     const int slice_cap = (max_live + CL - 1) / CL;
-    if (total_q < 2 * 152 && max_live > k && slice_cap <= 48 * 1024) {
+    const bool few_long = total_q < 2 * 152 && max_live >= LONG_ROW && max_live > k;
+    if (few_long && slice_cap <= 48 * 1024) {
         const size_t smem = (size_t)slice_cap * sizeof(uint32_t);
         e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess) topk_cluster_kernel<<<total_q * CL, CT, smem, s>>>(scores, ld, st, k, idx);
-    } else if (total_q < 2 * 152) {
-        // Few rows: the wide kernel.  Its dynamic shared memory (200 KB) holds the key cache (at
+    } else if (few_long) {
+        // Few rows longer than the cluster's cache: the wide kernel.  Its dynamic shared memory (200 KB) holds the key cache (at
         // least one chunk: it is also the staging area of the ordered pass for longer rows) and
         // the staged output row.
         constexpr int words = 50 * 1024, chunk = KPT * WIDE_THREADS;

@@ -111,10 +111,10 @@ def test_topk(name):
         H.check_selection_row(idx[r], o["scores"], o["absterm"], p, k)
 
 
-# A launch with fewer than 2 x 152 rows takes the cluster top-k kernel (decode: eight CTAs per row),
-# or the wide one-CTA-per-row kernel when a row's slices would not fit the CTAs' shared memory; more
-# rows take the many-rows kernel (prefill: a candidate list, or the global row when the list would
-# overflow).  The cases below run on every side of those switches.
+# A launch with fewer than 2 x 152 rows of at least 8192 causal keys takes the cluster top-k kernel
+# (decode: eight CTAs per row), or the wide one-CTA-per-row kernel when a row's slices would not fit
+# the CTAs' shared memory; every other launch takes the filter kernel (a candidate list, or the global
+# row when the list would overflow).  The cases below run on every side of those switches.
 @pytest.mark.parametrize("T", [700, 100])
 @pytest.mark.parametrize("fill", [1.0, 0.0, -3.5])
 def test_topk_all_equal_scores(fill, T):
