@@ -253,6 +253,18 @@ int dsa_last_cuda_error(void);
  * the recorded site in *site when non-NULL), or DSA_ERR_CUDA.  This is the
  * only entry point that synchronises. */
 int dsa_check_device_error(void *stream, int *site);
+/* Self-test of the failure-detection path (no counterpart on the pages: a
+ * diagnostic of this library).  Launches, on `stream`, one CTA that waits on an
+ * mbarrier phase that nothing completes, through the same bounded wait every
+ * tensor-core kernel here uses, with a limit of `limit_cycles` SM clock cycles
+ * (1 .. 2^32) instead of the kernels' ~2 s.  The wait gives up, records site 90
+ * in the device error word and returns; the CTA then completes the phase and
+ * checks that a second wait on it succeeds, writing 1 to *completed_ok (a device
+ * int, may be NULL) when both behaved.  The GPU does not fault or hang: the
+ * caller reads the outcome with dsa_check_device_error (DSA_ERR_TIMEOUT, site
+ * 90), after which the context is usable as before.  Returns DSA_ERR_INVALID_ARG
+ * for a limit out of range. */
+int dsa_selftest_bounded_wait(int64_t limit_cycles, int *completed_ok, void *stream);
 /* Bit mask of the kernels the last entry point launched on this host thread
  * (DSA_KERNEL_* bits), and how many kernel launches it made. */
 uint32_t dsa_last_kernels(void);
@@ -279,6 +291,7 @@ int dsa_set_stage_events(void *const *events, int n_events);
 #define DSA_KERNEL_MLA_SIMT     (1u << 7)
 #define DSA_KERNEL_MLA_TC       (1u << 8)
 #define DSA_KERNEL_COMBINE      (1u << 9)
+#define DSA_KERNEL_SELFTEST     (1u << 10)
 
 #ifdef __cplusplus
 }

@@ -19,7 +19,7 @@ from ._abi import DSA_BF16, DSA_E4M3, DSA_F32, KERNEL_BITS
 __all__ = [
     "Seqs", "DSAError", "dsa_quant_e4m3_ue8m0", "dsa_indexer_scores", "dsa_topk_select",
     "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_fwd", "dsa_forward_workspace_size", "dsa_forward",
-    "dsa_check_device_error", "last_kernels", "last_launch_count", "build",
+    "dsa_check_device_error", "dsa_selftest_bounded_wait", "last_kernels", "last_launch_count", "build",
 ]
 
 
@@ -107,6 +107,14 @@ def dsa_check_device_error(stream=None):
     site = ctypes.c_int(0)
     st = _abi.load().dsa_check_device_error(_stream(stream), ctypes.byref(site))
     return st, site.value
+
+
+def dsa_selftest_bounded_wait(limit_cycles: int, completed_ok=None, stream=None):
+    """Launch the bounded-wait self-test (a wait that runs out after limit_cycles);
+    read its outcome with dsa_check_device_error."""
+    _check("dsa_selftest_bounded_wait",
+           _abi.load().dsa_selftest_bounded_wait(int(limit_cycles), _ptr(completed_ok) if completed_ok is not None else None,
+                                                 _stream(stream)))
 
 
 def dsa_quant_e4m3_ue8m0(x: torch.Tensor, codes=None, scales=None, stream=None):

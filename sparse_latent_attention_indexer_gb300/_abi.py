@@ -15,6 +15,7 @@ DSA_NOALLOC_SCRATCH_BYTES = 64 << 20
 KERNEL_BITS = {
     "quant": 1 << 0, "indexer_simt": 1 << 1, "indexer_tc": 1 << 2, "indexer_fp8": 1 << 3, "topk": 1 << 4,
     "absorb_simt": 1 << 5, "absorb_tc": 1 << 6, "mla_simt": 1 << 7, "mla_tc": 1 << 8, "combine": 1 << 9,
+    "selftest": 1 << 10,
 }
 
 
@@ -53,6 +54,7 @@ SIGNATURES = [
     ("dsa_status_string", ctypes.c_char_p, [I]),
     ("dsa_last_cuda_error", I, []),
     ("dsa_check_device_error", I, [P, ctypes.POINTER(ctypes.c_int)]),
+    ("dsa_selftest_bounded_wait", I, [I64, P, P]),
     ("dsa_last_kernels", U32, []),
     ("dsa_last_launch_count", I, []),
     ("dsa_set_stage_events", I, [ctypes.POINTER(ctypes.c_void_p), I]),

@@ -255,7 +255,15 @@ int dsa_check_device_error(void *stream, int *site) {
     int rc = indexer_tc_read_error(site);
     if (rc) return rc;
     if ((rc = absorb_tc_read_error(site))) return rc;
-    return mla_tc_read_error(site);
+    if ((rc = mla_tc_read_error(site))) return rc;
+    return selftest_read_error(site);
+}
+
+int dsa_selftest_bounded_wait(int64_t limit_cycles, int *completed_ok, void *stream) {
+    reset_trace();
+    if (limit_cycles < 1 || limit_cycles > (int64_t(1) << 32)) return DSA_ERR_INVALID_ARG;
+    cudaError_t e = launch_bounded_wait_selftest((long long)limit_cycles, completed_ok, (cudaStream_t)stream);
+    return e == cudaSuccess ? DSA_OK : fail_cuda(e);
 }
 
 int dsa_quant_e4m3_ue8m0(const void *x, int x_dtype, int64_t n_blocks, uint8_t *codes, float *scales, void *stream) {

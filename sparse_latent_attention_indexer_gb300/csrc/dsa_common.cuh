@@ -155,4 +155,8 @@ cudaError_t launch_mla_tc(const void *qt, const void *qpe, const void *kv, int64
                           bool prefix_valid, void *olat, float *lse, void *part_ws, cudaStream_t s);
 int mla_tc_read_error(int *site);
 
+// Bounded-wait self-test (selftest.cu): one CTA whose first wait runs out after limit_cycles.
+cudaError_t launch_bounded_wait_selftest(long long limit_cycles, int *completed_ok, cudaStream_t s);
+int selftest_read_error(int *site);
+
 }  // namespace dsa

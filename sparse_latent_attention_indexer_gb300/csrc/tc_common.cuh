@@ -53,16 +53,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 constexpr long long kWaitLimitCycles = 4LL << 30;
 
 // Bounded wait on phase `parity` of `bar`.  Gives up (returns false) when the
-// CTA-wide abort flag is raised or after kWaitLimitCycles; in the second case
+// CTA-wide abort flag is raised or after limit_cycles (default kWaitLimitCycles); in the second case
 // it records `site` in the error word and raises the abort flag.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *err_word,
-                                          int site) {
+                                          int site, long long limit_cycles = kWaitLimitCycles) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(a, parity)) {
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit_cycles) {
             atomicCAS(err_word, 0, site);
             *abort_flag = 1;
             return false;

@@ -105,3 +105,9 @@ def test_forward_rejects_small_workspace():
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         _abi.load(str(tmp_path / "libdsa.so"))
+
+
+def test_bounded_wait_selftest_rejects_out_of_range_limits():
+    lib = _abi.load()
+    assert lib.dsa_selftest_bounded_wait(0, None, None) == _abi.DSA_ERR_INVALID_ARG
+    assert lib.dsa_selftest_bounded_wait((1 << 32) + 1, None, None) == _abi.DSA_ERR_INVALID_ARG
