@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     volatile int *nv = (volatile int *)&never;
+    pdl_wait();  // the set-up above overlapped the previous kernel; global memory only from here
 
     if (mine > 0) {
         if (warp == 0 && lane == 0) {
@@ -309,7 +310,8 @@ cudaError_t launch_absorb(const void *A, const void *W, void *C, int M, int H, i
     cudaError_t e = cudaFuncSetAttribute(absorb_tc_kernel<K_TOTAL, N_TILE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
     if (e != cudaSuccess) return e;
-    absorb_tc_kernel<K_TOTAL, N_TILE><<<grid, NUM_THREADS, G::SMEM, s>>>(ta, tb, tcm, P);
+    e = launch_pdl(absorb_tc_kernel<K_TOTAL, N_TILE>, dim3(grid), dim3(NUM_THREADS), G::SMEM, s, ta, tb, tcm, P);
+    if (e != cudaSuccess) return e;
     note_launch(DSA_KERNEL_ABSORB_TC);
     return cudaGetLastError();
 }

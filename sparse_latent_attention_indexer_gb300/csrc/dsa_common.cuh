@@ -69,6 +69,29 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 // Host-side bookkeeping and shared host logic (dsa_api.cu)
 // ---------------------------------------------------------------------------
 void note_launch(uint32_t kernel_bit);
+
+// Programmatic dependent launch: the kernel may be scheduled while the kernel before it on the
+// stream drains (its on-chip set-up overlaps that tail).  Such a kernel executes pdl_wait() in
+// every thread before its first global-memory access, which waits for the previous grid to
+// complete and its writes to be visible, and pdl_trigger() in every thread once it needs no more
+// SM resources for new work, which lets the next kernel be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
 void reset_trace();
 int fail_cuda(cudaError_t e);
 

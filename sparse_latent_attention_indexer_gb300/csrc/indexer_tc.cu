@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(num_threads<FP8>(), 1)
         tc::tmem_alloc(tmem_slot, 512);
         tc::tmem_relinquish();
     }
+    pdl_wait();  // the set-up above overlapped the previous kernel; global memory only from here
     if (warp >= EPI_WARP0) {
         for (int i = threadIdx.x - EPI_WARP0 * 32; i < TOK * HI; i += (num_threads<FP8>() - EPI_WARP0 * 32)) {
             const int tt = i / HI, h = i % HI;
@@ -277,6 +278,7 @@ __global__ void __launch_bounds__(num_threads<FP8>(), 1)
         }
     }
     __syncthreads();
+    pdl_trigger();
     // Masked tail: keys past every computed block are future keys of all rows.
     if (P.fill_future && split == 0 && warp >= EPI_WARP0) {
         const int start = nblk * BM;
@@ -386,13 +388,17 @@ cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k
     if (fp8) {
         e = cudaFuncSetAttribute(indexer_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true>::SMEM);
         if (e != cudaSuccess) return e;
-        indexer_tc_kernel<true><<<grid, num_threads<true>(), Cfg<true>::SMEM, s>>>(tq, tk, w, q_scale, k_scale, P, scores);
+        e = launch_pdl(indexer_tc_kernel<true>, dim3(grid), dim3(num_threads<true>()), Cfg<true>::SMEM, s, tq, tk, w,
+                       q_scale, k_scale, P, scores);
+        if (e != cudaSuccess) return e;
         note_launch(DSA_KERNEL_INDEXER_FP8);
     } else {
         e = cudaFuncSetAttribute(indexer_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg<false>::SMEM);
         if (e != cudaSuccess) return e;
-        indexer_tc_kernel<false><<<grid, num_threads<false>(), Cfg<false>::SMEM, s>>>(tq, tk, w, nullptr, nullptr, P, scores);
+        e = launch_pdl(indexer_tc_kernel<false>, dim3(grid), dim3(num_threads<false>()), Cfg<false>::SMEM, s, tq, tk,
+                       w, (const float *)nullptr, (const float *)nullptr, P, scores);
+        if (e != cudaSuccess) return e;
         note_launch(DSA_KERNEL_INDEXER_TC);
     }
     return cudaGetLastError();

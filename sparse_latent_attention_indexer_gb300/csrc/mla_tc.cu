@@ -169,6 +169,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
     tc::tc_fence_after();
     tc::cluster_sync();  // both CTAs' barriers exist before any remote arrive
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();  // the set-up above overlapped the previous kernel; global memory only from here
     // This CTA's q~ slice (128 heads x 256 latent columns) comes in by TMA as four 128-byte-swizzled
     // boxes of 64 columns, staged in the exchange buffers, which carry no scores yet.
     if (warp == 2 && lane == 0 && n > 0) {
@@ -547,6 +548,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
 __global__ void __launch_bounds__(256) mla_combine_kernel(const float *__restrict__ opart,
                                                           const float *__restrict__ lpart, int M, int splits,
                                                           __nv_bfloat16 *__restrict__ olat, float *__restrict__ lse) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t rh = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (rh >= (int64_t)M * NH) return;
@@ -646,15 +648,16 @@ cudaError_t launch_mla_tc(const void *qt, const void *qpe, const void *kv, int64
     cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)M * P.splits * 2;
-    mla_tc_kernel<<<grid, NUM_THREADS, SMEM, s>>>(tq, to, (const __nv_bfloat16 *)kv, ld_kv, (const __nv_bfloat16 *)kpe, ld_pe,
-                                                   (const __nv_bfloat16 *)qt, (const __nv_bfloat16 *)qpe, idx, P,
-                                                   (__nv_bfloat16 *)olat, lse,
-                                                   opart, lpart);
+    e = launch_pdl(mla_tc_kernel, dim3(grid), dim3(NUM_THREADS), SMEM, s, tq, to, (const __nv_bfloat16 *)kv, ld_kv,
+                   (const __nv_bfloat16 *)kpe, ld_pe, (const __nv_bfloat16 *)qt, (const __nv_bfloat16 *)qpe, idx, P,
+                   (__nv_bfloat16 *)olat, lse, opart, lpart);
+    if (e != cudaSuccess) return e;
     note_launch(DSA_KERNEL_MLA_TC);
-    e = cudaGetLastError();
-    if (e != cudaSuccess || P.splits == 1) return e;
+    if (P.splits == 1) return cudaSuccess;
     const unsigned cgrid = (unsigned)(((int64_t)M * NH + 7) / 8);
-    mla_combine_kernel<<<cgrid, 256, 0, s>>>(opart, lpart, M, P.splits, (__nv_bfloat16 *)olat, lse);
+    e = launch_pdl(mla_combine_kernel, dim3(cgrid), dim3(256), 0, s, (const float *)opart, (const float *)lpart, M,
+                   P.splits, (__nv_bfloat16 *)olat, lse);
+    if (e != cudaSuccess) return e;
     note_launch(DSA_KERNEL_COMBINE);
     return cudaGetLastError();
 }

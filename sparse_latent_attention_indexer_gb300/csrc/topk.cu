@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(TF_THREADS) topk_filter_kernel(const float *__
     __shared__ int warp_gt[TF_WARPS], warp_eq[TF_WARPS];
     __shared__ int shared3[3];
     int32_t *cand_idx = (int32_t *)(cand + cap);
+    pdl_wait();  // everything below reads or writes global memory
 
     const int r = blockIdx.x;
     const RowInfo ri = row_info(st, r);
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1) topk_radix_wide_kernel(const 
     __shared__ uint32_t warp_tot[2][WARPS];
     __shared__ int sel_bin, sel_above;
 
+    pdl_wait();  // everything below reads or writes global memory
     const int r = blockIdx.x;
     const RowInfo ri = row_info(st, r);
     const int n_live = min(ri.p + 1, ri.S);
@@ -481,6 +483,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(CT)
     __shared__ uint32_t warp_tot[2][CT_WARPS];
     __shared__ int sel[3], warp_sum[CT_WARPS];
 
+    pdl_wait();  // everything below reads or writes global memory
     const int r = blockIdx.x / CL;
     const uint32_t c = cluster_ctarank();
     const RowInfo ri = row_info(st, r);
@@ -649,7 +652,7 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int t
     if (few_long && slice_cap <= 48 * 1024) {
         const size_t smem = (size_t)slice_cap * sizeof(uint32_t);
         e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) topk_cluster_kernel<<<total_q * CL, CT, smem, s>>>(scores, ld, st, k, idx);
+        if (e == cudaSuccess) e = launch_pdl(topk_cluster_kernel, dim3(total_q * CL), dim3(CT), smem, s, scores, ld, st, k, idx);
     } else if (few_long) {
         // Few rows longer than the cluster's cache: the wide kernel.  Its dynamic shared memory (200 KB) holds the key cache (at
         // least one chunk: it is also the staging area of the ordered pass for longer rows) and
@@ -659,7 +662,8 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int t
         const int cap = max_live <= k ? 0 : max(min(max_live, min(CACHE_MAX, words - k)), chunk);
         const size_t smem = ((size_t)cap + (size_t)k) * sizeof(uint32_t);
         e = cudaFuncSetAttribute(topk_radix_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) topk_radix_wide_kernel<<<total_q, WIDE_THREADS, smem, s>>>(scores, ld, st, k, idx, cap);
+        if (e == cudaSuccess)
+            e = launch_pdl(topk_radix_wide_kernel, dim3(total_q), dim3(WIDE_THREADS), smem, s, scores, ld, st, k, idx, cap);
     } else {
         // Many rows: two streaming passes per row and a shared-memory candidate list as long as
         // the longest row (at most CAND_CAP), so that short rows keep more CTAs per SM.
@@ -667,7 +671,8 @@ cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int t
         const size_t smem = (size_t)cap * 2 * sizeof(uint32_t);
         const int vec = ((uintptr_t)scores % 16 == 0 && ld % 4 == 0) ? 1 : 0;
         e = cudaFuncSetAttribute(topk_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) topk_filter_kernel<<<total_q, TF_THREADS, smem, s>>>(scores, ld, st, k, idx, vec, cap);
+        if (e == cudaSuccess)
+            e = launch_pdl(topk_filter_kernel, dim3(total_q), dim3(TF_THREADS), smem, s, scores, ld, st, k, idx, vec, cap);
     }
     if (e != cudaSuccess) return e;
     note_launch(DSA_KERNEL_TOPK);
