@@ -12,23 +12,28 @@
 // row is handled by a cluster of two CTAs on two SMs.  CTA c owns latent
 // columns 256c..256c+255 and rope columns 32c..32c+31 of q~ and of every key,
 // so both gather the same 576 bytes per key.
-//   * q~ and q_pe slices: loaded once into tensor memory (the A operand of
-//     QK^T, so the score MMA reads only the key tile from shared memory).
+//   * q~ slice: loaded once into tensor memory (the A operand of the latent
+//     part of QK^T); the rope slice of q_pe sits in shared memory (A operand
+//     of the two rope MMAs).
 //   * Key tiles (64 keys): four gathering warps copy the selected rows with
 //     cp.async (8 lanes per 128-byte segment, 128-byte swizzle for the latent
 //     slabs, 64-byte swizzle for the rope half) into a 4-stage ring; a copy's
 //     completion arrives on the stage's barrier by itself.
-//   * One thread issues the MMAs: S_c = Q_c K_c^T (M = 128 heads, N = 64
-//     keys) into tensor memory, and O_c += P V_c (N = 256, V read MN-major
-//     straight from the gathered tile, P from tensor memory).
-//   * Eight softmax warps, two threads per head row (32 scores each): each
-//     CTA rounds its partial scores (log2-scaled) to fp16 and bulk-copies them
-//     into the peer's shared memory; both CTAs then add the same two rounded
-//     halves, so they hold bit-identical scores and take identical softmax
-//     decisions.  The exchange is software-pipelined: tile i is shipped while
-//     tile i-1, whose peer half has arrived, is finished.
+//   * One thread issues S_c = Q_c K_c^T (M = 128 heads, N = 64 keys) into one
+//     of two score buffers in tensor memory, another O_c += P V_c (N = 256,
+//     V read MN-major straight from the gathered tile, P from shared memory),
+//     each as its inputs become ready.
+//   * Two softmax groups of four warps take alternate tiles, one thread per
+//     head row and 64 keys each, so one group's exchange and exponentials
+//     overlap the other's.  A group rounds its CTA's partial scores
+//     (log2-scaled) to fp16 and bulk-copies them into the peer's shared
+//     memory; both CTAs then add the same two rounded halves, so they hold
+//     bit-identical scores and take identical softmax decisions.  The
+//     probabilities (bf16) overwrite the received half in place and are the
+//     A operand of that tile's PV product.
 //   * Lazy rescaling: the running maximum moves (and O is rescaled in tensor
-//     memory) only when a tile's maximum exceeds it by more than 2^8.
+//     memory) only when a tile's maximum exceeds it by more than 2^8; each
+//     group hands the row maxima it used to the group of the next tile.
 // Waits are bounded; a timeout records its site in the device error word and
 // both CTAs drain and exit.
 //
@@ -58,17 +63,21 @@ constexpr int SLAB_K = BK * 128;             // 8 KB: 64 keys x 64 columns, 128-
 constexpr int ROPE_K = BK * 64;              // 4 KB: 64 keys x 32 rope columns, 64-byte swizzle
 constexpr int KV_STAGE = NSLAB * SLAB_K + ROPE_K;  // 36 KB (a multiple of 1 KB: swizzle atoms stay aligned)
 constexpr int NSTAGE = 4;
-constexpr int X_BYTES = NH * BK * 2;         // 16 KB: one tile of fp16 partial scores
+// One tile of one group: 128 head rows x 64 keys x 16 bits = 128-byte rows, 128-byte swizzle
+// (chunk c of row h at c ^ (h & 7)): fp16 partial scores in flight, then bf16 probabilities.
+constexpr int X_BYTES = NH * BK * 2;
 constexpr int Q_BOX = NH * 128;              // 16 KB: 128 heads x 64 bf16 columns (one TMA box of q~ or o_lat)
+constexpr int QR_BYTES = NH * 64;            // 8 KB: 128 heads x this CTA's 32 rope columns, 64-byte swizzle
 static_assert(4 * Q_BOX <= 4 * X_BYTES, "the q~ slice is staged in the four exchange buffers");
 static_assert(4 * Q_BOX <= NSTAGE * KV_STAGE, "the context is staged in the key stages");
-constexpr int SMEM = 1024 + NSTAGE * KV_STAGE + 4 * X_BYTES + NSTAGE * BK + 3 * 2 * NH * 4 + 256;
-constexpr int NUM_THREADS = 448;
-constexpr uint32_t SOFT_BAR = 5;             // named barrier of the eight softmax warps (ids 1-4: warp pairs)             // warps 0, 3, 12, 13: gather; 1: MMA; 2: TMEM; 4-11: softmax
+constexpr int SMEM = 1024 + NSTAGE * KV_STAGE + 4 * X_BYTES + QR_BYTES + NSTAGE * BK + 2 * NH * 4 + 4 * NH * 4 + 320;
+static_assert(SMEM <= 232448, "shared memory per CTA");
+constexpr int NUM_THREADS = 448;             // warps 0, 3, 12, 13: gather; 1: QK^T; 2: TMEM, PV; 4-7, 8-11: softmax groups
+constexpr uint32_t SOFT_BAR = 1;             // named barrier of the eight softmax warps (start and end only)
 constexpr int NPROD = 4;                     // gathering warps
-// Tensor-memory columns (512 per CTA): scores, probabilities (bf16 pairs),
-// the resident q~ slice (bf16 pairs, A operand of QK^T) and the context.
-constexpr uint32_t COL_S = 0, COL_P = 64, COL_Q = 96, COL_O = 256;
+// Tensor-memory columns (512 per CTA): two score buffers (one per softmax group), the resident
+// q~ slice (bf16 pairs, A operand of QK^T) and the context.
+constexpr uint32_t COL_S = 0, COL_Q = 128, COL_O = 256;
 constexpr uint32_t IDESC_QK = tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, NH, BK, 0, 0);
 constexpr uint32_t IDESC_PV = tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, NH, 256, 0, 1);
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -96,10 +105,13 @@ __device__ __forceinline__ int find_seq(const MlaParams &P, int r) {
     return lo;
 }
 
+// Index [g] is the softmax group (tile parity); hand[q][g] carries group g's row maxima of lane
+// quarter q to the other group.
 struct Bars {
-    uint64_t q_stage, q_ready, kv_full[NSTAGE], kv_empty[NSTAGE], s_full, s_empty, p_full, p_empty, xfull[2], xempty[2],
-        o_done;
+    uint64_t q_stage, q_ready, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2],
+        xfull[2], xempty[2], hand[4][2], o_done;
 };
+static_assert(sizeof(Bars) + 8 <= 320, "barrier area");
 
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most 4 per SM sub-partition x 128 regs
     mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
@@ -111,12 +123,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *KV = base;
-    uint8_t *X = KV + NSTAGE * KV_STAGE;               // [2 tiles] the peer's partial scores land here
-    uint8_t *Y = X + 2 * X_BYTES;                      // [2 tiles] this CTA's partial scores, sent from here
-    uint8_t *kvalid = Y + 2 * X_BYTES;                 // [NSTAGE][BK]
-    float *pmax = (float *)(kvalid + NSTAGE * BK);     // [2 tiles][2 halves][NH] row-maximum halves
-    float *lsum = pmax + 4 * NH;                       // [2 halves][NH] row-sum halves
-    Bars *bar = (Bars *)(lsum + 2 * NH);
+    uint8_t *X = KV + NSTAGE * KV_STAGE;               // [group] the peer's partial scores land here, then P
+    uint8_t *Y = X + 2 * X_BYTES;                      // [group] this CTA's partial scores, sent from here
+    uint8_t *QR = Y + 2 * X_BYTES;                     // rope slice of q_pe (A operand)
+    uint8_t *kvalid = QR + QR_BYTES;                   // [NSTAGE][BK]
+    float *m_pub = (float *)(kvalid + NSTAGE * BK);    // [group][NH] row maxima handed to the other group
+    float *lm = m_pub + 2 * NH;                        // [group][NH][2] final (row sum, reference) per group
+    Bars *bar = (Bars *)(lm + 4 * NH);
     uint32_t *tmem_slot = (uint32_t *)(bar + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
     __shared__ int never;
@@ -146,14 +159,16 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             tc::mbar_init(&bar->kv_full[i], 2 * NPROD * 32);
             tc::mbar_init(&bar->kv_empty[i], 1);
         }
-        tc::mbar_init(&bar->s_full, 1);
-        tc::mbar_init(&bar->s_empty, 8);
-        tc::mbar_init(&bar->p_full, 8);
-        tc::mbar_init(&bar->p_empty, 1);
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&bar->xfull[i], 1);   // armed locally with the 32 KB the peer sends
-            // one arrival per peer softmax warp; phase 0 = the peer's q~ staging (below) has been read
-            tc::mbar_init(&bar->xempty[i], 8);
+        for (int g = 0; g < 2; ++g) {
+            tc::mbar_init(&bar->s_full[g], 1);
+            tc::mbar_init(&bar->s_empty[g], 4);  // the group's four warps have read the scores
+            tc::mbar_init(&bar->p_full[g], 4);   // ... have written the probabilities
+            tc::mbar_init(&bar->p_empty[g], 1);
+            tc::mbar_init(&bar->xfull[g], 1);    // armed locally with the 16 KB the peer sends
+            // phase 0: the peer's q~ staging (below) has been read; then one phase per PV product
+            // of the peer on this buffer (its X[g] is free again)
+            tc::mbar_init(&bar->xempty[g], 1);
+            for (int qq = 0; qq < 4; ++qq) tc::mbar_init(&bar->hand[qq][g], 1);
         }
         tc::mbar_init(&bar->o_done, 1);
         *abort_flag = 0;
@@ -221,78 +236,86 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         }
         tc::cp_async_wait<0>();  // nothing may still be copying when the CTA exits
     } else if (warp == 1 && lane == 0 && n > 0) {
-        // ---------------- MMA issuer ----------------
+        // ---------------- QK^T issuer ----------------
+        // QK^T(j) needs tile j gathered and its score buffer (j & 1) read by the group of tile j-2.
+        // The PV products come from another thread (warp 2): an MMA issue blocks while the tensor
+        // pipe is busy, so one thread for both streams would hold each up behind the other.
         bool ok = tc::mbar_wait(&bar->q_ready, 0, abort_flag, err, 24);
-        const uint32_t kv0 = tc::smem_u32(KV);
-        auto issue_qk = [&](int j) -> bool {
+        const uint32_t kv0 = tc::smem_u32(KV), qr0 = tc::smem_u32(QR);
+        for (int j = 0; ok && j < n; ++j) {
             const int st = j % NSTAGE;
-            if (!tc::mbar_wait(&bar->kv_full[st], (j / NSTAGE) & 1, abort_flag, err, 25)) return false;
-            // the gathered rows were written by cp.async (generic proxy); the MMA reads them
-            // through the async proxy
+            if (j >= 2 && !(ok = tc::mbar_wait(&bar->s_empty[j & 1], ((j >> 1) - 1) & 1, abort_flag, err, 26))) break;
+            if (!(ok = tc::mbar_wait(&bar->kv_full[st], (j / NSTAGE) & 1, abort_flag, err, 25))) break;
+            // the gathered rows were written by cp.async (generic proxy); the MMA reads them through
+            // the async proxy
             tc::fence_proxy_async_smem();
-            if (!tc::mbar_wait(&bar->s_empty, (j & 1) ^ 1, abort_flag, err, 26)) return false;
             tc::tc_fence_after();
+            const uint32_t d = tmem + COL_S + (j & 1) * BK;
 #pragma unroll
             for (int js = 0; js < NSLAB; ++js)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t bd = tc::smem_desc(kv0 + st * KV_STAGE + js * SLAB_K + kk * 32, 16, 1024);
-                    tc::mma_f16_ts(tmem + COL_S, tmem + COL_Q + js * 32 + kk * 8, bd, IDESC_QK, (js | kk) != 0);
+                    tc::mma_f16_ts(d, tmem + COL_Q + js * 32 + kk * 8, bd, IDESC_QK, (js | kk) != 0);
                 }
-            // rope half: K-major, 64-byte swizzle (8-key atoms of 512 bytes)
+            // rope half: both operands K-major with the 64-byte swizzle (8-row atoms of 512 bytes)
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
+                const uint64_t ad = tc::smem_desc(qr0 + kk * 32, 16, 512, tc::kSwizzle64B);
                 const uint64_t bd = tc::smem_desc(kv0 + st * KV_STAGE + NSLAB * SLAB_K + kk * 32, 16, 512,
                                                   tc::kSwizzle64B);
-                tc::mma_f16_ts(tmem + COL_S, tmem + COL_Q + NSLAB * 32 + kk * 8, bd, IDESC_QK, true);
+                tc::mma_f16(d, ad, bd, IDESC_QK, 1);
             }
-            tc::mma_commit(&bar->s_full);
-            return true;
-        };
-        // The softmax warps read the scores of tile j at the start of their iteration j and hand back
-        // P(j-1) at its end, so QK^T(j+1) is issued as soon as S(j) is read, ahead of PV(j-1).
-        auto issue_pv = [&](int i) -> bool {
-            if (!tc::mbar_wait(&bar->p_full, i & 1, abort_flag, err, 27)) return false;
+            tc::mma_commit(&bar->s_full[j & 1]);
+        }
+        // Every score tile issued here is read by a softmax group before its PV product exists, so
+        // these MMAs have completed before the context is final.
+    } else if (warp == 2 && lane == 0 && n > 0) {
+        // ---------------- PV issuer ----------------
+        // PV(j) once P(j) is written; its completion frees the key stage, this CTA's X buffer (the
+        // peer may send the next tile of that group) and, for a rescale, the context.
+        const uint32_t kv0 = tc::smem_u32(KV), x0 = tc::smem_u32(X);
+        const uint16_t peer_mask = (uint16_t)(1u << peer);
+        for (int j = 0; j < n; ++j) {
+            if (!tc::mbar_wait(&bar->p_full[j & 1], (j >> 1) & 1, abort_flag, err, 27)) break;
             tc::tc_fence_after();
-            const int st = i % NSTAGE;
+            const int st = j % NSTAGE;
+            const uint32_t pa = x0 + (j & 1) * X_BYTES;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                // V: MN-major view of latent slabs 0..3 of the tile (LBO = slab stride, SBO = 8 keys).
+                // P: K-major rows of 64 keys (128-byte swizzle); V: MN-major view of latent slabs
+                // 0..3 of the tile (LBO = slab stride, SBO = 8 keys).
+                const uint64_t ad = tc::smem_desc(pa + kk * 32, 16, 1024);
                 const uint64_t bd = tc::smem_desc(kv0 + st * KV_STAGE + kk * 16 * 128, SLAB_K, 1024);
-                tc::mma_f16_ts(tmem + COL_O, tmem + COL_P + kk * 8, bd, IDESC_PV, (i | kk) != 0);
+                tc::mma_f16(tmem + COL_O, ad, bd, IDESC_PV, (j | kk) != 0);
             }
             tc::mma_commit(&bar->kv_empty[st]);
-            tc::mma_commit(&bar->p_empty);
-            return true;
-        };
-        if (ok) ok = issue_qk(0);
-        for (int j = 0; ok && j < n; ++j) {
-            if (j + 1 < n && !(ok = issue_qk(j + 1))) break;
-            if (j >= 1 && !(ok = issue_pv(j - 1))) break;
+            tc::mma_commit(&bar->p_empty[j & 1]);
+            tc::mma_commit_multicast(&bar->xempty[j & 1], peer_mask);  // the peer may refill our X
         }
-        if (ok) issue_pv(n - 1);
         tc::mma_commit(&bar->o_done);
         tc::mbar_wait(&bar->o_done, 0, nv, err, 28);
     } else if (warp >= 4 && warp < 12) {
-        // ---------------- softmax: two threads per head (TMEM lane), 32 score columns each ----------------
-        const int q = warp & 3, hf = (warp - 4) >> 2, h = q * 32 + lane;
+        // ---------------- softmax: group g takes tiles g, g+2, ...; one thread per head row ----------------
+        const int q = warp & 3, g = (warp - 4) >> 2, h = q * 32 + lane;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        float m_used = -INFINITY, l = 0.0f;  // l: this thread's half of the row sum
+        const unsigned FULL = 0xffffffffu;
+        float m_g = -INFINITY, l_g = 0.0f;  // this group's part of the row sum, relative to 2^m_g
         bool done_ok = true;
         if (n > 0) {
             // This CTA's slice of the head's q~ row -> tensor memory (A operand of QK^T): latent
             // columns as 4 slabs of 32 packed columns (from the TMA staging; chunk e of row h sits at
-            // e ^ (h & 7)), then the rope half as 16 more; the two threads of a row split the slabs
-            // and the second one also takes the rope half (read in place).
+            // e ^ (h & 7)); group g moves slabs 2g and 2g+1.  Group 1 also puts the rope slice of
+            // q_pe (read in place) into shared memory, K-major with the 64-byte swizzle.
             uint4 rq[4];
-            if (hf) {
+            if (g) {
                 const uint4 *rsrc = (const uint4 *)(qpe + ((int64_t)r * NH + h) * DR + rank * 32);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) rq[e] = __ldg(rsrc + e);
             }
             if (!tc::mbar_wait(&bar->q_stage, 0, abort_flag, err, 23)) done_ok = false;
             if (done_ok) {
-                for (int js = hf * 2; js < hf * 2 + 2; ++js) {
+                for (int js = g * 2; js < g * 2 + 2; ++js) {
                     const uint8_t *srow = X + js * Q_BOX + h * 128;
                     uint32_t qv[32];
 #pragma unroll
@@ -305,190 +328,193 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                     }
                     tc::tmem_st32(tmem + lane_off + COL_Q + js * 32, qv);
                 }
-                if (hf) {
-                    uint32_t qv[16];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        qv[4 * e] = rq[e].x;
-                        qv[4 * e + 1] = rq[e].y;
-                        qv[4 * e + 2] = rq[e].z;
-                        qv[4 * e + 3] = rq[e].w;
-                    }
-                    tc::tmem_st16(tmem + lane_off + COL_Q + NSLAB * 32, qv);
-                }
                 tc::tmem_st_wait();
+            }
+            if (g) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) *(uint4 *)(QR + h * 64 + ((e ^ ((h >> 1) & 3)) << 4)) = rq[e];
+                tc::fence_proxy_async_smem();  // read by the rope MMAs (async proxy)
             }
             tc::tc_fence_before();
             // Every softmax warp has read its part of the staging before any of them writes a score
-            // tile into Y, and then tells the peer that this CTA's X buffers may receive scores.
+            // tile into Y, and then the peer learns that this CTA's X buffers may receive scores.
             asm volatile("bar.sync %0, %1;" ::"r"(SOFT_BAR), "r"(8 * 32) : "memory");
-            if (lane == 0) {
-                tc::mbar_arrive(&bar->q_ready);
+            if (lane == 0) tc::mbar_arrive(&bar->q_ready);
+            if (threadIdx.x == 4 * 32) {
                 tc::mbar_arrive_remote(tc::map_peer(tc::smem_u32(&bar->xempty[0]), peer));
                 tc::mbar_arrive_remote(tc::map_peer(tc::smem_u32(&bar->xempty[1]), peer));
             }
         }
         const float sl2 = P.scale_log2;
-        const uint32_t row_sw = (uint32_t)((h >> 1) & 3);
-        // The partial scores travel as fp16 of the log2-scaled scores, 64 bytes per half row.
-        // X[2] and Y[2] are [half][128 rows][32 fp16]: a warp's 32 rows of one half form a contiguous
-        // 2 KB block; the 16-byte chunks of a row are rotated by the row to spread the banks.
-        const int roff = (hf * NH + h) * 64, wblk = (hf * NH + q * 32) * 64;
-        const uint32_t named = 1 + q;  // the two warps of a lane quarter
-        // Software pipeline: iteration i loads tile i's partial scores and ships them to the
-        // peer, then finishes tile i-1, whose peer half arrived while tile i was being shipped.
-        // Both CTAs sum the same two rounded halves, so they hold bit-identical scores.
-        uint32_t prev[16];  // the previous tile's own partial scores (packed fp16 pairs)
-        for (int i = 0; i <= n; ++i) {
-            uint32_t cur[16];
-            if (i < n) {
-                if (!tc::mbar_wait(&bar->s_full, i & 1, abort_flag, err, 31)) { done_ok = false; break; }
-                tc::tc_fence_after();
-                float sc[32];
-                tc::tmem_ld32(tmem + lane_off + COL_S + hf * 32, sc);
+        const uint32_t hsw = (uint32_t)(h & 7);
+        uint8_t *Xg = X + g * X_BYTES, *Yg = Y + g * X_BYTES;
+        const int roff = h * 128, wblk = q * 32 * 128;  // this row; this warp's 32 rows (4 KB)
+        for (int t = g, k = 0; done_ok && t < n; t += 2, ++k) {
+            const uint32_t ph = (uint32_t)k & 1u;
+            // --- this CTA's partial scores of tile t -> fp16 of the log2-scaled values ---
+            if (!__all_sync(FULL, tc::mbar_wait(&bar->s_full[g], ph, abort_flag, err, 31))) { done_ok = false; break; }
+            tc::tc_fence_after();
+            uint32_t cur[32];
+            {
+                float sa[32], sb[32];
+                tc::tmem_ld32(tmem + lane_off + COL_S + g * BK, sa);
+                tc::tmem_ld32(tmem + lane_off + COL_S + g * BK + 32, sb);
                 tc::tmem_ld_wait();
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&bar->s_empty);  // the MMA may now compute the next tile's scores
-#pragma unroll
-                for (int j = 0; j < 16; ++j) cur[j] = tc::f16x2_satfinite(sc[2 * j] * sl2, sc[2 * j + 1] * sl2);
-                const int xb = i & 1;
-                if (threadIdx.x == 4 * 32) tc::mbar_arrive_expect_tx(&bar->xfull[xb], X_BYTES);
-                // The peer's X[xb] is free once the peer has read its q~ staging (tiles 0, 1) or tile
-                // i-2 from it (then the copy that delivered tile i-2 has also finished reading Y[xb]).
-                bool ok = true;
-                if (lane == 0) ok = tc::mbar_wait_cluster(&bar->xempty[xb], (i >> 1) & 1, abort_flag, err, 32);
-                __syncwarp();
-                if (!__shfl_sync(0xffffffffu, ok, 0)) { done_ok = false; break; }
-                uint8_t *yrow = Y + xb * X_BYTES + roff;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *(uint4 *)(yrow + ((c ^ row_sw) << 4)) = make_uint4(cur[4 * c], cur[4 * c + 1], cur[4 * c + 2], cur[4 * c + 3]);
-                tc::fence_proxy_async_smem();  // the stores are read by the bulk copy (async proxy)
-                __syncwarp();
-                if (lane == 0)
-                    tc::bulk_copy_to_peer(tc::map_peer(tc::smem_u32(X + xb * X_BYTES) + wblk, peer),
-                                          Y + xb * X_BYTES + wblk, 32 * 64,
-                                          tc::map_peer(tc::smem_u32(&bar->xfull[xb]), peer));
-            }
-            if (i > 0) {
-                // ---------------- finish tile t = i - 1 ----------------
-                const int t = i - 1, xb = t & 1, st = t % NSTAGE;
-                float v[32];
-                if (!tc::mbar_wait_cluster(&bar->xfull[xb], (t >> 1) & 1, abort_flag, err, 33)) { done_ok = false; break; }
-                const uint8_t *xrow = X + xb * X_BYTES + roff;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 x = *(const uint4 *)(xrow + ((c ^ row_sw) << 4));
-                    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        // peer half + own half in fp32 (addition commutes: both CTAs get the same sum)
-                        const uint32_t own = prev[4 * c + e];
-                        v[8 * c + 2 * e] = tc::add_f16_f32((uint16_t)(xs[e] & 0xffffu), tc::f16_to_f32((uint16_t)(own & 0xffffu)));
-                        v[8 * c + 2 * e + 1] = tc::add_f16_f32((uint16_t)(xs[e] >> 16), tc::f16_to_f32((uint16_t)(own >> 16)));
-                    }
-                }
-                // X[xb] may be overwritten by the peer's copy of tile t+2 once every lane of every warp
-                // has read it.  The warp barrier orders the lanes' loads before lane 0's arrive, and the
-                // arrive's release (CTA scope: the loads are of this CTA's own shared memory) keeps them
-                // ahead of the peer's view of the arrival.
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive_remote(tc::map_peer(tc::smem_u32(&bar->xempty[xb]), peer));
-                // --- mask: entries that are padding, future or outside the sequence ---
-                if (!tc::mbar_wait(&bar->kv_full[st], (t / NSTAGE) & 1, abort_flag, err, 34)) { done_ok = false; break; }
-                {
-                    const uint4 *kv4 = (const uint4 *)(kvalid + st * BK + hf * 32);
-                    const uint4 m0 = kv4[0], m1 = kv4[1];
-                    const uint32_t all = m0.x & m0.y & m0.z & m0.w & m1.x & m1.y & m1.z & m1.w;
-                    if (all != 0x01010101u) {
-                        const uint32_t *kvw = (const uint32_t *)(kvalid + st * BK + hf * 32);
-#pragma unroll
-                        for (int wd = 0; wd < 8; ++wd) {
-                            const uint32_t bits = kvw[wd];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                if (!((bits >> (8 * u)) & 0xffu)) v[4 * wd + u] = -INFINITY;
-                        }
-                    }
-                }
-                float mh = tc::max3(v[0], v[1], v[2]);
-#pragma unroll
-                for (int j = 3; j < 31; j += 2) mh = tc::max3(mh, v[j], v[j + 1]);
-                mh = fmaxf(mh, v[31]);
-                // row maximum = max of the two halves (double-buffered by tile parity)
-                pmax[(t & 1) * 2 * NH + hf * NH + h] = mh;
-                asm volatile("bar.sync %0, 64;" ::"r"(named) : "memory");
-                const float mraw = fmaxf(mh, pmax[(t & 1) * 2 * NH + (1 - hf) * NH + h]);
-                const float mt = mraw;  // the scores are already in log2 units
-                bool rescale = false;
-                float alpha = 1.0f;
-                if (mt != -INFINITY) {
-                    if (m_used == -INFINITY) {
-                        m_used = mt;
-                    } else if (mt > m_used + RESCALE_LOG2) {
-                        alpha = tc::ex2_approx(m_used - mt);
-                        l *= alpha;
-                        m_used = mt;
-                        rescale = true;
-                    }
-                }
-                const float neg_m = m_used == -INFINITY ? 0.0f : -m_used;
-                uint32_t pk[16];
-                float psum0 = 0.0f, psum1 = 0.0f;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const float p0 = tc::ex2_approx(v[2 * j] + neg_m);
-                    const float p1 = tc::ex2_approx(v[2 * j + 1] + neg_m);
-                    const __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
-                    pk[j] = *(const uint32_t *)&t2;
-                    // the row sum takes the rounded probabilities that the PV product uses
-                    psum0 = tc::add_bf16_f32((uint16_t)(pk[j] & 0xffffu), psum0);
-                    psum1 = tc::add_bf16_f32((uint16_t)(pk[j] >> 16), psum1);
+                    cur[j] = tc::f16x2_satfinite(sa[2 * j] * sl2, sa[2 * j + 1] * sl2);
+                    cur[16 + j] = tc::f16x2_satfinite(sb[2 * j] * sl2, sb[2 * j + 1] * sl2);
                 }
-                l += psum0 + psum1;
-                // the previous PV product must be done before P and O are touched
-                if (t > 0 && !tc::mbar_wait(&bar->p_empty, (t - 1) & 1, abort_flag, err, 35)) { done_ok = false; break; }
-                tc::tc_fence_after();
-                // tcgen05.ld/st are warp-wide: rescale the warp's half of the O columns when any
-                // of its rows needs it (rows that do not keep alpha = 1).
-                if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-                    for (int cc = hf * 4; cc < hf * 4 + 4; ++cc) {
-                        float o[32];
-                        uint32_t ob[32];
-                        tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
-                        tc::tmem_ld_wait();
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bar->s_empty[g]);  // the MMA may compute tile t+2 into this buffer
+            // --- ship: Y[g] -> the peer's X[g]; the peer's half of this tile arrives in ours ---
+            if (q == 0 && lane == 0) tc::mbar_arrive_expect_tx(&bar->xfull[g], X_BYTES);
+            // The peer's X[g] is free once the peer has read its q~ staging (first tile of the group)
+            // or its PV product of tile t-2 is done (which also means its copy of tile t-2 had landed,
+            // so our copy has finished reading Y[g]).
+            bool ok = true;
+            if (lane == 0) ok = tc::mbar_wait_cluster(&bar->xempty[g], ph, abort_flag, err, 32);
+            __syncwarp();
+            if (!__shfl_sync(FULL, ok, 0)) { done_ok = false; break; }
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) ob[j] = __float_as_uint(o[j] * alpha);
-                        tc::tmem_st32(tmem + lane_off + COL_O + cc * 32, ob);
+            for (int c = 0; c < 8; ++c)
+                *(uint4 *)(Yg + roff + ((c ^ hsw) << 4)) = make_uint4(cur[4 * c], cur[4 * c + 1], cur[4 * c + 2], cur[4 * c + 3]);
+            tc::fence_proxy_async_smem();  // the stores are read by the bulk copy (async proxy)
+            __syncwarp();
+            if (lane == 0)
+                tc::bulk_copy_to_peer(tc::map_peer(tc::smem_u32(Xg) + wblk, peer), Yg + wblk, 32 * 128,
+                                      tc::map_peer(tc::smem_u32(&bar->xfull[g]), peer));
+            // --- peer half + own half in fp32 (addition commutes: both CTAs get the same sum) ---
+            if (!__all_sync(FULL, tc::mbar_wait_cluster(&bar->xfull[g], ph, abort_flag, err, 33))) { done_ok = false; break; }
+            float v[64];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 x = *(const uint4 *)(Xg + roff + ((c ^ hsw) << 4));
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t own = cur[4 * c + e];
+                    v[8 * c + 2 * e] = tc::add_f16_f32((uint16_t)(xs[e] & 0xffffu), tc::f16_to_f32((uint16_t)(own & 0xffffu)));
+                    v[8 * c + 2 * e + 1] = tc::add_f16_f32((uint16_t)(xs[e] >> 16), tc::f16_to_f32((uint16_t)(own >> 16)));
+                }
+            }
+            // --- mask: entries that are padding, future or outside the sequence ---
+            const int st = t % NSTAGE;
+            if (!__all_sync(FULL, tc::mbar_wait(&bar->kv_full[st], (t / NSTAGE) & 1, abort_flag, err, 34))) { done_ok = false; break; }
+            {
+                const uint4 *kv4 = (const uint4 *)(kvalid + st * BK);
+                const uint4 m0 = kv4[0], m1 = kv4[1], m2 = kv4[2], m3 = kv4[3];
+                const uint32_t all = m0.x & m0.y & m0.z & m0.w & m1.x & m1.y & m1.z & m1.w & m2.x & m2.y & m2.z &
+                                     m2.w & m3.x & m3.y & m3.z & m3.w;
+                if (all != 0x01010101u) {
+                    const uint32_t *kvw = (const uint32_t *)(kvalid + st * BK);
+#pragma unroll
+                    for (int wd = 0; wd < 16; ++wd) {
+                        const uint32_t bits = kvw[wd];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            if (!((bits >> (8 * u)) & 0xffu)) v[4 * wd + u] = -INFINITY;
                     }
                 }
-                tc::tmem_st16(tmem + lane_off + COL_P + hf * 16, pk);  // 32 bf16 probabilities as 16 packed columns
+            }
+            float mt = tc::max3(v[0], v[1], v[2]);
+#pragma unroll
+            for (int j = 3; j < 63; j += 2) mt = tc::max3(mt, v[j], v[j + 1]);
+            mt = fmaxf(mt, v[63]);
+            // --- running maximum: the one used for tile t-1 comes from the other group ---
+            float m_prev = -INFINITY;
+            if (t > 0) {
+                if (!__all_sync(FULL, tc::mbar_wait(&bar->hand[q][1 - g], ((t - 1) >> 1) & 1, abort_flag, err, 37))) {
+                    done_ok = false;
+                    break;
+                }
+                m_prev = m_pub[(1 - g) * NH + h];
+            }
+            float m_now = m_prev;  // the scores are already in log2 units
+            bool rescale = false;
+            if (mt != -INFINITY) {
+                if (m_prev == -INFINITY) {
+                    m_now = mt;
+                } else if (mt > m_prev + RESCALE_LOG2) {
+                    m_now = mt;
+                    rescale = true;
+                }
+            }
+            if (t + 1 < n) {
+                m_pub[g * NH + h] = m_now;
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bar->hand[q][g]);
+            }
+            if (m_now != m_g) {
+                if (m_g != -INFINITY) l_g *= tc::ex2_approx(m_g - m_now);
+                m_g = m_now;
+            }
+            const float neg_m = m_now == -INFINITY ? 0.0f : -m_now;
+            uint32_t pk[32];
+            float psum0 = 0.0f, psum1 = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = tc::ex2_approx(v[2 * j] + neg_m);
+                const float p1 = tc::ex2_approx(v[2 * j + 1] + neg_m);
+                const __nv_bfloat162 t2 = __floats2bfloat162_rn(p0, p1);
+                pk[j] = *(const uint32_t *)&t2;
+                // the row sum takes the rounded probabilities that the PV product uses
+                psum0 = tc::add_bf16_f32((uint16_t)(pk[j] & 0xffffu), psum0);
+                psum1 = tc::add_bf16_f32((uint16_t)(pk[j] >> 16), psum1);
+            }
+            l_g += psum0 + psum1;
+            // --- O is rescaled after PV(t-1) and before PV(t); tcgen05.ld/st are warp-wide, so the
+            // whole warp takes part when any of its rows moves (the others keep alpha = 1) ---
+            if (__any_sync(FULL, rescale)) {
+                const float alpha = rescale ? tc::ex2_approx(m_prev - m_now) : 1.0f;
+                if (!__all_sync(FULL, tc::mbar_wait(&bar->p_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, err, 35))) {
+                    done_ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+#pragma unroll 1
+                for (int cc = 0; cc < 8; ++cc) {
+                    float o[32];
+                    uint32_t ob[32];
+                    tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ob[j] = __float_as_uint(o[j] * alpha);
+                    tc::tmem_st32(tmem + lane_off + COL_O + cc * 32, ob);
+                }
                 tc::tmem_st_wait();
                 tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&bar->p_full);
             }
-            if (i < n) {
+            // --- P(t) overwrites the received half (each row is read and written by its own thread) ---
 #pragma unroll
-                for (int j = 0; j < 16; ++j) prev[j] = cur[j];
-            }
+            for (int c = 0; c < 8; ++c)
+                *(uint4 *)(Xg + roff + ((c ^ hsw) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            tc::fence_proxy_async_smem();  // read by the PV product (async proxy)
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bar->p_full[g]);
         }
         // ---------------- epilogue: normalise and store this thread's 128 columns ----------------
-        lsum[hf * NH + h] = l;
-        asm volatile("bar.sync %0, 64;" ::"r"(named) : "memory");
-        const float lrow = l + lsum[(1 - hf) * NH + h];
+        // The row sum of each group is relative to the last maximum that group used; the context is
+        // relative to the last maximum of all (the running maximum never decreases).
+        lm[(g * NH + h) * 2] = l_g;
+        lm[(g * NH + h) * 2 + 1] = m_g;
+        asm volatile("bar.sync %0, %1;" ::"r"(SOFT_BAR), "r"(8 * 32) : "memory");
+        const float la = lm[h * 2], ma = lm[h * 2 + 1], lb = lm[(NH + h) * 2], mb = lm[(NH + h) * 2 + 1];
+        const float m_f = fmaxf(ma, mb);
+        const float lrow = (ma == -INFINITY ? 0.0f : la * tc::ex2_approx(ma - m_f)) +
+                           (mb == -INFINITY ? 0.0f : lb * tc::ex2_approx(mb - m_f));
         const int64_t rh = (int64_t)r * NH + h;
-        const bool have = __all_sync(0xffffffffu, n > 0 && done_ok && tc::mbar_wait(&bar->o_done, 0, abort_flag, err, 36));
+        const bool have = __all_sync(FULL, n > 0 && done_ok && tc::mbar_wait(&bar->o_done, 0, abort_flag, err, 36));
         const float inv = (have && lrow > 0.0f) ? 1.0f / lrow : 0.0f;
-        const float row_lse = (have && lrow > 0.0f) ? (m_used + log2f(lrow)) * LN2 : -INFINITY;
+        const float row_lse = (have && lrow > 0.0f) ? (m_f + log2f(lrow)) * LN2 : -INFINITY;
         if (have) tc::tc_fence_after();
         if (P.splits == 1) {
             // bf16 context -> the key stages (free: every PV product is done), as four 128-byte-
             // swizzled boxes of 64 columns, then out by TMA tensor stores.
 #pragma unroll 1
-            for (int cc = hf * 4; cc < hf * 4 + 4; ++cc) {
+            for (int cc = g * 4; cc < g * 4 + 4; ++cc) {
                 float o[32];
                 if (have) {
                     tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
@@ -515,12 +541,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                 tc::bulk_commit_group();
                 tc::bulk_wait_read_all();  // the staging must outlive the stores' reads (the CTA exits next)
             }
-            if (rank == 0 && hf == 0 && lse) lse[rh] = row_lse;
+            if (rank == 0 && g == 0 && lse) lse[rh] = row_lse;
         } else {
             const int64_t part = ((int64_t)r * P.splits + split) * NH + h;
             float *dst = opart + part * DC + rank * 256;
 #pragma unroll 1
-            for (int cc = hf * 4; cc < hf * 4 + 4; ++cc) {
+            for (int cc = g * 4; cc < g * 4 + 4; ++cc) {
                 float o[32];
                 if (have) {
                     tc::tmem_ld32(tmem + lane_off + COL_O + cc * 32, o);
@@ -532,7 +558,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                     d4[e] = have ? make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv)
                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
-            if (rank == 0 && hf == 0) lpart[part] = row_lse;
+            if (rank == 0 && g == 0) lpart[part] = row_lse;
         }
     }
     __syncthreads();
