@@ -109,7 +109,7 @@ __device__ __forceinline__ int find_seq(const MlaParams &P, int r) {
 // quarter q to the other group.
 struct Bars {
     uint64_t q_stage, q_ready, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2],
-        xfull[2], xempty[2], hand[4][2], o_done;
+        xfull[2], xempty[2], yfree[2], hand[4][2], o_done;
 };
 static_assert(sizeof(Bars) + 8 <= 320, "barrier area");
 
@@ -168,6 +168,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             // phase 0: the peer's q~ staging (below) has been read; then one phase per PV product
             // of the peer on this buffer (its X[g] is free again)
             tc::mbar_init(&bar->xempty[g], 1);
+            tc::mbar_init(&bar->yfree[g], 1);    // the peer has received our previous tile of group g
             for (int qq = 0; qq < 4; ++qq) tc::mbar_init(&bar->hand[qq][g], 1);
         }
         tc::mbar_init(&bar->o_done, 1);
@@ -371,36 +372,33 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             if (lane == 0) tc::mbar_arrive(&bar->s_empty[g]);  // the MMA may compute tile t+2 into this buffer
             // --- ship: Y[g] -> the peer's X[g]; the peer's half of this tile arrives in ours ---
             if (q == 0 && lane == 0) tc::mbar_arrive_expect_tx(&bar->xfull[g], X_BYTES);
-            // The peer's X[g] is free once the peer has read its q~ staging (first tile of the group)
-            // or its PV product of tile t-2 is done (which also means its copy of tile t-2 had landed,
-            // so our copy has finished reading Y[g]).
-            bool ok = true;
-            if (lane == 0) ok = tc::mbar_wait_cluster(&bar->xempty[g], ph, abort_flag, err, 32);
-            __syncwarp();
-            if (!__shfl_sync(FULL, ok, 0)) { done_ok = false; break; }
+            // Y[g] may be rewritten once the peer has received the group's previous tile from it (the
+            // copy has then finished reading it).
+            if (k > 0 && !__all_sync(FULL, tc::mbar_wait_cluster(&bar->yfree[g], (k - 1) & 1, abort_flag, err, 38))) {
+                done_ok = false;
+                break;
+            }
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 *(uint4 *)(Yg + roff + ((c ^ hsw) << 4)) = make_uint4(cur[4 * c], cur[4 * c + 1], cur[4 * c + 2], cur[4 * c + 3]);
             tc::fence_proxy_async_smem();  // the stores are read by the bulk copy (async proxy)
+            // The peer's X[g] is free once the peer has read its q~ staging (first tile of the group)
+            // or its PV product of tile t-2 is done.
+            bool ok = true;
+            if (lane == 0) ok = tc::mbar_wait_cluster(&bar->xempty[g], ph, abort_flag, err, 32);
             __syncwarp();
+            if (!__shfl_sync(FULL, ok, 0)) { done_ok = false; break; }
             if (lane == 0)
                 tc::bulk_copy_to_peer(tc::map_peer(tc::smem_u32(Xg) + wblk, peer), Yg + wblk, 32 * 128,
                                       tc::map_peer(tc::smem_u32(&bar->xfull[g]), peer));
-            // --- peer half + own half in fp32 (addition commutes: both CTAs get the same sum) ---
-            if (!__all_sync(FULL, tc::mbar_wait_cluster(&bar->xfull[g], ph, abort_flag, err, 33))) { done_ok = false; break; }
+            // --- own half in fp32 and the mask (entries that are padding, future or outside the sequence),
+            // while the peer's half is in flight ---
             float v[64];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 x = *(const uint4 *)(Xg + roff + ((c ^ hsw) << 4));
-                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t own = cur[4 * c + e];
-                    v[8 * c + 2 * e] = tc::add_f16_f32((uint16_t)(xs[e] & 0xffffu), tc::f16_to_f32((uint16_t)(own & 0xffffu)));
-                    v[8 * c + 2 * e + 1] = tc::add_f16_f32((uint16_t)(xs[e] >> 16), tc::f16_to_f32((uint16_t)(own >> 16)));
-                }
+            for (int j = 0; j < 32; ++j) {
+                v[2 * j] = tc::f16_to_f32((uint16_t)(cur[j] & 0xffffu));
+                v[2 * j + 1] = tc::f16_to_f32((uint16_t)(cur[j] >> 16));
             }
-            // --- mask: entries that are padding, future or outside the sequence ---
             const int st = t % NSTAGE;
             if (!__all_sync(FULL, tc::mbar_wait(&bar->kv_full[st], (t / NSTAGE) & 1, abort_flag, err, 34))) { done_ok = false; break; }
             {
@@ -419,10 +417,33 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                     }
                 }
             }
-            float mt = tc::max3(v[0], v[1], v[2]);
+            // --- + peer half, one rounding in fp32 (addition commutes: both CTAs get the same sum; a
+            // masked entry stays -inf) ---
+            if (!__all_sync(FULL, tc::mbar_wait_cluster(&bar->xfull[g], ph, abort_flag, err, 33))) { done_ok = false; break; }
+            // all four copies of the peer's half have landed: its Y[g] may be rewritten
+            if (q == 0 && lane == 0) tc::mbar_arrive_remote(tc::map_peer(tc::smem_u32(&bar->yfree[g]), peer));
 #pragma unroll
-            for (int j = 3; j < 63; j += 2) mt = tc::max3(mt, v[j], v[j + 1]);
-            mt = fmaxf(mt, v[63]);
+            for (int c = 0; c < 8; ++c) {
+                const uint4 x = *(const uint4 *)(Xg + roff + ((c ^ hsw) << 4));
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[8 * c + 2 * e] = tc::add_f16_f32((uint16_t)(xs[e] & 0xffffu), v[8 * c + 2 * e]);
+                    v[8 * c + 2 * e + 1] = tc::add_f16_f32((uint16_t)(xs[e] >> 16), v[8 * c + 2 * e + 1]);
+                }
+            }
+            // row maximum as a tree (depth 4)
+            float mt;
+            {
+                float a[22], b8[8];
+#pragma unroll
+                for (int i = 0; i < 21; ++i) a[i] = tc::max3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+                a[21] = v[63];
+#pragma unroll
+                for (int i = 0; i < 7; ++i) b8[i] = tc::max3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+                b8[7] = a[21];
+                mt = tc::max3(tc::max3(b8[0], b8[1], b8[2]), tc::max3(b8[3], b8[4], b8[5]), fmaxf(b8[6], b8[7]));
+            }
             // --- running maximum: the one used for tile t-1 comes from the other group ---
             float m_prev = -INFINITY;
             if (t > 0) {
