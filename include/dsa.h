@@ -153,7 +153,9 @@ int dsa_topk_select(const float *scores, int64_t ld_scores, const dsa_seqs *seqs
  *   W_UV     [H, d_c, d_v] (dtype): V[s,h,e] = sum_c c[s,c] W_UV[h,c,e]
  *   idx      [sum T, k] int32 key indices local to the row's sequence.  Entries
  *            outside 0 .. min(p, S_b-1) (e.g. the -1 padding) are masked.
- *            Each listed index counts once per occurrence.
+ *            Each listed index counts once per occurrence.  NULL selects the
+ *            dense causal pattern: entry e of every row is key e (so a row
+ *            attends to keys 0 .. min(k, p + 1, S_b) - 1).
  *   softmax_scale  multiplies q.k before the softmax (1/sqrt(d_n + d_r), or the
  *            YaRN-scaled 0.1352 of the released model)
  *   out      out [sum T, H, d_v] (dtype)
@@ -213,6 +215,12 @@ int dsa_sparse_mla_fwd_noalloc(const void *q_nope, const void *q_pe, int dtype, 
  * that the fp32 score buffer stays bounded; the workspace size covers one
  * chunk of scores, the selection (unless idx_out is given), the FP8 copies
  * of q^I / k^I (idx_fp8) and the attention scratch.
+ * When every row's causal prefix holds at most top_k keys (k >= S, the case
+ * the deepseek_v32 note on the nnterp page calls plain causal attention), the
+ * selection is every causal key and is known without scores: the quantiser,
+ * indexer and top-k are not launched, the attention reads the dense causal
+ * pattern, and idx_out (when given) is filled with 0 .. n-1 and -1 padding,
+ * exactly what the top-k writes for such rows.
  * ---------------------------------------------------------------------- */
 typedef struct dsa_problem {
     /* shapes */
@@ -292,6 +300,7 @@ int dsa_set_stage_events(void *const *events, int n_events);
 #define DSA_KERNEL_MLA_TC       (1u << 8)
 #define DSA_KERNEL_COMBINE      (1u << 9)
 #define DSA_KERNEL_SELFTEST     (1u << 10)
+#define DSA_KERNEL_DENSE_IDX    (1u << 11)
 
 #ifdef __cplusplus
 }

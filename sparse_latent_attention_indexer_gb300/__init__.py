@@ -154,14 +154,18 @@ def dsa_sparse_mla_workspace_size(dtype: int, H: int, d_n: int, d_r: int, d_c: i
 
 
 def dsa_sparse_mla_fwd(q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, idx, seqs: Seqs, softmax_scale: float, out=None,
-                       lse=None, workspace=None, want_lse=True, stream=None):
+                       lse=None, workspace=None, want_lse=True, stream=None, k=None):
     """kv_cache and k_pe are 2-D views [sum S, d_c] / [sum S, d_r] with contiguous rows
-    (k_pe may be a column slice of a packed cache)."""
+    (k_pe may be a column slice of a packed cache).  idx=None selects the dense causal
+    pattern (entry e of a row is key e) for k entries per row."""
     M, H, d_n = q_nope.shape
     d_r = q_pe.shape[2]
     d_c = W_UK.shape[2]
     d_v = W_UV.shape[2]
-    k = idx.shape[1]
+    if idx is not None:
+        k = idx.shape[1]
+    elif k is None:
+        raise ValueError("dsa_sparse_mla_fwd: idx=None needs k")
     dt = _dt(q_nope)
     dev = q_nope.device
     if out is None:

@@ -194,8 +194,8 @@ int validate_mla_call(const void *q_nope, const void *q_pe, int dtype, const voi
     if ((rc = check_mla_shape(dtype, H, d_n, d_r, d_c, d_v, k))) return rc;
     if (ld_kv < d_c || ld_pe < d_r) return DSA_ERR_INVALID_ARG;
     if (bt.total_q == 0) return DSA_OK;
-    if (!q_nope || (d_r > 0 && (!q_pe || !k_pe)) || !kv_cache || !W_UK || !W_UV || !idx || !out)
-        return DSA_ERR_INVALID_ARG;
+    // idx may be null: the dense causal selection (entry e of a row is key e)
+    if (!q_nope || (d_r > 0 && (!q_pe || !k_pe)) || !kv_cache || !W_UK || !W_UV || !out) return DSA_ERR_INVALID_ARG;
     return DSA_OK;
 }
 
@@ -401,6 +401,27 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
     char *ws = (char *)workspace;
     cudaError_t e;
     stage_mark(0, s);
+
+    // A row whose causal prefix holds at most top_k keys selects all of them, in ascending order.
+    // When every row of the batch does (the last row of each sequence is enough to check), the
+    // selection is known without scores: the quantiser, indexer and top-k do not run, the attention
+    // reads the dense causal pattern directly, and the index output is filled only if asked for.
+    bool all_dense = true;
+    for (int b = 0; b < bt.st.B && all_dense; ++b) {
+        const int Tb = bt.st.q_off[b + 1] - bt.st.q_off[b];
+        if (Tb > 0 && std::min(bt.st.start_pos[b] + Tb, bt.st.k_len[b]) > p->top_k) all_dense = false;
+    }
+    if (all_dense) {
+        stage_mark(1, s);
+        if (p->idx_out) {
+            e = launch_dense_idx(bt.st, bt.total_q, p->top_k, p->idx_out, s);
+            if (e != cudaSuccess) return fail_cuda(e);
+        }
+        stage_mark(2, s);
+        return run_mla(p->q_nope, p->q_pe, p->dtype, p->kv_cache, p->ld_kv, p->k_pe, p->ld_pe, p->W_UK, p->W_UV,
+                       p->H, p->d_n, p->d_r, p->d_c, p->d_v, nullptr, p->top_k, bt, p->softmax_scale, p->out, p->lse,
+                       ws + L.mla, s, true, true);
+    }
 
     const void *q_idx = p->q_idx, *k_idx = p->k_idx;
     const float *q_scale = nullptr, *k_scale = nullptr;

@@ -143,6 +143,7 @@ int indexer_tc_read_error(int *site);
 // CUDA-core kernels (used by the tests to cross-check the tensor-core ones).
 bool force_generic();
 
+cudaError_t launch_dense_idx(const SeqTab &st, int total_q, int k, int32_t *idx, cudaStream_t s);
 cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int total_q, int k, int32_t *idx,
                         cudaStream_t s);
 

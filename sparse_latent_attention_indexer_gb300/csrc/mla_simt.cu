@@ -114,12 +114,12 @@ __global__ void __launch_bounds__(HG * 32) mla_simt_kernel(const TQ *__restrict_
 #pragma unroll
     for (int i = 0; i < MAX_PER_LANE; ++i) o[i] = 0.0f;
     float m = -INFINITY, l = 0.0f;
-    const int32_t *row_idx = idx + (int64_t)r * k;
+    const int32_t *row_idx = idx ? idx + (int64_t)r * k : nullptr;  // none: entry j is key j (dense causal)
     for (int j0 = 0; j0 < k; j0 += KC) {
         __syncthreads();
         if (threadIdx.x < KC) {
             const int j = j0 + threadIdx.x;
-            int s = j < k ? row_idx[j] : -1;
+            int s = j < k ? (row_idx ? row_idx[j] : j) : -1;
             if (s < 0 || s >= ri.S || s > ri.p) s = -1;
             keys[threadIdx.x] = s;
         }

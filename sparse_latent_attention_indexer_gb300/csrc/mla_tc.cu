@@ -200,7 +200,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         // moves four full segments; the 128-byte swizzle of the MMA operand
         // layout is applied to the 16-byte chunk index.
         const int pw = warp == 0 ? 0 : (warp == 3 ? 1 : warp - 10), c = lane & 7, jr = pw * 4 + (lane >> 3);
-        const int32_t *row_idx = idx + (int64_t)r * P.k;
+        // no selection array: the dense causal pattern, entry e is key e
+        const int32_t *row_idx = idx ? idx + (int64_t)r * P.k : nullptr;
         const int last = min(p, S - 1);
         const uint32_t kv_s = tc::smem_u32(KV);
         constexpr int PASSES = BK / (NPROD * 4);
@@ -209,7 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
 #pragma unroll
             for (int ps = 0; ps < PASSES; ++ps) {
                 const int e = e0 + i * BK + ps * NPROD * 4 + jr;
-                const int sidx = e < e1 ? __ldg(row_idx + e) : -1;
+                const int sidx = e < e1 ? (row_idx ? __ldg(row_idx + e) : e) : -1;
                 rows[ps] = (sidx >= 0 && sidx <= last) ? sidx : -1;
             }
         };

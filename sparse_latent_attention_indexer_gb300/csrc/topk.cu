@@ -633,7 +633,26 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(CT)
     }
 }
 
+// The selection of rows that see at most k keys, written without scores: every causal key in
+// ascending order, then -1 (what the top-k writes for such rows).  One CTA per row.
+__global__ void __launch_bounds__(256) dense_idx_kernel(SeqTab st, int k, int32_t *__restrict__ idx) {
+    pdl_wait();
+    const int r = blockIdx.x;
+    const RowInfo ri = row_info(st, r);
+    const int n_live = min(ri.p + 1, ri.S);
+    int32_t *out = idx + (int64_t)r * k;
+    for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < n_live ? j : -1;
+}
+
 }  // namespace
+
+cudaError_t launch_dense_idx(const SeqTab &st, int total_q, int k, int32_t *idx, cudaStream_t s) {
+    if (total_q == 0) return cudaSuccess;
+    cudaError_t e = launch_pdl(dense_idx_kernel, dim3(total_q), dim3(256), 0, s, st, k, idx);
+    if (e != cudaSuccess) return e;
+    note_launch(DSA_KERNEL_DENSE_IDX);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_topk(const float *scores, int64_t ld, const SeqTab &st, int total_q, int k, int32_t *idx,
                         cudaStream_t s) {

@@ -280,6 +280,60 @@ def test_forward_dense_when_k_covers_the_sequence():
     assert np.abs(out.float().cpu().numpy()[rows] - ref).max() <= H.OUT_ATOL_BF16
 
 
+INDEXER_AND_TOPK = {"quant", "indexer_simt", "indexer_tc", "indexer_fp8", "topk"}
+
+
+@pytest.mark.parametrize("shape", ["bf16", "fp8", "f32"])
+def test_forward_dense_batch_launches_no_indexer_or_topk(shape):
+    """Every row of the batch sees at most k keys (k >= S; the second sequence
+    continues at position 100 with 37 rows): the selection is every causal key,
+    known without scores, so no quantiser, indexer or top-k kernel runs.  The
+    index output is the dense pattern the top-k writes for such rows, and the
+    outputs match the oracle's whole path on sampled rows."""
+    sh = {"bf16": di.Shape(k=512), "fp8": di.Shape(k=512, idx_fp8=True),
+          "f32": di.workload(0).shape}[shape]
+    if shape == "f32":
+        wl = di.generate("dense-f32", sh, 16, [40, 9], [40, 70], [0, 55])   # k = 64 covers p + 1 <= 64
+    else:
+        wl = di.generate("dense-" + shape, sh, 15, [200, 37], [200, 300], [0, 100])
+    t = H.to_device(wl)
+    out, lse, idx = H.gpu_forward(wl, t)
+    kernels = dsa.last_kernels()
+    assert not kernels & INDEXER_AND_TOPK, kernels
+    assert "dense_idx" in kernels, kernels
+    idx = idx.cpu().numpy()
+    for b in range(wl.B):
+        for tt in range(wl.T[b]):
+            r, p = wl.cu_q[b] + tt, wl.start_pos[b] + tt
+            n = min(p + 1, wl.S[b])
+            want = np.full(sh.k, -1, np.int32)
+            want[:n] = np.arange(n)
+            assert np.array_equal(idx[r], want), (b, tt)
+    rows = [0, 1, wl.cu_q[1] - 1, wl.cu_q[1], wl.cu_q[2] - 1]
+    ref = H.oracle_rows(wl, rows)
+    out = out.float().cpu().numpy()
+    err = max(np.abs(out[r] - o["out"]).max() for r, o in ref.items())
+    assert err <= out_atol(wl), f"max abs err {err:.3e}"
+
+
+@pytest.mark.parametrize("name", ["bf16-ragged", "f32-tiny"])
+def test_sparse_mla_null_selection_is_the_dense_causal_one(name):
+    """idx = NULL means entry e of a row is key e: bit-identical to passing the
+    explicit selection 0 .. min(k, p+1, S)-1 followed by -1 padding."""
+    wl, t = case(name)
+    sh = wl.shape
+    explicit = np.full((wl.cu_q[-1], sh.k), -1, np.int32)
+    for b in range(wl.B):
+        for tt in range(wl.T[b]):
+            n = min(sh.k, wl.start_pos[b] + tt + 1, wl.S[b])
+            explicit[wl.cu_q[b] + tt, :n] = np.arange(n)
+    args = (t["q_nope"], t["q_pe"], t["ckv"], t["kpe"], t["W_UK"], t["W_UV"])
+    o1, l1 = dsa.dsa_sparse_mla_fwd(*args, torch.from_numpy(explicit).cuda(), H.seqs_of(wl), sh.softmax_scale)
+    o2, l2 = dsa.dsa_sparse_mla_fwd(*args, None, H.seqs_of(wl), sh.softmax_scale, k=sh.k)
+    assert torch.equal(o1, o2)
+    assert torch.equal(l1, l2)
+
+
 def test_forward_yarn_scale_and_empty_sequence():
     """The released model's YaRN-scaled softmax scale 0.1352, and a batch
     holding an empty sequence (T = 0) between two others."""
