@@ -332,8 +332,12 @@ int dsa_sparse_mla_fwd(const void *q_nope, const void *q_pe, int dtype, const vo
 namespace dsa {
 namespace {
 
-// Bound on the fp32 score buffer of one chunk of query rows.
-constexpr size_t SCORE_CHUNK_BYTES = size_t(256) << 20;
+// Bound on the fp32 score buffer of one chunk of query rows.  Larger chunks give the indexer and
+// the top-k more rows per launch (more query groups, so the indexer leaves the split-table mode and
+// balances better); on GB300 the long prefills ran faster up to the largest size measured: 32768
+// rows of 32768 keys spent 8.5 / 7.6 / 7.5 ms in indexer + top-k with 256 MB / 512 MB / 1 GB
+// chunks, and the chunked FP8 prefill 29.8 / 25.5 / 24.9 ms.  1 GB of a GB300's HBM is small.
+constexpr size_t SCORE_CHUNK_BYTES = size_t(1024) << 20;
 
 struct FwdWs {
     int64_t ld = 0;
