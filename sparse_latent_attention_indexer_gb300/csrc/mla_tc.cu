@@ -109,7 +109,7 @@ __device__ __forceinline__ int find_seq(const MlaParams &P, int r) {
 // quarter q to the other group.
 struct Bars {
     uint64_t q_stage, q_ready, kv_full[NSTAGE], kv_empty[NSTAGE], s_full[2], s_empty[2], p_full[2], p_empty[2],
-        xfull[2], xempty[2], yfree[2], hand[4][2], o_done;
+        xfull[2], xempty[2], yfree[2], hand[4][2], qk_done, o_done;
 };
 static_assert(sizeof(Bars) + 8 <= 320, "barrier area");
 
@@ -171,6 +171,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             tc::mbar_init(&bar->yfree[g], 1);    // the peer has received our previous tile of group g
             for (int qq = 0; qq < 4; ++qq) tc::mbar_init(&bar->hand[qq][g], 1);
         }
+        tc::mbar_init(&bar->qk_done, 1);
         tc::mbar_init(&bar->o_done, 1);
         *abort_flag = 0;
         never = 0;
@@ -270,8 +271,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             }
             tc::mma_commit(&bar->s_full[j & 1]);
         }
-        // Every score tile issued here is read by a softmax group before its PV product exists, so
-        // these MMAs have completed before the context is final.
+        // No MMA of this thread may still be running when the tensor memory is released (after an
+        // abort the loop can stop with score tiles in flight).
+        tc::mma_commit(&bar->qk_done);
+        tc::mbar_wait(&bar->qk_done, 0, nv, err, 39);
     } else if (warp == 2 && lane == 0 && n > 0) {
         // ---------------- PV issuer ----------------
         // PV(j) once P(j) is written; its completion frees the key stage, this CTA's X buffer (the
