@@ -53,6 +53,10 @@ def _bind(lib):
     lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_value.restype = D
     lib.oracle_num_threads.restype = I
+    lib.oracle_linear.argtypes = [P, P, I64, I64, I64, P]
+    lib.oracle_rmsnorm.argtypes = [P, I64, I64, P, D, P]
+    lib.oracle_layernorm.argtypes = [P, I64, I64, P, P, D, P]
+    lib.oracle_rope_deinterleave.argtypes = [P, I64, I64, P, P, P]
     return lib
 
 
@@ -223,3 +227,65 @@ def dsa_rows(qI, w, kI, q_nope, q_pe, ckv, kpe, W_UK, W_UV, pos, k: int, scale: 
         KC, V = kv_up(ckv, W_UK, W_UV)
     out, lse = sparse_mla_unabsorbed(q_nope, q_pe, KC, kpe, V, idx, pos, scale)
     return dict(scores=scores, absterm=absterm, idx=idx, out=out, lse=lse)
+
+
+# ---------------------------------------------------------------------------
+# The projections on either side of the path (oracle.c section 8)
+# ---------------------------------------------------------------------------
+def linear(x, W):
+    """y = x W^T for x [n, D] and W [N, D] (nn.Linear without bias), in float64."""
+    x, W = _f32(x), _f32(W)
+    n, D = x.shape
+    N = W.shape[0]
+    assert W.shape[1] == D
+    y = np.empty((n, N), np.float64)
+    _load().oracle_linear(_p(x), _p(W), n, D, N, _p(y))
+    return y
+
+
+def rmsnorm(x, gain, eps: float = 1e-6):
+    x, gain = _f64(x), _f32(gain)
+    n, d = x.shape
+    y = np.empty((n, d), np.float64)
+    _load().oracle_rmsnorm(_p(x), n, d, _p(gain), float(eps), _p(y))
+    return y
+
+
+def layernorm(x, gain, bias, eps: float = 1e-6):
+    x, gain, bias = _f64(x), _f32(gain), _f32(bias)
+    n, d = x.shape
+    y = np.empty((n, d), np.float64)
+    _load().oracle_layernorm(_p(x), n, d, _p(gain), _p(bias), float(eps), _p(y))
+    return y
+
+
+def rope_deinterleave(x, cos_t, sin_t):
+    """x [n, 2*half] float64; cos_t, sin_t [n, half] (each row's angles)."""
+    x, cos_t, sin_t = _f64(x), _f32(cos_t), _f32(sin_t)
+    n, d = x.shape
+    half = d // 2
+    assert cos_t.shape == (n, half) and sin_t.shape == (n, half)
+    y = np.empty((n, d), np.float64)
+    _load().oracle_rope_deinterleave(_p(x), n, half, _p(cos_t), _p(sin_t), _p(y))
+    return y
+
+
+def kv_prologue(x, W_proj, kv_gain, k_gain, k_bias, cos_t, sin_t, d_c: int = 512, d_r: int = 64,
+                D_I: int = 128, H_I: int = 64, eps: float = 1e-6):
+    """The step before the path for rows x [n, dim], in the pages' order.
+    W_proj stacks the three projections that read x: rows 0 .. d_c+d_r-1 are
+    wkv_a, the next D_I rows wk, the last H_I rows weights_proj.  Returns
+    dict(latent [n, d_c], k_pe [n, d_r], kI [n, D_I], w [n, H_I]) in float64."""
+    y = linear(x, W_proj)
+    kv, k_pe = y[:, :d_c], y[:, d_c:d_c + d_r]
+    kI = y[:, d_c + d_r:d_c + d_r + D_I]
+    w = y[:, d_c + d_r + D_I:d_c + d_r + D_I + H_I]
+    return dict(latent=rmsnorm(kv, kv_gain, eps), k_pe=rope_deinterleave(k_pe, cos_t, sin_t),
+                kI=layernorm(kI, k_gain, k_bias, eps), w=np.array(w))
+
+
+def output_proj(out, wo):
+    """y = out wo^T for the attention output out [n, H, d_v] (heads side by
+    side, [n, H * d_v]) and wo [dim, H * d_v]."""
+    out = np.asarray(out)
+    return linear(out.reshape(out.shape[0], -1), wo)

@@ -433,6 +433,86 @@ ORACLE_API void oracle_quant_e4m3_ue8m0(const float *x, int64_t n_blocks, uint8_
     }
 }
 
+/* ------------------------------------------------------------------------
+ * 8. The projections on either side of the path.
+ *
+ *    Before it [P5 mla-init and mla-kv excerpts; P4 RMSNorm excerpt; P1
+ *    printout of DeepseekV32Attention and its indexer]:
+ *        kv      = wkv_a(x)                      (dim -> kv_lora_rank + rope)
+ *        kv, k_pe = split(kv, [kv_lora_rank, qk_rope_head_dim])
+ *        kv      = kv_norm(kv)                   (RMSNorm, gain, eps 1e-6, float32 compute)
+ *        k_pe    = rotary(k_pe, freqs_cis)       (served de-interleaved)
+ *        k^I     = k_norm(wk(x))                 (LayerNorm(128), gain and bias, eps 1e-6)
+ *        w       = weights_proj(x)               (dim -> 64 per-head weights)
+ *    After it [P5 mla-init excerpt: wo maps n_heads * v_head_dim -> dim]:
+ *        y       = wo(out)                       (out [T, H * d_v] of the attention)
+ *
+ *    Every Linear here has no bias: y = x W^T with W stored [out, in].
+ *    The linear outputs go into the norms and the rotary step unrounded.
+ * ---------------------------------------------------------------------- */
+
+/* y[n, N] = x[n, D] . W[N, D]^T */
+ORACLE_API void oracle_linear(const float *x, const float *W, int64_t n, int64_t D, int64_t N, double *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t o = 0; o < N; ++o) {
+            double sum = 0.0;
+            for (int64_t i = 0; i < D; ++i) sum += (double)x[r * D + i] * (double)W[o * D + i];
+            y[r * N + o] = sum;
+        }
+}
+
+/* RMSNorm of rows of d values [P4 RMSNorm excerpt]: y = gain * x / sqrt(mean(x^2) + eps). */
+ORACLE_API void oracle_rmsnorm(const double *x, int64_t n, int64_t d, const float *gain, double eps, double *y)
+{
+    for (int64_t r = 0; r < n; ++r) {
+        double ms = 0.0;
+        for (int64_t i = 0; i < d; ++i) ms += x[r * d + i] * x[r * d + i];
+        ms /= (double)d;
+        const double inv = 1.0 / sqrt(ms + eps);
+        for (int64_t i = 0; i < d; ++i) y[r * d + i] = (double)gain[i] * (x[r * d + i] * inv);
+    }
+}
+
+/* LayerNorm of rows of d values with gain and bias [P1 printout: k_norm
+ * LayerNorm((128,), eps=1e-06, elementwise_affine=True, bias=True)]:
+ * y = (x - mean) / sqrt(var + eps) * gain + bias, var = mean of (x - mean)^2. */
+ORACLE_API void oracle_layernorm(const double *x, int64_t n, int64_t d, const float *gain, const float *bias,
+                                 double eps, double *y)
+{
+    for (int64_t r = 0; r < n; ++r) {
+        double mean = 0.0;
+        for (int64_t i = 0; i < d; ++i) mean += x[r * d + i];
+        mean /= (double)d;
+        double var = 0.0;
+        for (int64_t i = 0; i < d; ++i) var += (x[r * d + i] - mean) * (x[r * d + i] - mean);
+        var /= (double)d;
+        const double inv = 1.0 / sqrt(var + eps);
+        for (int64_t i = 0; i < d; ++i)
+            y[r * d + i] = (x[r * d + i] - mean) * inv * (double)gain[i] + (double)bias[i];
+    }
+}
+
+/* Rotary embedding of rows of 2*half values [P5 mla-kv excerpt,
+ * apply_rotary_emb with freqs_cis; P1 "The rotary part is served
+ * de-interleaved": pair (2i, 2i+1) is turned by the angle of frequency i and
+ * lands in dimensions i and half + i]:
+ *     y[i]        = x[2i] cos_i - x[2i+1] sin_i
+ *     y[half + i] = x[2i] sin_i + x[2i+1] cos_i
+ * cos_t, sin_t: [n, half], the row's position already applied. */
+ORACLE_API void oracle_rope_deinterleave(const double *x, int64_t n, int64_t half, const float *cos_t,
+                                         const float *sin_t, double *y)
+{
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t i = 0; i < half; ++i) {
+            const double a = x[r * 2 * half + 2 * i], b = x[r * 2 * half + 2 * i + 1];
+            const double c = (double)cos_t[r * half + i], s = (double)sin_t[r * half + i];
+            y[r * 2 * half + i] = a * c - b * s;
+            y[r * 2 * half + half + i] = a * s + b * c;
+        }
+}
+
 /* Number of OpenMP threads this library runs with (reported by the bench). */
 ORACLE_API int oracle_num_threads(void)
 {

@@ -50,6 +50,15 @@ MUTANTS = [
     ("ue8m0 scale one step high", "while (e < 127 && amax > 448.0 * ldexp(1.0, e)) ++e;",
      "while (e < 127 && amax >= 448.0 * ldexp(1.0, e)) ++e;", 0),
     ("ue8m0 no clamp", "e = -127;", "e = -160;", 0),
+    ("linear transposes W", "(double)W[o * D + i]", "(double)W[i * N + o]", 0),
+    ("rmsnorm drops the mean", "ms /= (double)d;", "ms /= 1.0;", 0),
+    ("rmsnorm drops the gain", "y[r * d + i] = (double)gain[i] * (x[r * d + i] * inv);",
+     "y[r * d + i] = x[r * d + i] * inv;", 0),
+    ("layernorm unbiased variance", "var /= (double)d;", "var /= (double)(d - 1);", 0),
+    ("layernorm drops the bias", "* (double)gain[i] + (double)bias[i];", "* (double)gain[i];", 0),
+    ("rotary sign", "y[r * 2 * half + i] = a * c - b * s;", "y[r * 2 * half + i] = a * c + b * s;", 0),
+    ("rotary interleaved output", "y[r * 2 * half + half + i] = a * s + b * c;",
+     "y[r * 2 * half + 2 * i + 1] = a * s + b * c;", 0),
 ]
 
 

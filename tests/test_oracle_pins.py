@@ -398,3 +398,117 @@ def test_ue8m0_scale_rules():
                 assert abs(deq[b, i] - x[b, i]) <= 2.0 ** (math.floor(math.log2(abs(v))) - 4) * e * (1 + 1e-12)
             else:
                 assert abs(deq[b, i] - x[b, i]) <= 2.0 ** -10 * e * (1 + 1e-12)
+
+
+# ---------------------------------------------------------------------------
+# The projections on either side of the path (the step before: wkv_a, kv_norm,
+# rotary k_pe, wk + k_norm, weights_proj; the step after: wo)
+# ---------------------------------------------------------------------------
+def test_linear_is_the_matmul_with_the_weight_stored_out_by_in():
+    """nn.Linear without bias: y = x W^T, W stored [out, in] (the printout's
+    Linear(in_features, out_features)); a plain float64 matmul."""
+    g = np.random.default_rng(11)
+    x = g.standard_normal((7, 33)).astype(np.float32)
+    W = g.standard_normal((5, 33)).astype(np.float32)
+    ref = x.astype(np.float64) @ W.astype(np.float64).T
+    assert np.allclose(oracle.linear(x, W), ref, rtol=1e-13, atol=1e-12)
+    # an identity weight copies its inputs; a one-hot row picks one input
+    assert np.array_equal(oracle.linear(x, np.eye(33, dtype=np.float32)), x.astype(np.float64))
+    e = np.zeros((1, 33), np.float32)
+    e[0, 4] = 1.0
+    assert np.array_equal(oracle.linear(x, e)[:, 0], x[:, 4].astype(np.float64))
+
+
+def test_rmsnorm_matches_the_library_and_its_closed_form():
+    g = np.random.default_rng(12)
+    x = g.standard_normal((6, 512)) * 3.0
+    gain = g.uniform(0.5, 1.5, 512).astype(np.float32)
+    ref = torch.nn.functional.rms_norm(torch.tensor(x), (512,), torch.tensor(gain, dtype=torch.float64), eps=1e-6)
+    assert np.allclose(oracle.rmsnorm(x, gain), ref.numpy(), rtol=1e-12, atol=1e-12)
+    # a constant row c: y = gain * c / sqrt(c^2 + eps)
+    c = 0.25
+    y = oracle.rmsnorm(np.full((1, 512), c), np.ones(512, np.float32))
+    assert np.allclose(y, c / math.sqrt(c * c + 1e-6), rtol=1e-14)
+    # unit gain: the mean square of the output is ms / (ms + eps)
+    y = oracle.rmsnorm(x, np.ones(512, np.float32))
+    ms = (x ** 2).mean(-1)
+    assert np.allclose((y ** 2).mean(-1), ms / (ms + 1e-6), rtol=1e-12)
+
+
+def test_layernorm_matches_the_library_and_its_closed_form():
+    g = np.random.default_rng(13)
+    x = g.standard_normal((6, 128)) * 2.0 + 0.7
+    gain = g.uniform(0.5, 1.5, 128).astype(np.float32)
+    bias = g.standard_normal(128).astype(np.float32)
+    ref = torch.nn.functional.layer_norm(torch.tensor(x), (128,), torch.tensor(gain, dtype=torch.float64),
+                                         torch.tensor(bias, dtype=torch.float64), eps=1e-6)
+    assert np.allclose(oracle.layernorm(x, gain, bias), ref.numpy(), rtol=1e-12, atol=1e-12)
+    # x = a + b * (+1, -1, +1, ...): mean a, variance b^2, so y = +-b / sqrt(b^2 + eps) * gain + bias
+    a, b = 3.0, 0.5
+    sgn = np.tile([1.0, -1.0], 64)
+    y = oracle.layernorm((a + b * sgn)[None, :], gain, bias)[0]
+    want = sgn * b / math.sqrt(b * b + 1e-6) * gain.astype(np.float64) + bias.astype(np.float64)
+    assert np.allclose(y, want, rtol=1e-13, atol=1e-13)
+
+
+def test_rotary_is_served_de_interleaved():
+    """The nnterp deepseek_v32 note: at position 0, where the rotary step is the
+    identity, the served rotary part is the projection's even dimensions
+    followed by its odd ones; at any angle, pair (2i, 2i+1) is turned as the
+    complex number x[2i] + i x[2i+1] times e^{i theta_i} into dims i, 32 + i."""
+    g = np.random.default_rng(14)
+    x = g.standard_normal((5, 64))
+    ones, zeros = np.ones((5, 32), np.float32), np.zeros((5, 32), np.float32)
+    y0 = oracle.rope_deinterleave(x, ones, zeros)
+    assert np.array_equal(y0, np.concatenate([x[:, 0::2], x[:, 1::2]], axis=1))
+    theta = g.uniform(-math.pi, math.pi, (5, 32))
+    c, s = np.cos(theta).astype(np.float32), np.sin(theta).astype(np.float32)
+    y = oracle.rope_deinterleave(x, c, s)
+    z = (x[:, 0::2] + 1j * x[:, 1::2]) * (c.astype(np.float64) + 1j * s.astype(np.float64))
+    assert np.allclose(y[:, :32], z.real, rtol=1e-14, atol=1e-14)
+    assert np.allclose(y[:, 32:], z.imag, rtol=1e-14, atol=1e-14)
+    # turning back by -theta restores the pairs
+    back = oracle.rope_deinterleave(np.stack([y[:, :32], y[:, 32:]], axis=2).reshape(5, 64), c, -s)
+    assert np.allclose(back, y0, rtol=1e-6, atol=1e-6)
+
+
+def test_kv_prologue_split_and_scale_invariance():
+    """The step before the path, composed in the pages' order: the first 512
+    outputs of wkv_a are normalised (RMSNorm: invariant to a positive scale of
+    x up to eps), the next 64 rotated (linear in x), wk's 128 outputs
+    layer-normalised (invariant to scale and shift of the outputs), and the 64
+    head weights are weights_proj(x) as they come."""
+    g = np.random.default_rng(15)
+    dim = 96
+    x = g.standard_normal((4, dim)).astype(np.float32)
+    W = (g.standard_normal((512 + 64 + 128 + 64, dim)) / math.sqrt(dim)).astype(np.float32)
+    kvg = g.uniform(0.5, 1.5, 512).astype(np.float32)
+    kg = g.uniform(0.5, 1.5, 128).astype(np.float32)
+    kb = g.standard_normal(128).astype(np.float32)
+    th = g.uniform(-3, 3, (4, 32))
+    c, s = np.cos(th).astype(np.float32), np.sin(th).astype(np.float32)
+    r = oracle.kv_prologue(x, W, kvg, kg, kb, c, s)
+    lin = x.astype(np.float64) @ W.astype(np.float64).T
+    assert np.allclose(r["w"], lin[:, 704:768], rtol=1e-12, atol=1e-12)
+    # the rotated key keeps each pair's length
+    assert np.allclose(r["k_pe"][:, :32] ** 2 + r["k_pe"][:, 32:] ** 2, lin[:, 512:576:2] ** 2 + lin[:, 513:576:2] ** 2,
+                       rtol=1e-6)  # cos^2 + sin^2 = 1 to float32 precision
+    r2 = oracle.kv_prologue(x * 4.0, W, kvg, kg, kb, c, s)
+    assert np.allclose(r2["latent"], r["latent"], rtol=1e-5)
+    assert np.allclose(r2["kI"], r["kI"], rtol=1e-5, atol=1e-5)
+    assert np.allclose(r2["k_pe"], 4.0 * r["k_pe"], rtol=1e-12, atol=1e-12)
+    assert np.allclose(r2["w"], 4.0 * r["w"], rtol=1e-12, atol=1e-12)
+    # the latent rows have mean square ~ gain^2 weighted; with unit gain it is ~1
+    r3 = oracle.kv_prologue(x, W, np.ones(512, np.float32), kg, kb, c, s)
+    assert np.allclose((r3["latent"] ** 2).mean(-1), 1.0, atol=1e-4)
+
+
+def test_output_projection_of_the_heads_side_by_side():
+    """wo reads the attention output with the heads side by side
+    ([n, H * d_v], the printout's attention_premix): y = sum_h out_h wo_h^T."""
+    g = np.random.default_rng(16)
+    out = g.standard_normal((3, 4, 8)).astype(np.float32)
+    wo = g.standard_normal((6, 32)).astype(np.float32)
+    y = oracle.output_proj(out, wo)
+    per_head = sum(out[:, h, :].astype(np.float64) @ wo[:, h * 8:(h + 1) * 8].astype(np.float64).T for h in range(4))
+    assert np.allclose(y, per_head, rtol=1e-12, atol=1e-12)
