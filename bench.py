@@ -1,6 +1,12 @@
 #!/usr/bin/env python
-"""Benchmark of the DSA hot path on GB300: DSA prefill tokens/s at T = S = 4096
-(671B head shapes, bf16, top-2048), one JSON line on rank 0.
+"""Benchmark of the DSA hot path on GB300, one JSON line on rank 0.
+
+Headline: DSA prefill tokens/s on the largest single-GPU prefill workload,
+the chunked prefill with the FP8 indexer (8 sequences x 8192 new queries on
+caches of 16K-65K keys, 671B head shapes, top-2048).  The same line carries
+``decode`` (64 sequences x 1 query on caches of 8K-64K keys: decode
+queries/s) and ``prefill_4k`` (T = S = 4096, bf16), each with its own stage
+times, roofline, kernel timings and end-to-end figure.
 
 A step is one dsa_forward call (FP8 quantisation when configured, indexer,
 top-k, q~ = q_nope W_UK, sparse latent attention, o_lat W_UV) over the whole
@@ -10,7 +16,7 @@ plain CPU oracle instead (a bounded sample of rows per step).
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (the
 path shards by query rows / sequences with no exchange): weak scaling, value =
-tokens of all ranks / the slowest rank's time.
+queries of all ranks / the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -32,16 +38,29 @@ CONFIG_NAMES = {0: "tiny-fp32-T256", 1: "prefill-bf16-T4096-S4096-top2048", 2: "
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+UNITS = {0: "tokens/s", 1: "tokens/s", 2: "tokens/s", 3: "queries/s", 4: "tokens/s"}
+EXTRA_KEYS = {3: "decode", 1: "prefill_4k", 2: "prefill_32k", 0: "tiny", 4: "chunked_prefill"}
+# rows of the oracle's bounded sample: about 10 s on 16 host cores for the cpu_baseline leg, and a
+# few seconds per step for the reference arm
+CPU_ROWS = {0: 256, 1: 1024, 2: 320, 3: 64, 4: 384}
+REF_ROWS = {0: 256, 1: 256, 2: 96, 3: 32, 4: 128}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1, help="workload 0..4 (1 = the headline prefill)")
-    ap.add_argument("--cpu-rows", type=int, default=1024, help="rows of the oracle's bounded sample")
+    ap.add_argument("--config", type=int, default=4,
+                    help="headline workload 0..4 (4 = the chunked prefill with the FP8 indexer)")
+    ap.add_argument("--extra", default="3,1",
+                    help="comma-separated workloads measured in the same run (default: decode, 4K prefill)")
+    ap.add_argument("--cpu-rows", type=int, default=None, help="rows of the oracle's bounded sample")
+    ap.add_argument("--ref-rows", type=int, default=None, help="rows per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the steps around the path and the FP8 latent cache")
     return ap.parse_args()
 
 
@@ -232,40 +251,133 @@ def barrier(world):
 
 def run_reference(args, world, rank):
     """The oracle on the host cores: each step a bounded sample of rows of the
-    same workload; throughput in the same unit (tokens/s)."""
+    headline workload; throughput in the same unit (tokens/s)."""
     if rank != 0:
         return
     import dsa_inputs as di
     wl = di.workload(args.config)
+    n_rows = args.ref_rows if args.ref_rows is not None else REF_ROWS[args.config]
     for _ in range(args.warmup):
-        oracle_sample(wl, max(1, args.cpu_rows // 8))
+        oracle_sample(wl, max(1, n_rows // 8))
     secs, rows, threads = 0.0, 0, 1
     for _ in range(args.steps):
-        s, n, threads = oracle_sample(wl, args.cpu_rows)
+        s, n, threads = oracle_sample(wl, n_rows)
         secs += s
         rows += n
     value = rows / secs
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+    unit = UNITS[args.config]
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": CONFIG_NAMES[args.config], "sample_rows_per_step": args.cpu_rows},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{args.cpu_rows} fixed query rows per step of the {CONFIG_NAMES[args.config]} "
+            "config": {"workload": CONFIG_NAMES[args.config], "sample_rows_per_step": n_rows},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                             "sample": f"{n_rows} fixed query rows per step of the {CONFIG_NAMES[args.config]} "
                                        "workload, each row doing its full indexer, top-k and attention work"},
-            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, world, rank, local):
+def sub_batch(wl, r0, r1):
+    """Rows [r0, r1) of a batch as their own batch: (seqs arrays, first sequence,
+    last sequence + 1), the sequences keeping their whole key caches."""
+    cu_q = wl.cu_q
+    bs = [b for b in range(wl.B) if cu_q[b] < r1 and cu_q[b + 1] > r0]
+    sub_q, sub_k, sub_p = [0], [0], []
+    for b in bs:
+        lo, hi = max(cu_q[b], r0), min(cu_q[b + 1], r1)
+        sub_q.append(sub_q[-1] + hi - lo)
+        sub_k.append(sub_k[-1] + wl.S[b])
+        sub_p.append(wl.start_pos[b] + lo - cu_q[b])
+    return (sub_q, sub_k, sub_p), bs[0], bs[-1] + 1
+
+
+def score_chunks(wl):
+    """Row ranges of the forward's indexer launches (fp32 scores bounded at 1 GiB per chunk)."""
+    ld = (max(max(wl.S), 1) + 3) // 4 * 4
+    per = max(1, min(wl.total_q, (1 << 30) // (ld * 4)))
+    return [(r0, min(wl.total_q, r0 + per)) for r0 in range(0, wl.total_q, per)]
+
+
+def indexer_pairs_computed(wl, skip_dense=True):
+    """(query, key) pairs the tensor-core indexer multiplies: for every group of
+    4 consecutive queries of a sequence, every 128-key block up to the last
+    query's position, for each query of the group; the forward skips groups
+    whose queries all see at most k keys."""
+    k = wl.shape.k
+    total = 0
+    for b in range(wl.B):
+        T = wl.T[b]
+        for t0 in range(0, T, 4):
+            ntok = min(4, T - t0)
+            last = wl.start_pos[b] + t0 + ntok - 1
+            if skip_dense and last < k:
+                continue
+            total += (last // 128 + 1) * 128 * ntok
+    return total
+
+
+def stage_work(wl):
+    """Algorithmic flops and compulsory HBM bytes of each stage of one step."""
+    sh = wl.shape
+    M = wl.total_q
+    pairs_sel, pairs_causal = wl.selected_pairs(), wl.causal_pairs()
+    elt = 4 if sh.dtype == "f32" else 2
+    ki_elt = 1 if sh.idx_fp8 else elt
+    # rows that need scores (the others select every causal key without them)
+    scored = sum(1 for b in range(wl.B) for p in wl.row_positions(b) if p + 1 > sh.k)
+    scored_pairs = sum(p + 1 for b in range(wl.B) for p in wl.row_positions(b) if p + 1 > sh.k)
+    flops = {
+        "indexer+topk": 2.0 * sh.H_I * sh.D_I * pairs_causal,
+        "absorb_q": 2.0 * M * sh.H * sh.d_n * sh.d_c,
+        "sparse_mla": 2.0 * sh.H * (2 * sh.d_c + sh.d_r) * pairs_sel,
+        "absorb_v": 2.0 * M * sh.H * sh.d_c * sh.d_v,
+    }
+    hbm = {
+        # k^I once, q^I and w of the scored rows, their fp32 scores written and read back, the selection
+        "indexer+topk": wl.total_k * sh.D_I * ki_elt + scored * sh.H_I * (sh.D_I * ki_elt + 4) + 8 * scored_pairs
+                        + 4 * M * sh.k,
+        # W_UK, q_nope in, q~ out (the attention reads q_pe in place)
+        "absorb_q": sh.H * sh.d_n * sh.d_c * elt + M * sh.H * sh.d_n * elt + M * sh.H * sh.d_c * elt,
+        # each distinct selected latent row once, q~ and q_pe rows in, latent context out, the selection
+        "sparse_mla": min(pairs_sel, wl.total_k) * (sh.d_c + sh.d_r) * elt + M * sh.H * (sh.d_c + sh.d_r) * elt
+                      + M * sh.H * sh.d_c * elt + 4 * M * sh.k,
+        "absorb_v": sh.H * sh.d_c * sh.d_v * elt + M * sh.H * (sh.d_c + sh.d_v) * elt,
+    }
+    return flops, hbm
+
+
+def roofline_of(stage, ms, flops, hbm, peaks, peak_src, wl_name, fp8=False):
+    """Tensor-bound when the stage's intensity is above the ridge point of the
+    measured peaks, else HBM-bound.  The burst peak applies: every timed region
+    here lasts well under a second."""
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if flops / hbm >= ridge:
+        achieved, peak, unit, bound = flops / (ms * 1e9), tensor_peak, "TFLOP/s", "tensor"
+        psrc = (f"{peak_src} bf16 burst" + (" x 2 (nominal FP8 : bf16 ratio)" if fp8 else ""))
+        alg = f"{flops / 1e9:.1f} GFLOP per launch"
+    else:
+        achieved, peak, unit, bound = hbm / (ms * 1e6), peaks["hbm_gbs"], "GB/s", "hbm"
+        psrc = f"{peak_src} HBM copy bandwidth"
+        alg = f"{hbm / 1e6:.1f} MB per launch"
+    return {"kernel": stage, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": ncu_traffic(stage, wl_name), "peak_source": psrc,
+            "algorithmic": alg}
+
+
+def measure_workload(cfg, args, world, rank, local, with_cpu):
+    """Times whole dsa_forward steps of workload `cfg`, then its indexer and
+    top-k kernels on their own, then the end-to-end step from host buffers."""
     import torch
 
     import dsa_inputs as di
     import sparse_latent_attention_indexer_gb300 as dsa
 
     dev = torch.device("cuda", local)
-    wl = di.workload(args.config)
+    wl = di.workload(cfg)
     sh = wl.shape
+    name = CONFIG_NAMES[cfg]
     seqs = dsa.Seqs(wl.cu_q, wl.cu_k, wl.start_pos)
     host = wl.tensors
     t = {k: v.to(dev) for k, v in host.items()}
@@ -308,70 +420,243 @@ def run_ours(args, world, rank, local):
     stage_ms = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
                 for j in range(nst - 1)]
     ms = max_over_ranks(statistics.mean(step_ms), world)
-    value = wl.total_q * world / (ms / 1e3)
+    value = M * world / (ms / 1e3)
 
-    # roofline of the dominant stage: flops and compulsory HBM bytes per stage; the stage is
-    # tensor-bound when its intensity is above the measured ridge point, else HBM-bound
     peaks, peak_src = load_peaks()
-    pairs_sel, pairs_causal = wl.selected_pairs(), wl.causal_pairs()
-    elt = 4 if sh.dtype == "f32" else 2
-    ki_elt = 1 if sh.idx_fp8 else elt
-    flops = {
-        "indexer+topk": 2.0 * sh.H_I * sh.D_I * pairs_causal,
-        "absorb_q": 2.0 * M * sh.H * sh.d_n * sh.d_c,
-        "sparse_mla": 2.0 * sh.H * (2 * sh.d_c + sh.d_r) * pairs_sel,
-        "absorb_v": 2.0 * M * sh.H * sh.d_c * sh.d_v,
-    }
-    hbm_bytes = {
-        # k^I once, q^I, w, the fp32 scores written and read back, the selection written
-        "indexer+topk": wl.total_k * sh.D_I * ki_elt + M * sh.H_I * (sh.D_I * ki_elt + 4) + 8 * pairs_causal
-                        + 4 * M * sh.k,
-        # W_UK, q_nope in, q~ out (the attention reads q_pe in place)
-        "absorb_q": sh.H * sh.d_n * sh.d_c * elt + M * sh.H * sh.d_n * elt + M * sh.H * sh.d_c * elt,
-        # each distinct selected latent row once, q~ and q_pe rows in, latent context out
-        "sparse_mla": min(pairs_sel, wl.total_k) * (sh.d_c + sh.d_r) * elt + M * sh.H * (sh.d_c + sh.d_r) * elt
-                      + M * sh.H * sh.d_c * elt + 4 * M * sh.k,
-        "absorb_v": sh.H * sh.d_c * sh.d_v * elt + M * sh.H * (sh.d_c + sh.d_v) * elt,
-    }
+    flops, hbm = stage_work(wl)
     names = ["quant", "indexer+topk", "absorb_q", "sparse_mla", "absorb_v"]
     stages = {n: {"ms": stage_ms[j]} for j, n in enumerate(names)}
-    for n, f in flops.items():
+    for n in flops:
         ok = stages[n]["ms"] > 0
-        stages[n]["tflops"] = f / (stages[n]["ms"] * 1e9) if ok else None
-        stages[n]["gbs"] = hbm_bytes[n] / (stages[n]["ms"] * 1e6) if ok else None
+        stages[n]["tflops"] = flops[n] / (stages[n]["ms"] * 1e9) if ok else None
+        stages[n]["gbs"] = hbm[n] / (stages[n]["ms"] * 1e6) if ok else None
     dom = max(["sparse_mla", "indexer+topk", "absorb_q", "absorb_v"], key=lambda n: stages[n]["ms"])
-    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if flops[dom] / hbm_bytes[dom] >= ridge:
-        achieved, peak, unit, bound = stages[dom]["tflops"], peaks["bf16_tflops_sustained"], "TFLOP/s", "tensor"
-        psrc = f"{peak_src} bf16 sustained (kernel timed inside a step)"
-        alg = f"{flops[dom] / 1e9:.1f} GFLOP per launch"
-    else:
-        achieved, peak, unit, bound = stages[dom]["gbs"], peaks["hbm_gbs"], "GB/s", "hbm"
-        psrc = f"{peak_src} HBM copy bandwidth"
-        alg = f"{hbm_bytes[dom] / 1e6:.1f} MB per launch"
-    roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak if achieved else None,
-                "traffic": ncu_traffic(dom, CONFIG_NAMES[args.config]),
-                "peak_source": psrc, "algorithmic": alg}
+    roofline = roofline_of(dom, stages[dom]["ms"], flops[dom], hbm[dom], peaks, peak_src, name,
+                           fp8=(dom == "indexer+topk" and sh.idx_fp8))
+    kernels = measure_indexer_topk(args, dsa, torch, wl, t, flush, peaks, peak_src)
 
-    e2e = None if args.no_e2e else measure_e2e(args, dsa, torch, dev, wl, host, t, seqs, out, lse, idx, ws)
+    e2e = None if args.no_e2e else measure_e2e(args, dsa, torch, wl, host, t, seqs, out, lse, idx, ws, UNITS[cfg])
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        secs, rows, threads = oracle_sample(wl, args.cpu_rows)
-        cpu = {"value": rows / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+    if with_cpu and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_rows = args.cpu_rows if args.cpu_rows is not None else CPU_ROWS[cfg]
+        secs, rows, threads = oracle_sample(wl, n_rows)
+        cpu = {"value": rows / secs, "unit": UNITS[cfg], "cores": threads, "kind": "oracle",
                "sample": f"{rows} fixed query rows of the same workload (first/last rows, rows around t = k-1, "
                          f"random rows), each doing its full indexer, top-k and attention work, {secs:.1f} s"}
+    res = {"value": value, "unit": UNITS[cfg], "ms_per_step": ms,
+           "dtype": "bf16" if sh.dtype == "bf16" else "f32",
+           "config": {"workload": name, "queries_per_step": M, "keys": wl.total_k, "top_k": sh.k,
+                      "indexer": "fp8 e4m3 + ue8m0 block scales" if sh.idx_fp8 else sh.dtype,
+                      "l2": "flushed (256 MiB write) before every timed step",
+                      "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+           "roofline": roofline, "stages": stages, "kernels": kernels, "gpu_launches": launches, "clocks": clk,
+           "e2e": e2e, "cpu_baseline": cpu}
+    del t, out, lse, idx, ws, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_indexer_topk(args, dsa, torch, wl, t, flush, peaks, peak_src):
+    """The indexer and the top-k kernels timed on their own (CUDA events around
+    each launch, on the current stream), over the same row chunks the forward
+    launches them on; the indexer's rate counts the pairs it multiplies."""
+    sh = wl.shape
+    if all(p + 1 <= sh.k for b in range(wl.B) for p in wl.row_positions(b)):
+        return None  # every row selects all its causal keys: neither kernel runs
+    q, k = t["qI"], t["kI"]
+    qs = ks = None
+    if sh.idx_fp8:
+        q, qs = dsa.dsa_quant_e4m3_ue8m0(t["qI"])
+        k, ks = dsa.dsa_quant_e4m3_ue8m0(t["kI"])
+    chunks = score_chunks(wl)
+    ld = (max(max(wl.S), 1) + 3) // 4 * 4
+    per = chunks[0][1] - chunks[0][0]
+    scores = torch.empty((per, ld), dtype=torch.float32, device=q.device)
+    sel = torch.empty((per, sh.k), dtype=torch.int32, device=q.device)
+    cu_k = wl.cu_k
+    reps = max(1, min(3, args.steps))
+    t_idx = t_topk = 0.0
+    for rep in range(reps + 1):
+        evs = []
+        for r0, r1 in chunks:
+            (sq, sk, sp), b0, b1 = sub_batch(wl, r0, r1)
+            s = dsa.Seqs(sq, sk, sp)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            flush.zero_()
+            e[0].record()
+            dsa.dsa_indexer_scores(q[r0:r1], k[cu_k[b0]:cu_k[b1]], t["w"][r0:r1], s,
+                                   q_scale=None if qs is None else qs[r0 * sh.H_I:r1 * sh.H_I],
+                                   k_scale=None if ks is None else ks[cu_k[b0]:cu_k[b1]], scores=scores[:r1 - r0])
+            e[1].record()
+            dsa.dsa_topk_select(scores[:r1 - r0], s, sh.k, idx=sel[:r1 - r0])
+            e[2].record()
+            evs.append(e)
+        torch.cuda.synchronize()
+        if rep == 0:
+            continue  # warm-up
+        t_idx += sum(e[0].elapsed_time(e[1]) for e in evs)
+        t_topk += sum(e[1].elapsed_time(e[2]) for e in evs)
+    t_idx /= reps
+    t_topk /= reps
+    pairs = indexer_pairs_computed(wl, skip_dense=False)
+    flops = 2.0 * sh.H_I * sh.D_I * pairs
+    fp8 = sh.idx_fp8
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    causal_scores = sum(p + 1 for b in range(wl.B) for p in wl.row_positions(b))
+    decode = max(wl.T) == 1
+    res = {"indexer": {"ms": t_idx, "pairs_computed": pairs, "tflops_computed": flops / (t_idx * 1e9),
+                       "peak_tflops": tensor_peak,
+                       "peak_source": f"{peak_src} bf16 burst" + (" x 2 (nominal FP8 : bf16 ratio)" if fp8 else ""),
+                       "frac_of_tensor_peak": flops / (t_idx * 1e9) / tensor_peak},
+           "topk": {"ms": t_topk, "score_bytes_read": 4 * causal_scores,
+                    "gbs": 4 * causal_scores / (t_topk * 1e6)}}
+    if decode:  # the decode indexer streams k^I once: HBM-bound
+        kbytes = wl.total_k * sh.D_I * (1 if fp8 else 2)
+        res["indexer"]["hbm_bytes"] = kbytes
+        res["indexer"]["gbs"] = kbytes / (t_idx * 1e6)
+        res["indexer"]["frac_of_hbm"] = kbytes / (t_idx * 1e6) / peaks["hbm_gbs"]
+    res["note"] = ("timed outside the step, launch by launch over the forward's row chunks; dsa_indexer_scores "
+                   "also writes -inf for the masked keys past the causal blocks, which the forward skips")
+    return res
+
+
+def run_ours(args, world, rank, local):
+    extra = [int(x) for x in args.extra.split(",") if x.strip() != ""] if args.extra else []
+    extra = [c for c in extra if c != args.config]
+    main = measure_workload(args.config, args, world, rank, local, with_cpu=True)
+    others = {}
+    for c in extra:
+        others[EXTRA_KEYS.get(c, f"config{c}")] = measure_workload(c, args, world, rank, local, with_cpu=False)
+    nxt = None if args.no_next else measure_next(args, local)
     if rank != 0:
         return
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if sh.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {"workload": CONFIG_NAMES[args.config], "tokens_per_step": M, "keys": wl.total_k,
-                       "top_k": sh.k, "l2": "flushed (256 MiB write) before every timed step",
-                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
-            "roofline": roofline, "stages": stages, "gpu_launches": launches, "clocks": clk,
-            "e2e": e2e, "cpu_baseline": cpu}
+    line = {"metric": METRIC, "value": main["value"], "unit": main["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": main["dtype"], "data": "synthetic", "config": main["config"],
+            "roofline": main["roofline"], "stages": main["stages"], "kernels": main["kernels"],
+            "gpu_launches": main["gpu_launches"], "clocks": main["clocks"], "e2e": main["e2e"],
+            "cpu_baseline": main["cpu_baseline"]}
+    for key, r in others.items():
+        r.pop("cpu_baseline", None)
+        line[key] = r
+    if nxt is not None:
+        line["next"] = nxt
     print(json.dumps(line), flush=True)
+
+
+def _time_ms(torch, fn, flush, steps, warmup):
+    """Mean CUDA-event time of fn() on the current stream, L2 flushed before each call."""
+    for _ in range(max(warmup, 1)):
+        flush.zero_()
+        fn()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.mean(times)
+
+
+def measure_next(args, local):
+    """The steps on either side of the path and the FP8 latent cache, each timed
+    on its own with CUDA events:
+      * kv_prologue: the key side of 4096 new tokens (x [4096, 7168] bf16 times
+        the stacked [768, 7168] weight, kv_norm, rotary k_pe, k_norm, the cache
+        append with the FP8 indexer key);
+      * output_proj: wo on the 4K prefill's attention output (4096 x 16384 ->
+        7168);
+      * prefill_4k_with_wo: the 4K prefill step with W_UV and wo chunk by chunk;
+      * decode_fp8_latent: the decode workload with its latent cache in e4m3 +
+        ue8m0 scales (656 instead of 1152 bytes per key)."""
+    import math
+
+    import torch
+
+    import dsa_inputs as di
+    import sparse_latent_attention_indexer_gb300 as dsa
+
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    g = torch.Generator().manual_seed(5)
+    res = {}
+    T, dim = 4096, 7168
+    x = torch.randn(T, dim, generator=g).to(torch.bfloat16).to(dev)
+    W = (torch.randn(768, dim, generator=g) / math.sqrt(dim)).to(torch.bfloat16).to(dev)
+    ones512, ones128, zeros128 = (torch.ones(512, device=dev), torch.ones(128, device=dev),
+                                  torch.zeros(128, device=dev))
+    ang = torch.arange(T, dtype=torch.float64)[:, None] * (10000.0 ** (-torch.arange(32, dtype=torch.float64) / 32))
+    cos_t, sin_t = torch.cos(ang).float().to(dev), torch.sin(ang).float().to(dev)
+    seqs = dsa.Seqs([0, T], [0, T], [0])
+    kv_cache = torch.empty(T, 576, dtype=torch.bfloat16, device=dev)
+    k_codes = torch.empty(T, 128, dtype=torch.uint8, device=dev)
+    k_scale = torch.empty(T, device=dev)
+    wts = torch.empty(T, 64, device=dev)
+    ws = torch.empty(dsa._abi.load().dsa_kv_prologue_workspace_size(dim, 512, 64, 128, 64, seqs.ref()),
+                     dtype=torch.uint8, device=dev)
+    ms = _time_ms(torch, lambda: dsa.dsa_kv_prologue(x, W, ones512, ones128, zeros128, cos_t, sin_t, seqs, kv_cache,
+                                                     k_codes, w=wts, k_scale=k_scale, workspace=ws),
+                  flush, args.steps, args.warmup)
+    gemm_flop = 2.0 * T * dim * 768
+    res["kv_prologue"] = {"tokens": T, "ms": ms, "tokens_per_s": T / (ms / 1e3),
+                          "gemm_tflops": gemm_flop / (ms * 1e9),
+                          "frac_of_tensor_peak": gemm_flop / (ms * 1e9) / peaks["bf16_tflops"],
+                          "peak_source": f"{peak_src} bf16 burst",
+                          "note": "tensor-core GEMM x . W_proj^T (45.1 GFLOP) plus the per-token norms, rotation "
+                                  "and FP8 append, timed together"}
+    del x, W, kv_cache, k_codes, k_scale, wts, ws
+    out = torch.randn(T, 128 * 128, generator=g).to(torch.bfloat16).to(dev)
+    wo = (torch.randn(dim, 128 * 128, generator=g) / 128.0).to(torch.bfloat16).to(dev)
+    y = torch.empty(T, dim, dtype=torch.bfloat16, device=dev)
+    ms = _time_ms(torch, lambda: dsa.dsa_output_proj(out, wo, y=y), flush, args.steps, args.warmup)
+    flop = 2.0 * T * 16384 * dim
+    res["output_proj"] = {"rows": T, "ms": ms, "tflops": flop / (ms * 1e9),
+                          "frac_of_tensor_peak": flop / (ms * 1e9) / peaks["bf16_tflops"],
+                          "peak_source": f"{peak_src} bf16 burst", "algorithmic": f"{flop / 1e9:.1f} GFLOP"}
+    del out, y
+
+    wl = di.workload(1)
+    sh = wl.shape
+    t = {k: v.to(dev) for k, v in wl.tensors.items()}
+    ckv, kpe = t["kv_cache"][:, :sh.d_c], t["kv_cache"][:, sh.d_c:]
+    s1 = dsa.Seqs(wl.cu_q, wl.cu_k, wl.start_pos)
+    outs = {}
+
+    def fwd(with_wo):
+        outs["r"] = dsa.dsa_forward(t["qI"], t["kI"], t["w"], t["q_nope"], t["q_pe"], ckv, kpe, t["W_UK"], t["W_UV"],
+                                    s1, sh.k, sh.softmax_scale, wo=wo if with_wo else None, want_out=not with_wo)
+    ms0 = _time_ms(torch, lambda: fwd(False), flush, args.steps, args.warmup)
+    ms1 = _time_ms(torch, lambda: fwd(True), flush, args.steps, args.warmup)
+    res["prefill_4k_with_wo"] = {"ms": ms1, "tokens_per_s": wl.total_q / (ms1 / 1e3), "ms_without_wo": ms0,
+                                 "wo_added_ms": ms1 - ms0,
+                                 "note": "dsa_forward with the output projection: W_UV and wo in chunks of 2048 "
+                                         "rows, the attention output of a chunk read back from L2 (not kept)"}
+    del t, outs, wo
+    torch.cuda.empty_cache()
+
+    wl = di.workload(3)
+    sh = wl.shape
+    t = {k: v.to(dev) for k, v in wl.tensors.items()}
+    ckv, kpe = t["kv_cache"][:, :sh.d_c], t["kv_cache"][:, sh.d_c:]
+    codes, scales = dsa.dsa_quant_e4m3_ue8m0(ckv.contiguous())
+    scales = scales.view(-1, sh.d_c // 128)
+    s3 = dsa.Seqs(wl.cu_q, wl.cu_k, wl.start_pos)
+
+    def dec(fp8):
+        dsa.dsa_forward(t["qI"], t["kI"], t["w"], t["q_nope"], t["q_pe"], codes if fp8 else ckv, kpe, t["W_UK"],
+                        t["W_UV"], s3, sh.k, sh.softmax_scale, kv_scale=scales if fp8 else None)
+    ms_b = _time_ms(torch, lambda: dec(False), flush, args.steps, args.warmup)
+    ms_8 = _time_ms(torch, lambda: dec(True), flush, args.steps, args.warmup)
+    res["decode_fp8_latent"] = {"ms": ms_8, "queries_per_s": wl.total_q / (ms_8 / 1e3), "ms_bf16_latent": ms_b,
+                                "latent_bytes_per_key": {"fp8": sh.d_c + 4 * (sh.d_c // 128) + 2 * sh.d_r,
+                                                         "bf16": 2 * (sh.d_c + sh.d_r)}}
+    del t, codes, scales
+    torch.cuda.empty_cache()
+    return res
 
 
 def _gpu_uuid(local):
@@ -383,15 +668,27 @@ def _gpu_uuid(local):
         return None
 
 
-def measure_e2e(args, dsa, torch, dev, wl, host, t, seqs, out, lse, idx, ws):
-    """The same step through the public API with HOST buffers: pinned host
-    inputs copied in, dsa_forward, the output copied back, all inside the
-    timed events."""
+def measure_e2e(args, dsa, torch, wl, host, t, seqs, out, lse, idx, ws, unit):
+    """The same step through the public API with HOST buffers: every step
+    copies that step's inputs from pinned host memory -- the new queries'
+    tensors and the key-cache rows they append (each sequence's cache rows
+    start_pos .. S-1; the rows before start_pos are the cache the earlier
+    steps left resident) -- runs dsa_forward and copies the output back, all
+    inside the timed events."""
     sh = wl.shape
-    pinned = {k: v.pin_memory() for k, v in host.items()}
+    query_keys = ["qI", "w", "q_nope", "q_pe"]
+    pinned = {k: host[k].pin_memory() for k in query_keys}
+    weights = {k: host[k].pin_memory() for k in ("W_UK", "W_UV")}
+    cu_k = wl.cu_k
+    spans = [(cu_k[b] + wl.start_pos[b], cu_k[b + 1]) for b in range(wl.B)]
+    new_rows = torch.cat([torch.arange(a, b) for a, b in spans])
+    cache_new = {k: host[k][new_rows].pin_memory() for k in ("kv_cache", "kI")}
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    h2d = sum(v.numel() * v.element_size() for v in list(pinned.values()) + list(cache_new.values()))
     d2h = out_host.numel() * out_host.element_size()
+    # the weights are copied once, outside the timed region (they do not change between steps)
+    for k, v in weights.items():
+        t[k].copy_(v)
     ckv, kpe = t["kv_cache"][:, :sh.d_c], t["kv_cache"][:, sh.d_c:]
     times = []
     for i in range(args.warmup + args.steps):
@@ -399,6 +696,11 @@ def measure_e2e(args, dsa, torch, dev, wl, host, t, seqs, out, lse, idx, ws):
         s_ev.record()
         for k, v in pinned.items():
             t[k].copy_(v, non_blocking=True)
+        for k, v in cache_new.items():
+            off = 0
+            for a, b in spans:
+                t[k][a:b].copy_(v[off:off + (b - a)], non_blocking=True)
+                off += b - a
         dsa.dsa_forward(t["qI"], t["kI"], t["w"], t["q_nope"], t["q_pe"], ckv, kpe, t["W_UK"], t["W_UV"], seqs, sh.k,
                         sh.softmax_scale, idx_fp8=sh.idx_fp8, out=out, lse=lse, idx_out=idx, workspace=ws)
         out_host.copy_(out, non_blocking=True)
@@ -407,8 +709,10 @@ def measure_e2e(args, dsa, torch, dev, wl, host, t, seqs, out, lse, idx, ws):
         if i >= args.warmup:
             times.append(s_ev.elapsed_time(e_ev))
     ms = statistics.mean(times)
-    return {"value": wl.total_q / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+    return {"value": wl.total_q / (ms / 1e3), "unit": unit, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "inputs": "the step's queries (q^I, w, q_nope, q_pe) and the cache rows they append "
+                      "(latent + k_pe, k^I); the earlier cache rows stay resident"}
 
 
 def main():

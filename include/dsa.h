@@ -177,6 +177,31 @@ int dsa_sparse_mla_fwd(const void *q_nope, const void *q_pe, int dtype, const vo
                        void *stream);
 
 /* ------------------------------------------------------------------------
+ * Sparse latent attention over an FP8 latent cache.
+ * Source: the "DeepSeek-V3.2-Exp - Block input" page, config_671B_v3.2.json
+ * excerpt (dtype fp8, scale_fmt ue8m0), read as the storage format of the
+ * latent rows c^KV: e4m3 codes with one power-of-two scale per 128 values,
+ * the same block recipe as dsa_quant_e4m3_ue8m0 (which produces them).  The
+ * rotary keys k_pe stay bf16.
+ *
+ * Computes what dsa_sparse_mla_fwd computes on the dequantised latent rows
+ * c[s, j] = code[s, j] * kv_scale[s, j / 128] (exact in bf16), with the same
+ * arguments except:
+ *   kv_codes  [sum S, ld_kv] uint8 e4m3 codes (d_c per row; ld_kv in bytes, a
+ *             multiple of 16; 16-byte aligned)
+ *   kv_scale  [sum S, d_c / 128] fp32 power-of-two scales
+ *   k_pe      [sum S, ld_pe] bf16
+ * Only the tensor-core kernel's shapes (H = 128, d_n = 128, d_r = 64,
+ * d_c = 512, d_v = 128, bf16 queries and weights) are supported.
+ * Errors: DSA_ERR_INVALID_ARG, DSA_ERR_WORKSPACE, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+int dsa_sparse_mla_fwd_fp8kv(const void *q_nope, const void *q_pe, const uint8_t *kv_codes, int64_t ld_kv,
+                             const float *kv_scale, const void *k_pe, int64_t ld_pe, const void *W_UK, const void *W_UV,
+                             int H, int d_n, int d_r, int d_c, int d_v, const int32_t *idx, int k,
+                             const dsa_seqs *seqs, float softmax_scale, void *out, float *lse, void *workspace,
+                             size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Sparse latent attention without a caller workspace.
  * The pages have no counterpart to this entry point: it exists for callers
  * that cannot obtain device memory when they run the attention, e.g. a
@@ -184,8 +209,8 @@ int dsa_sparse_mla_fwd(const void *q_nope, const void *q_pe, int dtype, const vo
  * pool (a late cudaMalloc would fail or stall every stream), or a plugin
  * called from such a runtime that receives only its input and output
  * tensors.  It computes exactly what dsa_sparse_mla_fwd computes, with the
- * same arguments minus the workspace, using scratch memory the library
- * reserves on every GPU that loads it (DSA_NOALLOC_SCRATCH_BYTES, held until
+ * same arguments minus the workspace, using scratch memory that is part of
+ * the library's device code (DSA_NOALLOC_SCRATCH_BYTES per device, held until
  * the process exits) instead of a caller buffer.  It allocates nothing.
  *
  *   - Limit: the call needs the same scratch as dsa_sparse_mla_workspace_size()
@@ -193,9 +218,16 @@ int dsa_sparse_mla_fwd(const void *q_nope, const void *q_pe, int dtype, const vo
  *     DSA_ERR_WORKSPACE and launches nothing.  With the 671B head shapes and
  *     this version's scratch layout that is up to 128 query rows per call,
  *     e.g. one decode step of up to 128 sequences.
- *   - The first call on each device looks up the scratch's device address
- *     (with that device current) and caches it; make that first call before
- *     any stream capture.
+ *   - When the scratch is reserved: CUDA loads the library's device code on a
+ *     device lazily by default, at the first call of this entry point on that
+ *     device, and the scratch is reserved then.  A call with zero query rows
+ *     (cu_q[B] = 0) does this set-up and launches nothing.  A caller that
+ *     hands the rest of HBM to its own pool makes that first call before
+ *     carving the pool (or runs with CUDA_MODULE_LOADING=EAGER, which loads
+ *     it with the context); make it before any stream capture as well.
+ *   - Every call looks up the scratch's device address for the current
+ *     device (a host-side lookup once loaded), so it stays right across a
+ *     device reset.
  *   - Every call on a device shares the one scratch array, which keeps the
  *     previous call's contents (the attention writes every scratch byte it
  *     reads, so nothing needs clearing).  Calls that overlap on the GPU --
@@ -208,6 +240,65 @@ int dsa_sparse_mla_fwd_noalloc(const void *q_nope, const void *q_pe, int dtype, 
                                int64_t ld_kv, const void *k_pe, int64_t ld_pe, const void *W_UK, const void *W_UV,
                                int H, int d_n, int d_r, int d_c, int d_v, const int32_t *idx, int k,
                                const dsa_seqs *seqs, float softmax_scale, void *out, float *lse, void *stream);
+
+/* ------------------------------------------------------------------------
+ * The step before the path: the key side of the new tokens, appended to the
+ * caches.
+ * Sources: "DeepSeek-V3.2-Exp - Attention input" page, mla-init and mla-kv
+ * excerpts (kv = wkv_a(x); split into kv_lora_rank + qk_rope_head_dim;
+ * kv_norm; apply_rotary_emb on k_pe with freqs_cis); "DeepSeek-V3.2-Exp -
+ * Block input" page, RMSNorm excerpt (float32 compute, one gain per feature,
+ * eps 1e-6); nnterp deepseek_v32 printout (indexer wk 7168 -> 128, k_norm
+ * LayerNorm(128, eps 1e-6, gain and bias), weights_proj 7168 -> 64) and its
+ * note that the rotary part is served de-interleaved.
+ *
+ * For token t of sequence b (position p = start_pos[b] + t, cache row
+ * j = cu_k[b] + p), with Y = x . W_proj^T kept in fp32:
+ *   kv_cache[j, 0 .. d_c-1]       = bf16(kv_gain * Y[0:d_c] / sqrt(mean(Y[0:d_c]^2) + 1e-6))
+ *   kv_cache[j, d_c + i]          = bf16(a cos_i - b sin_i)   with (a, b) = Y[d_c + 2i], Y[d_c + 2i + 1]
+ *   kv_cache[j, d_c + d_r/2 + i]  = bf16(a sin_i + b cos_i)   (cos_i, sin_i of position p)
+ *   k^I = bf16(LayerNorm(Y[d_c+d_r : +D_I]) * k_gain + k_bias)  (mean, biased variance, eps 1e-6)
+ *   k_cache[j] = k^I (bf16), or its e4m3 codes with k_scale[j] as
+ *                dsa_quant_e4m3_ue8m0 computes them from the bf16 k^I
+ *   w[r, :]    = Y[d_c+d_r+D_I : +H_I]   (r = cu_q[b] + t, the indexer's weights)
+ *
+ *   x          [sum T, dim] bf16: the new tokens as the attention receives them
+ *   W_proj     [d_c + d_r + D_I + H_I, dim] bf16: the rows of wkv_a, then of
+ *              wk, then of weights_proj (nn.Linear layout, stacked)
+ *   kv_gain    [d_c] fp32; k_gain, k_bias [D_I] fp32
+ *   rope_cos, rope_sin  [n_pos, d_r/2] fp32: cos and sin of the angle of
+ *              frequency i at position p (row p); every appended position
+ *              must be < n_pos
+ *   kv_cache   [sum S, ld_kv] bf16, ld_kv >= d_c + d_r (rows written: the
+ *              appended ones only)
+ *   k_cache    [sum S, D_I] of k_dtype (DSA_BF16, or DSA_E4M3 with D_I = 128
+ *              and k_scale [sum S] fp32)
+ *   w          out [sum T, H_I] fp32
+ *   workspace  >= dsa_kv_prologue_workspace_size(), 256-byte aligned (the fp32 Y)
+ * Errors: DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED (dim or the stacked width
+ * not a multiple of 64, odd d_r, D_I > 256), DSA_ERR_WORKSPACE, DSA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+size_t dsa_kv_prologue_workspace_size(int dim, int d_c, int d_r, int D_I, int H_I, const dsa_seqs *seqs);
+int dsa_kv_prologue(const void *x, int dim, const void *W_proj, const float *kv_gain, const float *k_gain,
+                    const float *k_bias, const float *rope_cos, const float *rope_sin, int n_pos, int d_c, int d_r,
+                    int D_I, int H_I, const dsa_seqs *seqs, void *kv_cache, int64_t ld_kv, void *k_cache, int k_dtype,
+                    float *k_scale, float *w, void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * The step after the path: the output projection y = out . wo^T.
+ * Source: "DeepSeek-V3.2-Exp - Attention input" page, mla-init excerpt (wo maps
+ * n_heads * v_head_dim to dim); nnterp deepseek_v32 printout (o_proj,
+ * 16384 -> 7168, reading every head's output side by side).
+ *
+ *   out   [M, in_features] bf16: the attention output [M, H, d_v] viewed as
+ *         [M, H * d_v]
+ *   wo    [d_model, in_features] bf16 (nn.Linear layout)
+ *   y     out [M, d_model] bf16
+ * in_features and d_model multiples of 64; pointers 16-byte aligned.  fp32
+ * accumulation on the tensor cores.
+ * Errors: DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+int dsa_output_proj(const void *out, const void *wo, int M, int in_features, int d_model, void *y, void *stream);
 
 /* ------------------------------------------------------------------------
  * The whole path: [quantise] -> indexer -> top-k -> sparse latent attention.
@@ -244,6 +335,22 @@ typedef struct dsa_problem {
     void *out;                        /* [sum T, H, d_v] (dtype) */
     float *lse;                       /* [sum T, H] or NULL */
     int32_t *idx_out;                 /* [sum T, top_k] or NULL (then kept in the workspace) */
+    /* The step after the path, optional (NULL wo: not applied): the output
+     * projection y = out wo^T ("DeepSeek-V3.2-Exp - Attention input" page,
+     * mla-init excerpt, wo: n_heads * v_head_dim -> dim).  W_UV and wo run
+     * chunk by chunk (2048 rows), so each chunk of the attention output is read
+     * back from L2 right after it is written.  `out` may then be NULL (the
+     * chunks live in the workspace).  bf16 only; d_model and H * d_v multiples
+     * of 64. */
+    const void *wo;                   /* [d_model, H * d_v] */
+    int32_t d_model;
+    void *y;                          /* out [sum T, d_model] */
+    /* FP8 latent cache (as dsa_sparse_mla_fwd_fp8kv): kv_fp8 = 1 makes kv_cache
+     * e4m3 codes with ld_kv in bytes (a multiple of 16) and kv_scale their
+     * [sum S, d_c / 128] fp32 block scales; k_pe stays bf16.  bf16 only, at
+     * the tensor-core kernel's head shapes. */
+    int32_t kv_fp8;
+    const float *kv_scale;
 } dsa_problem;
 
 size_t dsa_forward_workspace_size(const dsa_problem *p, const dsa_seqs *seqs);
@@ -273,6 +380,27 @@ int dsa_check_device_error(void *stream, int *site);
  * 90), after which the context is usable as before.  Returns DSA_ERR_INVALID_ARG
  * for a limit out of range. */
 int dsa_selftest_bounded_wait(int64_t limit_cycles, int *completed_ok, void *stream);
+/* Wait limit of the tensor-core kernels (no counterpart on the pages: a
+ * diagnostic of this library).  Every wait of the indexer, absorption and
+ * attention kernels on a barrier phase gives up after this many SM clock cycles
+ * (default, and `cycles` = 0: 2^32, about two seconds), records its site in the
+ * device error word, and the CTA drains its copies and MMAs already in flight
+ * (those drain waits keep the default limit), frees its tensor memory and exits.
+ * A short limit makes the failure path of the production kernels run without a
+ * fault: the next dsa_check_device_error returns DSA_ERR_TIMEOUT with the site,
+ * the outputs of the calls made meanwhile are undefined, and calls made after
+ * the limit is restored behave normally.  The setting is process-wide and read
+ * when a kernel is launched.  Returns DSA_ERR_INVALID_ARG for cycles < 0 or
+ * above the default. */
+int dsa_set_wait_limit(int64_t cycles);
+/* Selects, for dsa_forward calls that follow, between the two implementations
+ * of the indexer + top-k on batches of at least 304 groups of 4 query rows
+ * (no counterpart on the pages: a choice of this library).  on = 1: one
+ * persistent kernel scores a group into a per-SM slot and selects its rows'
+ * top-k from it, with no [rows, S] score buffer; on = 0 (default): the indexer
+ * writes chunks of fp32 score rows and a separate top-k kernel selects from
+ * them.  Both give identical selections.  Process-wide; returns DSA_OK. */
+int dsa_set_fused_topk(int on);
 /* Bit mask of the kernels the last entry point launched on this host thread
  * (DSA_KERNEL_* bits), and how many kernel launches it made. */
 uint32_t dsa_last_kernels(void);
@@ -301,6 +429,9 @@ int dsa_set_stage_events(void *const *events, int n_events);
 #define DSA_KERNEL_COMBINE      (1u << 9)
 #define DSA_KERNEL_SELFTEST     (1u << 10)
 #define DSA_KERNEL_DENSE_IDX    (1u << 11)
+#define DSA_KERNEL_GEMM_TC      (1u << 12)
+#define DSA_KERNEL_PROLOGUE     (1u << 13)
+#define DSA_KERNEL_INDEXER_TOPK (1u << 14)  /* the indexer launch also selected the top-k (fused) */
 
 #ifdef __cplusplus
 }

@@ -19,7 +19,8 @@ from ._abi import DSA_BF16, DSA_E4M3, DSA_F32, KERNEL_BITS
 __all__ = [
     "Seqs", "DSAError", "dsa_quant_e4m3_ue8m0", "dsa_indexer_scores", "dsa_topk_select",
     "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_fwd", "dsa_forward_workspace_size", "dsa_forward",
-    "dsa_check_device_error", "dsa_selftest_bounded_wait", "last_kernels", "last_launch_count", "build",
+    "dsa_check_device_error", "dsa_selftest_bounded_wait", "dsa_set_wait_limit", "dsa_set_fused_topk", "dsa_kv_prologue",
+    "dsa_output_proj", "dsa_sparse_mla_fwd_fp8kv", "last_kernels", "last_launch_count", "build",
 ]
 
 
@@ -117,6 +118,17 @@ def dsa_selftest_bounded_wait(limit_cycles: int, completed_ok=None, stream=None)
                                                  _stream(stream)))
 
 
+def dsa_set_wait_limit(cycles: int):
+    """Wait limit (SM cycles) of the tensor-core kernels' bounded waits; 0 restores the default."""
+    _check("dsa_set_wait_limit", _abi.load().dsa_set_wait_limit(int(cycles)))
+
+
+def dsa_set_fused_topk(on: bool):
+    """Fused indexer + top-k (one persistent kernel, per-SM score slots) for the
+    dsa_forward calls that follow on large batches; off by default."""
+    _check("dsa_set_fused_topk", _abi.load().dsa_set_fused_topk(1 if on else 0))
+
+
 def dsa_quant_e4m3_ue8m0(x: torch.Tensor, codes=None, scales=None, stream=None):
     """x: [..., 128k] f32/bf16 -> (codes uint8 same shape, scales f32 [numel/128])."""
     x = x.contiguous()
@@ -183,8 +195,65 @@ def dsa_sparse_mla_fwd(q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, idx, seqs: Seqs
     return out, lse
 
 
+def dsa_kv_prologue(x, W_proj, kv_gain, k_gain, k_bias, rope_cos, rope_sin, seqs: Seqs, kv_cache, k_cache, w=None,
+                    k_scale=None, d_c=512, d_r=64, D_I=128, H_I=64, workspace=None, stream=None):
+    """The step before the path for the new tokens x [sum T, dim]: writes their
+    rows of kv_cache ([sum S, >= d_c + d_r] bf16) and k_cache ([sum S, D_I] bf16,
+    or uint8 e4m3 codes with k_scale [sum S]) and returns w [sum T, H_I]."""
+    dim = x.shape[1]
+    dev = x.device
+    if w is None:
+        w = torch.empty((seqs.total_q, H_I), dtype=torch.float32, device=dev)
+    k_dtype = DSA_E4M3 if k_cache.dtype in (torch.uint8, torch.float8_e4m3fn) else DSA_BF16
+    lib = _abi.load()
+    need = lib.dsa_kv_prologue_workspace_size(dim, d_c, d_r, D_I, H_I, seqs.ref())
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    st = lib.dsa_kv_prologue(_ptr(x), dim, _ptr(W_proj), _ptr(kv_gain), _ptr(k_gain), _ptr(k_bias), _ptr(rope_cos),
+                             _ptr(rope_sin), rope_cos.shape[0], d_c, d_r, D_I, H_I, seqs.ref(), _ptr(kv_cache),
+                             _row_stride(kv_cache), _ptr(k_cache), k_dtype, _ptr(k_scale), _ptr(w), _ptr(workspace),
+                             workspace.numel(), _stream(stream))
+    _check("dsa_kv_prologue", st)
+    return w
+
+
+def dsa_output_proj(out, wo, y=None, stream=None):
+    """y = out wo^T with out [M, H, d_v] (or [M, H * d_v]) and wo [d_model, H * d_v], bf16."""
+    M = out.shape[0]
+    K = out[0].numel() if M else wo.shape[1]
+    d_model = wo.shape[0]
+    if y is None:
+        y = torch.empty((M, d_model), dtype=out.dtype, device=out.device)
+    _check("dsa_output_proj", _abi.load().dsa_output_proj(_ptr(out), _ptr(wo), M, K, d_model, _ptr(y), _stream(stream)))
+    return y
+
+
+def dsa_sparse_mla_fwd_fp8kv(q_nope, q_pe, kv_codes, kv_scale, k_pe, W_UK, W_UV, idx, seqs: Seqs,
+                             softmax_scale: float, out=None, lse=None, workspace=None, stream=None):
+    """The sparse attention over an FP8 latent cache: kv_codes [sum S, >= d_c] uint8
+    e4m3 codes with kv_scale [sum S, d_c / 128] fp32 block scales; k_pe bf16."""
+    M, H, d_n = q_nope.shape
+    d_r, d_c, d_v = q_pe.shape[2], W_UK.shape[2], W_UV.shape[2]
+    k = idx.shape[1]
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((M, H, d_v), dtype=q_nope.dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((M, H), dtype=torch.float32, device=dev)
+    need = dsa_sparse_mla_workspace_size(DSA_BF16, H, d_n, d_r, d_c, d_v, k, seqs)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    st = _abi.load().dsa_sparse_mla_fwd_fp8kv(_ptr(q_nope), _ptr(q_pe), _ptr(kv_codes), _row_stride(kv_codes),
+                                              _ptr(kv_scale), _ptr(k_pe), _row_stride(k_pe), _ptr(W_UK), _ptr(W_UV), H,
+                                              d_n, d_r, d_c, d_v, _ptr(idx), k, seqs.ref(), float(softmax_scale),
+                                              _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                              _stream(stream))
+    _check("dsa_sparse_mla_fwd_fp8kv", st)
+    return out, lse
+
+
 def _problem(q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, top_k, softmax_scale, idx_fp8, out, lse,
-             idx_out):
+             idx_out, wo=None, y=None, kv_scale=None):
     p = _abi.dsa_problem()
     p.H_I, p.D_I = q_idx.shape[-2], q_idx.shape[-1]
     p.top_k = top_k
@@ -200,9 +269,13 @@ def _problem(q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, top_k, s
     p.kv_cache, p.ld_kv = kv_cache.data_ptr(), _row_stride(kv_cache)
     p.k_pe, p.ld_pe = k_pe.data_ptr(), _row_stride(k_pe)
     p.W_UK, p.W_UV = W_UK.data_ptr(), W_UV.data_ptr()
-    p.out = out.data_ptr()
+    p.out = out.data_ptr() if out is not None else None
     p.lse = lse.data_ptr() if lse is not None else None
     p.idx_out = idx_out.data_ptr() if idx_out is not None else None
+    if wo is not None:
+        p.wo, p.d_model, p.y = wo.data_ptr(), wo.shape[0], y.data_ptr()
+    if kv_scale is not None:
+        p.kv_fp8, p.kv_scale = 1, kv_scale.data_ptr()
     return p
 
 
@@ -212,18 +285,24 @@ def dsa_forward_workspace_size(problem, seqs: Seqs) -> int:
 
 def dsa_forward(q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, seqs: Seqs, top_k: int,
                 softmax_scale: float, idx_fp8: bool = False, out=None, lse=None, idx_out=None, workspace=None,
-                want_lse=True, want_idx=True, stream=None):
-    """The whole path.  Returns (out [sum T, H, d_v], lse [sum T, H] or None, idx [sum T, top_k] or None)."""
+                want_lse=True, want_idx=True, stream=None, wo=None, y=None, want_out=True, kv_scale=None):
+    """The whole path.  Returns (out [sum T, H, d_v] or None, lse [sum T, H] or None,
+    idx [sum T, top_k] or None), plus y [sum T, d_model] = out wo^T when wo is given
+    (the step after the path; with want_out=False the attention output stays in
+    the workspace).  With kv_scale, kv_cache holds the latent rows as e4m3 codes
+    (uint8) with kv_scale [sum S, d_c / 128] block scales."""
     dev = q_nope.device
     M, H = q_nope.shape[0], q_nope.shape[1]
-    if out is None:
+    if out is None and (want_out or wo is None):
         out = torch.empty((M, H, W_UV.shape[2]), dtype=q_nope.dtype, device=dev)
     if lse is None and want_lse:
         lse = torch.empty((M, H), dtype=torch.float32, device=dev)
     if idx_out is None and want_idx:
         idx_out = torch.empty((M, top_k), dtype=torch.int32, device=dev)
+    if wo is not None and y is None:
+        y = torch.empty((M, wo.shape[0]), dtype=q_nope.dtype, device=dev)
     p = _problem(q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, top_k, softmax_scale, idx_fp8, out, lse,
-                 idx_out)
+                 idx_out, wo, y, kv_scale)
     need = dsa_forward_workspace_size(p, seqs)
     if need == 0 and M > 0:
         raise DSAError("dsa_forward_workspace_size", _abi.DSA_ERR_INVALID_ARG)
@@ -231,6 +310,8 @@ def dsa_forward(q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, seqs:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     st = _abi.load().dsa_forward(ctypes.byref(p), seqs.ref(), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("dsa_forward", st)
+    if wo is not None:
+        return out, lse, idx_out, y
     return out, lse, idx_out
 
 

@@ -15,7 +15,8 @@ DSA_NOALLOC_SCRATCH_BYTES = 64 << 20
 KERNEL_BITS = {
     "quant": 1 << 0, "indexer_simt": 1 << 1, "indexer_tc": 1 << 2, "indexer_fp8": 1 << 3, "topk": 1 << 4,
     "absorb_simt": 1 << 5, "absorb_tc": 1 << 6, "mla_simt": 1 << 7, "mla_tc": 1 << 8, "combine": 1 << 9,
-    "selftest": 1 << 10, "dense_idx": 1 << 11,
+    "selftest": 1 << 10, "dense_idx": 1 << 11, "gemm_tc": 1 << 12, "prologue": 1 << 13,
+    "indexer_topk": 1 << 14,
 }
 
 
@@ -35,6 +36,8 @@ class dsa_problem(ctypes.Structure):
         ("ld_kv", ctypes.c_int64), ("k_pe", ctypes.c_void_p), ("ld_pe", ctypes.c_int64),
         ("W_UK", ctypes.c_void_p), ("W_UV", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("idx_out", ctypes.c_void_p),
+        ("wo", ctypes.c_void_p), ("d_model", ctypes.c_int32), ("y", ctypes.c_void_p),
+        ("kv_fp8", ctypes.c_int32), ("kv_scale", ctypes.c_void_p),
     ]
 
 
@@ -48,13 +51,19 @@ SIGNATURES = [
     ("dsa_topk_select", I, [P, I64, SEQS, I, P, P]),
     ("dsa_sparse_mla_workspace_size", SZ, [I, I, I, I, I, I, I, SEQS]),
     ("dsa_sparse_mla_fwd", I, [P, P, I, P, I64, P, I64, P, P, I, I, I, I, I, P, I, SEQS, F, P, P, P, SZ, P]),
+    ("dsa_sparse_mla_fwd_fp8kv", I, [P, P, P, I64, P, P, I64, P, P, I, I, I, I, I, P, I, SEQS, F, P, P, P, SZ, P]),
     ("dsa_sparse_mla_fwd_noalloc", I, [P, P, I, P, I64, P, I64, P, P, I, I, I, I, I, P, I, SEQS, F, P, P, P]),
+    ("dsa_kv_prologue_workspace_size", SZ, [I, I, I, I, I, SEQS]),
+    ("dsa_kv_prologue", I, [P, I, P, P, P, P, P, P, I, I, I, I, I, SEQS, P, I64, P, I, P, P, P, SZ, P]),
+    ("dsa_output_proj", I, [P, P, I, I, I, P, P]),
     ("dsa_forward_workspace_size", SZ, [PROB, SEQS]),
     ("dsa_forward", I, [PROB, SEQS, P, SZ, P]),
     ("dsa_status_string", ctypes.c_char_p, [I]),
     ("dsa_last_cuda_error", I, []),
     ("dsa_check_device_error", I, [P, ctypes.POINTER(ctypes.c_int)]),
     ("dsa_selftest_bounded_wait", I, [I64, P, P]),
+    ("dsa_set_wait_limit", I, [I64]),
+    ("dsa_set_fused_topk", I, [I]),
     ("dsa_last_kernels", U32, []),
     ("dsa_last_launch_count", I, []),
     ("dsa_set_stage_events", I, [ctypes.POINTER(ctypes.c_void_p), I]),

@@ -42,6 +42,7 @@ struct AbsorbParams {
     int n_tiles;  // N / N_TILE
     int mblocks;  // 128-row blocks of M
     int units;    // H * n_tiles * mblocks
+    long long wait_limit;  // SM cycles a wait may take before the CTA gives up (the drains keep the default)
 };
 
 template <int K_TOTAL, int N_TILE>
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const Unit x = unit_of<N_TILE>(P, u0 + i);
                 if (x.pair != prev) {
                     // the MMAs that read the previous pair's weights must be done before they are replaced
-                    if (nb > 0 && !tc::mbar_wait(bfree, (nb - 1) & 1, abort_flag, err, 11)) break;
+                    if (nb > 0 && !tc::mbar_wait(bfree, (nb - 1) & 1, abort_flag, err, 11, P.wait_limit)) break;
                     // B: N_TILE/64 column blocks x K_TOTAL/128 row boxes of [128 rows][64 cols]
                     tc::mbar_arrive_expect_tx(bfull, G::B_BYTES);
                     for (int c = 0; c < N_TILE / 64; ++c)
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 bool ok = true;
                 for (int j = 0; j < G::SLABS; ++j) {
                     const int it = i * G::SLABS + j, st = it % STAGES;
-                    if (!(ok = tc::mbar_wait(&empty[st], ((it / STAGES) & 1) ^ 1, abort_flag, err, 12))) break;
+                    if (!(ok = tc::mbar_wait(&empty[st], ((it / STAGES) & 1) ^ 1, abort_flag, err, 12, P.wait_limit))) break;
                     tc::mbar_arrive_expect_tx(&full[st], SLAB);
                     tc::tma_load_3d(As + st * SLAB, &tm_a, &full[st], j * 64, x.h, x.m0);
                     ++issued;
@@ -177,16 +178,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const Unit x = unit_of<N_TILE>(P, u0 + i);
                 if (x.pair != prev) {
                     if (nb > 0) tc::mma_commit(bfree);  // arrives once every MMA on the old weights is done
-                    if (!(ok = tc::mbar_wait(bfull, nb & 1, abort_flag, err, 15))) break;
+                    if (!(ok = tc::mbar_wait(bfull, nb & 1, abort_flag, err, 15, P.wait_limit))) break;
                     ++nb;
                     prev = x.pair;
                 }
                 const int acc = i & 1;
-                if (!(ok = tc::mbar_wait(&tempty[acc], ((i >> 1) & 1) ^ 1, abort_flag, err, 16))) break;
+                if (!(ok = tc::mbar_wait(&tempty[acc], ((i >> 1) & 1) ^ 1, abort_flag, err, 16, P.wait_limit))) break;
                 const uint32_t d = tmem + acc * N_TILE;
                 for (int j = 0; j < G::SLABS; ++j) {
                     const int it = i * G::SLABS + j, st = it % STAGES;
-                    if (!(ok = tc::mbar_wait(&full[st], (it / STAGES) & 1, abort_flag, err, 17))) break;
+                    if (!(ok = tc::mbar_wait(&full[st], (it / STAGES) & 1, abort_flag, err, 17, P.wait_limit))) break;
                     tc::tc_fence_after();
                     const uint32_t a0 = tc::smem_u32(As + st * SLAB);
 #pragma unroll
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr int COLS = N_TILE / 2;  // columns per epilogue thread
             for (int i = 0; i < mine; ++i) {
                 const int acc = i & 1;
-                bool ok = tc::mbar_wait(&tfull[acc], (i >> 1) & 1, abort_flag, err, 19);
+                bool ok = tc::mbar_wait(&tfull[acc], (i >> 1) & 1, abort_flag, err, 19, P.wait_limit);
                 // The previous unit's TMA stores must have read the staging tile before it is rewritten.
                 if (leader) tc::bulk_wait_read_all();
                 if (!epi_bar_and(bar_free, ok)) break;
@@ -306,6 +307,7 @@ cudaError_t launch_absorb(const void *A, const void *W, void *C, int M, int H, i
     P.n_tiles = N / N_TILE;
     P.mblocks = (M + BM - 1) / BM;
     P.units = H * P.n_tiles * P.mblocks;
+    P.wait_limit = wait_limit_cycles();
     const int grid = std::min(P.units, sm_count());
     cudaError_t e = cudaFuncSetAttribute(absorb_tc_kernel<K_TOTAL, N_TILE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);

@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "dsa_common.cuh"
 
@@ -35,6 +36,21 @@ int fail_cuda(cudaError_t e) {
     g_last_cuda = (int)e;
     return DSA_ERR_CUDA;
 }
+
+int device_sm_count() {
+    static int n[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (n[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
+        n[dev] = v;
+    }
+    return n[dev];
+}
+
+std::atomic<long long> g_wait_limit{kDefaultWaitLimitCycles};
+long long wait_limit_cycles() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 namespace {
 
@@ -138,12 +154,14 @@ MlaWs mla_ws_layout(int H, int d_c, int64_t total_q) {
 int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int64_t ld_kv, const void *k_pe,
             int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n, int d_r, int d_c, int d_v,
             const int32_t *idx, int k, const Batch &bt, float scale, void *out, float *lse, char *ws,
-            cudaStream_t s, bool mark, bool prefix_valid) {
+            cudaStream_t s, bool mark, bool prefix_valid, const void *wo, int d_model, void *y, char *obuf,
+            const float *kv_scale) {
     const MlaWs L = mla_ws_layout(H, d_c, bt.total_q);
     const int M = bt.total_q;
     cudaError_t e;
     const bool fast = !force_generic() && absorb_tc_supported(dtype, H, d_n, d_r, d_c, d_v) && aligned(q_nope, 16) &&
                       aligned(q_pe, 16) && aligned(W_UK, 16) && aligned(W_UV, 16) && aligned(out, 16);
+    if (kv_scale && !(fast && mla_tc_supported(dtype, H, d_n, d_r, d_c, d_v))) return DSA_ERR_UNSUPPORTED;
     if (fast) {
         // q~ rows [M, H, d_c] bf16 = q_nope W_UK (q_pe is read in place); latent context bf16 [M, H, d_c].
         __nv_bfloat16 *qt = (__nv_bfloat16 *)(ws + L.qt);
@@ -151,8 +169,11 @@ int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int
         e = launch_absorb_q_tc(q_nope, W_UK, qt, M, H, s);
         if (e != cudaSuccess) return fail_cuda(e);
         if (mark) stage_mark(3, s);
-        if (mla_tc_supported(dtype, H, d_n, d_r, d_c, d_v) && aligned(kv, 16) && aligned(k_pe, 16) && ld_kv % 8 == 0 &&
-            ld_pe % 8 == 0)
+        if (kv_scale)  // FP8 latent rows: validated by the caller for the tensor-core kernel
+            e = launch_mla_tc(qt, q_pe, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, bt.total_k, M, scale, prefix_valid, olat,
+                              lse, ws + L.part, s, kv_scale);
+        else if (mla_tc_supported(dtype, H, d_n, d_r, d_c, d_v) && aligned(kv, 16) && aligned(k_pe, 16) &&
+                 ld_kv % 8 == 0 && ld_pe % 8 == 0)
             e = launch_mla_tc(qt, q_pe, kv, ld_kv, k_pe, ld_pe, idx, k, bt.st, bt.total_k, M, scale, prefix_valid, olat,
                               lse, ws + L.part, s);
         else
@@ -160,8 +181,23 @@ int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int
                                 d_c, scale, olat, DSA_BF16, lse, s);
         if (e != cudaSuccess) return fail_cuda(e);
         if (mark) stage_mark(4, s);
-        e = launch_absorb_v_tc(olat, W_UV, out, M, H, s);
-        if (e != cudaSuccess) return fail_cuda(e);
+        if (!wo) {
+            e = launch_absorb_v_tc(olat, W_UV, out, M, H, s);
+            if (e != cudaSuccess) return fail_cuda(e);
+        } else {
+            // The step after the path: y = out wo^T, chunk by chunk, so that each chunk of the
+            // attention output is read back by the wo GEMM from L2 right after W_UV wrote it.
+            const int64_t hv = (int64_t)H * d_v;
+            for (int r0 = 0; r0 < M; r0 += kWoChunkRows) {
+                const int m = std::min(kWoChunkRows, M - r0);
+                void *o = out ? (void *)((__nv_bfloat16 *)out + r0 * hv) : (void *)obuf;
+                e = launch_absorb_v_tc(olat + (int64_t)r0 * H * d_c, W_UV, o, m, H, s);
+                if (e != cudaSuccess) return fail_cuda(e);
+                e = launch_gemm_tc(o, hv, wo, hv, (__nv_bfloat16 *)y + (int64_t)r0 * d_model, d_model, false, m,
+                                   d_model, (int)hv, s);
+                if (e != cudaSuccess) return fail_cuda(e);
+            }
+        }
         if (mark) stage_mark(5, s);
         return DSA_OK;
     }
@@ -252,11 +288,27 @@ int dsa_check_device_error(void *stream, int *site) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     if (site) *site = 0;
-    int rc = indexer_tc_read_error(site);
-    if (rc) return rc;
-    if ((rc = absorb_tc_read_error(site))) return rc;
-    if ((rc = mla_tc_read_error(site))) return rc;
-    return selftest_read_error(site);
+    // Every kernel family keeps its own error word; all of them are read and cleared, and the
+    // first one that recorded a timeout gives the site.
+    int (*readers[])(int *) = {indexer_tc_read_error, absorb_tc_read_error, mla_tc_read_error, gemm_tc_read_error,
+                               selftest_read_error};
+    int result = DSA_OK;
+    for (auto rd : readers) {
+        int s = 0;
+        const int rc = rd(&s);
+        if (rc == DSA_ERR_CUDA) return rc;
+        if (rc != DSA_OK && result == DSA_OK) {
+            result = rc;
+            if (site) *site = s;
+        }
+    }
+    return result;
+}
+
+int dsa_set_wait_limit(int64_t cycles) {
+    if (cycles < 0 || cycles > kDefaultWaitLimitCycles) return DSA_ERR_INVALID_ARG;
+    g_wait_limit.store(cycles == 0 ? kDefaultWaitLimitCycles : (long long)cycles, std::memory_order_relaxed);
+    return DSA_OK;
 }
 
 int dsa_selftest_bounded_wait(int64_t limit_cycles, int *completed_ok, void *stream) {
@@ -327,6 +379,27 @@ int dsa_sparse_mla_fwd(const void *q_nope, const void *q_pe, int dtype, const vo
                    softmax_scale, out, lse, (char *)workspace, (cudaStream_t)stream);
 }
 
+int dsa_sparse_mla_fwd_fp8kv(const void *q_nope, const void *q_pe, const uint8_t *kv_codes, int64_t ld_kv,
+                             const float *kv_scale, const void *k_pe, int64_t ld_pe, const void *W_UK, const void *W_UV,
+                             int H, int d_n, int d_r, int d_c, int d_v, const int32_t *idx, int k,
+                             const dsa_seqs *seqs, float softmax_scale, void *out, float *lse, void *workspace,
+                             size_t ws_bytes, void *stream) {
+    reset_trace();
+    Batch bt;
+    int rc = validate_mla_call(q_nope, q_pe, DSA_BF16, kv_codes, ld_kv, k_pe, ld_pe, W_UK, W_UV, H, d_n, d_r, d_c, d_v,
+                               idx, k, seqs, out, bt);
+    if (rc) return rc;
+    if (!mla_tc_supported(DSA_BF16, H, d_n, d_r, d_c, d_v)) return DSA_ERR_UNSUPPORTED;
+    if (bt.total_q == 0) return DSA_OK;
+    if (!kv_scale || ld_kv % 16 != 0 || !aligned(kv_codes, 16) || !aligned(k_pe, 16) || ld_pe % 8 != 0)
+        return DSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, WS_ALIGN)) return DSA_ERR_WORKSPACE;
+    if (ws_bytes < mla_workspace_bytes(H, d_c, bt.total_q)) return DSA_ERR_WORKSPACE;
+    return run_mla(q_nope, q_pe, DSA_BF16, kv_codes, ld_kv, k_pe, ld_pe, W_UK, W_UV, H, d_n, d_r, d_c, d_v, idx, k, bt,
+                   softmax_scale, out, lse, (char *)workspace, (cudaStream_t)stream, false, false, nullptr, 0, nullptr,
+                   nullptr, kv_scale);
+}
+
 }  // extern "C"
 
 namespace dsa {
@@ -342,7 +415,8 @@ constexpr size_t SCORE_CHUNK_BYTES = size_t(1024) << 20;
 struct FwdWs {
     int64_t ld = 0;
     int rows_per_chunk = 0;
-    size_t qcodes = 0, qscale = 0, kcodes = 0, kscale = 0, idx = 0, scores = 0, mla = 0, total = 0;
+    bool fused = false;  // the indexer selects the top-k itself (one launch, per-SM score slots)
+    size_t qcodes = 0, qscale = 0, kcodes = 0, kscale = 0, idx = 0, scores = 0, mla = 0, obuf = 0, total = 0;
 };
 
 int check_problem(const dsa_problem *p) {
@@ -354,6 +428,17 @@ int check_problem(const dsa_problem *p) {
     if (rc) return rc;
     if (p->top_k > 16384) return DSA_ERR_INVALID_ARG;
     if (p->ld_kv < p->d_c || p->ld_pe < p->d_r) return DSA_ERR_INVALID_ARG;
+    if (p->kv_fp8) {  // e4m3 latent rows: the tensor-core attention only
+        if (p->dtype != DSA_BF16 || !mla_tc_supported(p->dtype, p->H, p->d_n, p->d_r, p->d_c, p->d_v))
+            return DSA_ERR_UNSUPPORTED;
+        if (p->ld_kv % 16 != 0) return DSA_ERR_INVALID_ARG;
+    }
+    if (p->wo) {  // the output projection runs on the bf16 tensor-core GEMM only
+        if (p->d_model < 1) return DSA_ERR_INVALID_ARG;
+        if (p->dtype != DSA_BF16 || !gemm_tc_supported(1, p->d_model, p->H * p->d_v) ||
+            !absorb_tc_supported(p->dtype, p->H, p->d_n, p->d_r, p->d_c, p->d_v))
+            return DSA_ERR_UNSUPPORTED;
+    }
     return DSA_OK;
 }
 
@@ -361,7 +446,14 @@ FwdWs fwd_ws_layout(const dsa_problem *p, const Batch &bt) {
     FwdWs w;
     w.ld = ((int64_t)std::max(bt.max_S, 1) + 3) / 4 * 4;
     const int64_t per_row = w.ld * (int64_t)sizeof(float);
-    w.rows_per_chunk = (int)std::max<int64_t>(1, std::min<int64_t>(bt.total_q, SCORE_CHUNK_BYTES / per_row));
+    // Batches with enough query groups take the fused indexer + top-k, whose score slots are much
+    // smaller than a chunk; if it cannot run after all (misaligned inputs) the unfused path chunks
+    // its rows to fit the same region.
+    w.fused = !force_generic() && indexer_topk_fused_ok(p->idx_fp8 ? DSA_E4M3 : p->dtype, p->H_I, p->D_I, bt.st,
+                                                        p->top_k);
+    const int64_t region = w.fused ? (int64_t)indexer_topk_slot_bytes(bt.st, w.ld)
+                                   : (int64_t)std::min<size_t>(SCORE_CHUNK_BYTES, (size_t)bt.total_q * per_row);
+    w.rows_per_chunk = (int)std::max<int64_t>(1, std::min<int64_t>(bt.total_q, region / per_row));
     size_t off = 0;
     if (p->idx_fp8) {
         w.qcodes = off; off += align_up((size_t)bt.total_q * p->H_I * p->D_I);
@@ -372,8 +464,11 @@ FwdWs fwd_ws_layout(const dsa_problem *p, const Batch &bt) {
     if (!p->idx_out) {
         w.idx = off; off += align_up((size_t)bt.total_q * p->top_k * sizeof(int32_t));
     }
-    w.scores = off; off += align_up((size_t)w.rows_per_chunk * per_row);
+    w.scores = off; off += align_up(std::max<size_t>((size_t)w.rows_per_chunk * per_row, w.fused ? region : 0));
     w.mla = off; off += mla_ws_layout(p->H, p->d_c, bt.total_q).total;
+    if (p->wo && !p->out) {  // one chunk of the attention output between W_UV and wo
+        w.obuf = off; off += align_up((size_t)std::min(bt.total_q, kWoChunkRows) * p->H * p->d_v * 2);
+    }
     w.total = off;
     return w;
 }
@@ -396,9 +491,11 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
     Batch bt;
     if ((rc = build_batch(seqs, bt))) return rc;
     if (bt.total_q == 0) return DSA_OK;
-    if (!p->q_idx || !p->k_idx || !p->w || !p->q_nope || !p->kv_cache || !p->W_UK || !p->W_UV || !p->out ||
-        (p->d_r > 0 && (!p->q_pe || !p->k_pe)))
+    if (!p->q_idx || !p->k_idx || !p->w || !p->q_nope || !p->kv_cache || !p->W_UK || !p->W_UV ||
+        (!p->out && !p->wo) || (p->d_r > 0 && (!p->q_pe || !p->k_pe)))
         return DSA_ERR_INVALID_ARG;
+    if (p->wo && (!p->y || !aligned(p->wo, 16) || !aligned(p->y, 16))) return DSA_ERR_INVALID_ARG;
+    if (p->kv_fp8 && (!p->kv_scale || !aligned(p->kv_cache, 16))) return DSA_ERR_INVALID_ARG;
     const FwdWs L = fwd_ws_layout(p, bt);
     if (!workspace || !aligned(workspace, WS_ALIGN) || ws_bytes < L.total) return DSA_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
@@ -424,7 +521,8 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
         stage_mark(2, s);
         return run_mla(p->q_nope, p->q_pe, p->dtype, p->kv_cache, p->ld_kv, p->k_pe, p->ld_pe, p->W_UK, p->W_UV,
                        p->H, p->d_n, p->d_r, p->d_c, p->d_v, nullptr, p->top_k, bt, p->softmax_scale, p->out, p->lse,
-                       ws + L.mla, s, true, true);
+                       ws + L.mla, s, true, true, p->wo, p->d_model, p->y, ws + L.obuf,
+                       p->kv_fp8 ? p->kv_scale : nullptr);
     }
 
     const void *q_idx = p->q_idx, *k_idx = p->k_idx;
@@ -444,6 +542,17 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
     int32_t *idx = p->idx_out ? p->idx_out : (int32_t *)(ws + L.idx);
     float *scores = (float *)(ws + L.scores);
     const size_t qrow = dtype_bytes(idx_dtype) * p->H_I * p->D_I;
+    if (L.fused && aligned(q_idx, 16) && aligned(k_idx, 16)) {
+        // one launch over the whole batch: scores into per-SM slots, the top-k selected from them
+        e = launch_indexer_topk_tc(q_idx, q_scale, k_idx, k_scale, idx_dtype, p->w, bt.st, bt.total_k, scores, L.ld,
+                                   p->top_k, idx, s);
+        if (e != cudaSuccess) return fail_cuda(e);
+        stage_mark(2, s);
+        return run_mla(p->q_nope, p->q_pe, p->dtype, p->kv_cache, p->ld_kv, p->k_pe, p->ld_pe, p->W_UK, p->W_UV, p->H,
+                       p->d_n, p->d_r, p->d_c, p->d_v, idx, p->top_k, bt, p->softmax_scale, p->out, p->lse,
+                       ws + L.mla, s, true, true, p->wo, p->d_model, p->y, ws + L.obuf,
+                       p->kv_fp8 ? p->kv_scale : nullptr);
+    }
     for (int r0 = 0; r0 < bt.total_q; r0 += L.rows_per_chunk) {
         const int r1 = std::min(bt.total_q, r0 + L.rows_per_chunk);
         SeqTab st;
@@ -459,7 +568,7 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
     stage_mark(2, s);
     return run_mla(p->q_nope, p->q_pe, p->dtype, p->kv_cache, p->ld_kv, p->k_pe, p->ld_pe, p->W_UK, p->W_UV, p->H,
                    p->d_n, p->d_r, p->d_c, p->d_v, idx, p->top_k, bt, p->softmax_scale, p->out, p->lse, ws + L.mla, s,
-                   true, true);
+                   true, true, p->wo, p->d_model, p->y, ws + L.obuf, p->kv_fp8 ? p->kv_scale : nullptr);
 }
 
 }  // extern "C"

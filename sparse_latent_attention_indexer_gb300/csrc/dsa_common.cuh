@@ -57,6 +57,17 @@ template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+// Exponent e of the ue8m0 block scale 2^e: the smallest integer with amax <= 448 * 2^e, clamped to
+// the ue8m0 range (amax = 0 gives 0).  With amax = m * 2^E, m in [0.5, 1) and 448 = 0.875 * 2^9:
+// e = E - 9 when m <= 0.875, else E - 8.  Exact for every finite fp32 amax.
+__device__ __forceinline__ int ue8m0_exponent(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    int E;
+    float m = frexpf(amax, &E);
+    int e = (m <= 0.875f) ? E - 9 : E - 8;
+    return max(-127, min(127, e));
+}
+
 // Order-preserving map of an fp32 score to uint32 (larger float -> larger
 // key); -0 is folded onto +0 first so equal values get equal keys.
 __device__ __forceinline__ uint32_t ordered_key(float f) {
@@ -95,6 +106,14 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 void reset_trace();
 int fail_cuda(cudaError_t e);
 
+// Wait limit of the tensor-core kernels' bounded waits, in SM clock cycles: about two seconds by
+// default; dsa_set_wait_limit changes it for the launches that follow (the waits that drain copies
+// and MMAs already in flight keep the default).
+constexpr long long kDefaultWaitLimitCycles = 4LL << 30;
+long long wait_limit_cycles();
+// Streaming multiprocessors of the current device (152 on a GB300).
+int device_sm_count();
+
 // A validated batch: the kernel table for all rows plus summary sizes.
 struct Batch {
     SeqTab st;
@@ -119,7 +138,11 @@ int validate_mla_call(const void *q_nope, const void *q_pe, int dtype, const voi
 int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int64_t ld_kv, const void *k_pe,
             int64_t ld_pe, const void *W_UK, const void *W_UV, int H, int d_n, int d_r, int d_c, int d_v,
             const int32_t *idx, int k, const Batch &bt, float scale, void *out, float *lse, char *ws,
-            cudaStream_t s, bool mark = false, bool prefix_valid = false);
+            cudaStream_t s, bool mark = false, bool prefix_valid = false, const void *wo = nullptr,
+            int d_model = 0, void *y = nullptr, char *obuf = nullptr, const float *kv_scale = nullptr);
+// Rows per chunk of the W_UV -> wo sequence: the chunk's [rows, H * d_v] bf16 attention output
+// (64 MB at the 671B shapes) is read back by the wo GEMM while it is still in L2.
+constexpr int kWoChunkRows = 2048;
 
 // ---------------------------------------------------------------------------
 // Kernel launchers.  Each returns the cudaError_t of its launch.
@@ -138,6 +161,13 @@ cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k
                               const float *w, const SeqTab &st, int64_t total_k, float *scores, int64_t ld,
                               bool fill_future, cudaStream_t s, int dense_k = 0);
 int indexer_tc_read_error(int *site);
+// The indexer and the top-k in one persistent kernel (prefill-sized batches): per SM one slot of 4
+// fp32 score rows of ld columns (indexer_topk_slot_bytes) instead of a [rows, ld] buffer.
+bool indexer_topk_fused_ok(int dtype, int H_I, int D_I, const SeqTab &st, int k);
+size_t indexer_topk_slot_bytes(const SeqTab &st, int64_t ld);
+cudaError_t launch_indexer_topk_tc(const void *q, const float *q_scale, const void *k, const float *k_scale, int dtype,
+                                   const float *w, const SeqTab &st, int64_t total_k, float *slots, int64_t ld,
+                                   int topk, int32_t *idx, cudaStream_t s);
 
 // DSA_FORCE_GENERIC=1 in the environment routes every stage to the generic
 // CUDA-core kernels (used by the tests to cross-check the tensor-core ones).
@@ -176,8 +206,16 @@ int mla_tc_splits(int M);
 size_t mla_tc_partial_bytes(int M);
 cudaError_t launch_mla_tc(const void *qt, const void *qpe, const void *kv, int64_t ld_kv, const void *kpe, int64_t ld_pe,
                           const int32_t *idx, int k, const SeqTab &st, int64_t total_k, int M, float scale,
-                          bool prefix_valid, void *olat, float *lse, void *part_ws, cudaStream_t s);
+                          bool prefix_valid, void *olat, float *lse, void *part_ws, cudaStream_t s,
+                          const float *kv_scale = nullptr);
 int mla_tc_read_error(int *site);
+
+// tcgen05 dense GEMM C[M, N] = A[M, K] B[N, K]^T (bf16 in, fp32 accumulation, C bf16 or fp32);
+// N and K multiples of 64, rows 16-byte aligned.
+bool gemm_tc_supported(int M, int N, int K);
+cudaError_t launch_gemm_tc(const void *A, int64_t lda, const void *B, int64_t ldb, void *C, int64_t ldc, bool c_f32,
+                           int M, int N, int K, cudaStream_t s);
+int gemm_tc_read_error(int *site);
 
 // Bounded-wait self-test (selftest.cu): one CTA whose first wait runs out after limit_cycles.
 cudaError_t launch_bounded_wait_selftest(long long limit_cycles, int *completed_ok, cudaStream_t s);

@@ -27,7 +27,10 @@
 // 128-value row (ue8m0), MMA kind::f8f6f4.  Because each scale covers a whole
 // head row, sum_h w s_q ReLU(s_k cq.ck) = s_k sum_h (w s_q) ReLU(cq.ck) holds
 // exactly, so the scales need no block-scaled MMA.
+#include <atomic>
+
 #include "tc_common.cuh"
+#include "topk_row.cuh"
 
 namespace dsa {
 
@@ -79,8 +82,219 @@ struct IdxParams {
     int fill_future;
     int dense_k;  // > 0: skip groups whose rows all see at most dense_k keys (they select every causal key)
     int64_t ld;
+    long long wait_limit;  // SM cycles a wait may take before the CTA gives up (the drains keep the default)
     float c;
+    int topk;  // the fused kernel: k of the selection
 };
+
+// One group: 4 consecutive query rows of one sequence.
+struct Group {
+    int r0, p0, ntok, S, kbase, nblk;
+};
+
+__device__ __forceinline__ Group group_of(const IdxParams &P, int g) {
+    int lo = 0, hi = P.B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (P.g_off[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    Group G;
+    const int t0 = (g - P.g_off[b]) * TOK;
+    G.ntok = min(TOK, P.q_off[b + 1] - P.q_off[b] - t0);
+    G.r0 = P.q_off[b] + t0;
+    G.p0 = P.start_pos[b] + t0;
+    G.S = P.k_len[b];
+    G.kbase = P.k_base[b];
+    G.nblk = (G.p0 + G.ntok - 1) / BM + 1;  // blocks holding keys 0 .. last position
+    return G;
+}
+
+// Shared-memory layout of both indexer kernels: addresses computed from one base pointer.
+template <bool FP8>
+struct Smem {
+    using C = Cfg<FP8>;
+    uint8_t *base;
+    __device__ __forceinline__ explicit Smem(uint8_t *raw)
+        : base((uint8_t *)(((uintptr_t)raw + 1023) & ~(uintptr_t)1023)) {}
+    __device__ __forceinline__ uint8_t *Bt() const { return base; }
+    __device__ __forceinline__ uint8_t *As() const { return base + C::B_BYTES; }
+    __device__ __forceinline__ float *wsm() const { return (float *)(base + C::B_BYTES + C::STAGES * C::A_BYTES); }
+    __device__ __forceinline__ uint64_t *bars() const { return (uint64_t *)(wsm() + TOK * HI); }
+    __device__ __forceinline__ uint64_t *full(int i) const { return bars() + i; }
+    __device__ __forceinline__ uint64_t *empty(int i) const { return bars() + C::STAGES + i; }
+    __device__ __forceinline__ uint64_t *bfull() const { return bars() + 2 * C::STAGES; }
+    __device__ __forceinline__ uint64_t *tfull(int i) const { return bars() + 2 * C::STAGES + 1 + i; }
+    __device__ __forceinline__ uint64_t *tempty(int i) const { return bars() + 2 * C::STAGES + 3 + i; }
+    __device__ __forceinline__ uint64_t *mmadone() const { return bars() + 2 * C::STAGES + 5; }
+    __device__ __forceinline__ uint32_t *tmem_slot() const { return (uint32_t *)(bars() + 2 * C::STAGES + 6); }
+    __device__ __forceinline__ volatile int *abort_flag() const { return (volatile int *)(tmem_slot() + 1); }
+};
+
+// Barrier phases carried from group to group by a CTA that takes several groups: loads issued
+// into the stage ring, accumulators used, query-tile loads and MMA drains.
+struct Phases {
+    int it = 0, ai = 0, nq = 0, md = 0;
+    __device__ __forceinline__ void advance(int mine) {
+        it += mine;
+        ai += mine;
+        nq += mine > 0;
+        md += mine > 0;
+    }
+};
+
+template <bool FP8>
+__device__ __forceinline__ void init_barriers(const Smem<FP8> &sm) {
+    using C = Cfg<FP8>;
+    for (int i = 0; i < C::STAGES; ++i) {
+        tc::mbar_init(sm.full(i), 1);
+        tc::mbar_init(sm.empty(i), 1);
+    }
+    tc::mbar_init(sm.bfull(), 1);
+    for (int i = 0; i < 2; ++i) {
+        tc::mbar_init(sm.tfull(i), 1);
+        tc::mbar_init(sm.tempty(i), num_epi<FP8>());
+    }
+    tc::mbar_init(sm.mmadone(), 1);
+    *sm.abort_flag() = 0;
+    tc::fence_mbar_init();
+}
+
+// The weights of the group's rows, with the constant 1/sqrt(H_I D_I) and (FP8) the q block scale
+// folded in; written by the epilogue threads.
+template <bool FP8>
+__device__ __forceinline__ void load_weights(const Smem<FP8> &sm, const float *__restrict__ w,
+                                             const float *__restrict__ q_scale, const IdxParams &P, const Group &G) {
+    for (int i = threadIdx.x - EPI_WARP0 * 32; i < TOK * HI; i += (num_threads<FP8>() - EPI_WARP0 * 32)) {
+        const int tt = i / HI, h = i % HI;
+        float v = 0.0f;
+        if (tt < G.ntok) {
+            const int64_t qi = (int64_t)(G.r0 + tt) * HI + h;
+            v = w[qi] * P.c * (FP8 ? q_scale[qi] : 1.0f);
+        }
+        sm.wsm()[i] = v;
+    }
+}
+
+// The scores of `mine` key blocks of group G (blocks split, split + splits, ...): the TMA producer
+// (warp 0), the MMA issuer (warp 1) and the epilogue (warps EPI_WARP0..), which writes row tt of the
+// group to out_base + tt * P.ld.
+template <bool FP8>
+__device__ __forceinline__ void group_pipeline(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                                               const float *__restrict__ k_scale, const IdxParams &P,
+                                               const Group &G, int split, int splits, int mine, float *out_base,
+                                               const Smem<FP8> &sm, uint32_t tmem, const Phases &ph,
+                                               volatile int *never) {
+    using C = Cfg<FP8>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abort_flag = sm.abort_flag();
+    if (mine <= 0) return;
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        tc::prefetch_tmap(tm_q);
+        tc::prefetch_tmap(tm_k);
+        tc::mbar_arrive_expect_tx(sm.bfull(), C::B_BYTES);
+        for (int h = 0; h < C::HALVES; ++h) tc::tma_load_2d(sm.Bt() + h * C::B_HALF, tm_q, sm.bfull(), h * 64, G.r0 * HI);
+        int issued = 0;
+        for (int i = 0; i < mine; ++i) {
+            const int it = ph.it + i, st = it % C::STAGES;
+            if (!tc::mbar_wait(sm.empty(st), ((it / C::STAGES) & 1) ^ 1, abort_flag, &g_indexer_tc_error, 1,
+                               P.wait_limit))
+                break;
+            const int row = G.kbase + (split + i * splits) * BM;
+            tc::mbar_arrive_expect_tx(sm.full(st), C::A_BYTES);
+            for (int h = 0; h < C::HALVES; ++h)
+                tc::tma_load_2d(sm.As() + st * C::A_BYTES + h * C::A_HALF, tm_k, sm.full(st), h * 64, row);
+            ++issued;
+        }
+        // Drain: the last loads of each stage must have landed before the CTA exits.
+        tc::mbar_wait(sm.bfull(), ph.nq & 1, never, &g_indexer_tc_error, 2);
+        for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
+            const int it = ph.it + j;
+            tc::mbar_wait(sm.full(it % C::STAGES), (it / C::STAGES) & 1, never, &g_indexer_tc_error, 3);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        bool ok = tc::mbar_wait(sm.bfull(), ph.nq & 1, abort_flag, &g_indexer_tc_error, 4, P.wait_limit);
+        // Only the group's valid tokens are multiplied: N = 64 heads x ntok.
+        const uint32_t idesc = FP8 ? tc::instr_desc(tc::kFmtE4M3, tc::kFmtE4M3, BM, HI * G.ntok, 0, 0)
+                                   : tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, BM, HI * G.ntok, 0, 0);
+        int issued = 0;
+        for (int i = 0; ok && i < mine; ++i) {
+            const int it = ph.it + i, st = it % C::STAGES, a = ph.ai + i, acc = a & 1;
+            if (!tc::mbar_wait(sm.tempty(acc), ((a >> 1) & 1) ^ 1, abort_flag, &g_indexer_tc_error, 5, P.wait_limit))
+                break;
+            if (!tc::mbar_wait(sm.full(st), (it / C::STAGES) & 1, abort_flag, &g_indexer_tc_error, 6, P.wait_limit))
+                break;
+            tc::tc_fence_after();
+            const uint32_t d = tmem + acc * BN;
+            const uint32_t a0 = tc::smem_u32(sm.As() + st * C::A_BYTES), b0 = tc::smem_u32(sm.Bt());
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                // 32 bytes of K per step: 16 bf16 or 32 e4m3 values.
+                const int slab = FP8 ? 0 : kk / 4, off = (FP8 ? kk : kk % 4) * 32;
+                const uint64_t ad = tc::smem_desc(a0 + slab * C::A_HALF + off, 16, 1024);
+                const uint64_t bd = tc::smem_desc(b0 + slab * C::B_HALF + off, 16, 1024);
+                if (FP8) tc::mma_f8(d, ad, bd, idesc, kk > 0);
+                else tc::mma_f16(d, ad, bd, idesc, kk > 0);
+            }
+            tc::mma_commit(sm.empty(st));
+            tc::mma_commit(sm.tfull(acc));
+            ++issued;
+        }
+        // No MMA may still be running when the tensor memory is released (or the ring reused).
+        if (issued > 0) {
+            tc::mma_commit(sm.mmadone());
+            tc::mbar_wait(sm.mmadone(), ph.md & 1, never, &g_indexer_tc_error, 7);
+        }
+    } else if (warp >= EPI_WARP0) {
+        // ---------------- epilogue ----------------
+        // bf16: warp (q, tt) reduces token tt for the keys of lane quarter q.  FP8: the two
+        // warps of lane quarter q take tokens hf and hf + 2.  Absent tokens are skipped.
+        const int q = warp & 3, t_first = (warp - EPI_WARP0) >> 2, t_step = FP8 ? 2 : 4;
+        for (int i = 0; i < mine; ++i) {
+            const int a = ph.ai + i, acc = a & 1;
+            if (!tc::mbar_wait(sm.tfull(acc), (a >> 1) & 1, abort_flag, &g_indexer_tc_error, 8, P.wait_limit)) break;
+            tc::tc_fence_after();
+            const int key = (split + i * splits) * BM + q * 32 + lane;
+            const float ks = (FP8 && key < G.S) ? k_scale[G.kbase + key] : 1.0f;
+#pragma unroll 1
+            for (int tt = t_first; tt < G.ntok; tt += t_step) {
+                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + tt * HI;
+                float v0[32], v1[32];
+                tc::tmem_ld32(taddr, v0);
+                tc::tmem_ld32(taddr + 32, v1);
+                tc::tmem_ld_wait();
+                if (!FP8) {  // bf16: one token per warp, so the accumulator can go back at once
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(sm.tempty(acc));
+                }
+                const float4 *wv = (const float4 *)(sm.wsm() + tt * HI);
+                float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+                for (int h4 = 0; h4 < 8; ++h4) {
+                    const float4 a4 = wv[h4], c4 = wv[8 + h4];
+                    s0 = fmaf(a4.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
+                    s1 = fmaf(c4.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
+                    s0 = fmaf(a4.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
+                    s1 = fmaf(c4.y, fmaxf(v1[4 * h4 + 1], 0.0f), s1);
+                    s0 = fmaf(a4.z, fmaxf(v0[4 * h4 + 2], 0.0f), s0);
+                    s1 = fmaf(c4.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
+                    s0 = fmaf(a4.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
+                    s1 = fmaf(c4.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
+                }
+                if (key < G.S)
+                    out_base[(int64_t)tt * P.ld + key] = (key <= G.p0 + tt) ? (s0 + s1) * ks : -INFINITY;
+            }
+            if (FP8 || t_first >= G.ntok) {
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(sm.tempty(acc));
+            }
+        }
+    }
+}
 
 template <bool FP8>
 __global__ void __launch_bounds__(num_threads<FP8>(), 1)
@@ -88,20 +302,11 @@ __global__ void __launch_bounds__(num_threads<FP8>(), 1)
                       const float *__restrict__ w, const float *__restrict__ q_scale,
                       const float *__restrict__ k_scale, const __grid_constant__ IdxParams P,
                       float *__restrict__ scores) {
-    using C = Cfg<FP8>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *Bt = base;
-    uint8_t *As = Bt + C::B_BYTES;
-    float *wsm = (float *)(As + C::STAGES * C::A_BYTES);
-    uint64_t *bars = (uint64_t *)(wsm + TOK * HI);
-    uint64_t *full = bars, *empty = bars + C::STAGES, *bfull = bars + 2 * C::STAGES;
-    uint64_t *tfull = bfull + 1, *tempty = tfull + 2, *mmadone = tempty + 2;
-    uint32_t *tmem_slot = (uint32_t *)(mmadone + 1);
-    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+    const Smem<FP8> sm(smem_raw);
     __shared__ int never;  // an abort flag nobody raises, for the drain waits
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     // Heavier groups (later tokens of a sequence see more keys) start first.
     int g, split, splits;
     if (P.balanced) {
@@ -119,173 +324,116 @@ __global__ void __launch_bounds__(num_threads<FP8>(), 1)
         split = lin % P.splits;
         splits = P.splits;
     }
-    int b = 0;
-    {
-        int lo = 0, hi = P.B - 1;
-        while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
-            if (P.g_off[mid] <= g) lo = mid; else hi = mid - 1;
-        }
-        b = lo;
-    }
-    const int T_b = P.q_off[b + 1] - P.q_off[b];
-    const int t0 = (g - P.g_off[b]) * TOK;
-    const int ntok = min(TOK, T_b - t0);
-    const int r0 = P.q_off[b] + t0;
-    const int p0 = P.start_pos[b] + t0;
-    const int S = P.k_len[b], kbase = P.k_base[b];
-    const int nblk = (p0 + ntok - 1) / BM + 1;  // blocks holding keys 0 .. last position
+    const Group G = group_of(P, g);
     // A group whose last row sits at position < dense_k needs no scores: every row of it selects all
     // of its causal keys, and the top-k does not read them.
-    const bool dense = P.dense_k > 0 && p0 + ntok - 1 < P.dense_k;
-    const int mine = (split < nblk && !dense) ? (nblk - split + splits - 1) / splits : 0;
+    const bool dense = P.dense_k > 0 && G.p0 + G.ntok - 1 < P.dense_k;
+    const int mine = (split < G.nblk && !dense) ? (G.nblk - split + splits - 1) / splits : 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::STAGES; ++i) {
-            tc::mbar_init(&full[i], 1);
-            tc::mbar_init(&empty[i], 1);
-        }
-        tc::mbar_init(bfull, 1);
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&tfull[i], 1);
-            tc::mbar_init(&tempty[i], num_epi<FP8>());
-        }
-        tc::mbar_init(mmadone, 1);
-        *abort_flag = 0;
+        init_barriers(sm);
         never = 0;
-        tc::fence_mbar_init();
     }
     if (warp == 2) {
-        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_alloc(sm.tmem_slot(), 512);
         tc::tmem_relinquish();
     }
     pdl_wait();  // the set-up above overlapped the previous kernel; global memory only from here
-    if (warp >= EPI_WARP0) {
-        for (int i = threadIdx.x - EPI_WARP0 * 32; i < TOK * HI; i += (num_threads<FP8>() - EPI_WARP0 * 32)) {
-            const int tt = i / HI, h = i % HI;
-            float v = 0.0f;
-            if (tt < ntok) {
-                const int64_t qi = (int64_t)(r0 + tt) * HI + h;
-                v = w[qi] * P.c * (FP8 ? q_scale[qi] : 1.0f);
-            }
-            wsm[i] = v;
-        }
-    }
+    if (warp >= EPI_WARP0) load_weights(sm, w, q_scale, P, G);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    if (mine > 0) {
-        if (warp == 0 && lane == 0) {
-            // ---------------- TMA producer ----------------
-            tc::prefetch_tmap(&tm_q);
-            tc::prefetch_tmap(&tm_k);
-            tc::mbar_arrive_expect_tx(bfull, C::B_BYTES);
-            for (int h = 0; h < C::HALVES; ++h) tc::tma_load_2d(Bt + h * C::B_HALF, &tm_q, bfull, h * 64, r0 * HI);
-            int issued = 0;
-            for (int i = 0; i < mine; ++i) {
-                const int st = i % C::STAGES;
-                if (!tc::mbar_wait(&empty[st], ((i / C::STAGES) & 1) ^ 1, abort_flag, &g_indexer_tc_error, 1)) break;
-                const int row = kbase + (split + i * splits) * BM;
-                tc::mbar_arrive_expect_tx(&full[st], C::A_BYTES);
-                for (int h = 0; h < C::HALVES; ++h)
-                    tc::tma_load_2d(As + st * C::A_BYTES + h * C::A_HALF, &tm_k, &full[st], h * 64, row);
-                ++issued;
-            }
-            // Drain: the last loads of each stage must have landed before the CTA exits.
-            tc::mbar_wait(bfull, 0, (volatile int *)&never, &g_indexer_tc_error, 2);
-            for (int j = max(0, issued - C::STAGES); j < issued; ++j)
-                tc::mbar_wait(&full[j % C::STAGES], (j / C::STAGES) & 1, (volatile int *)&never, &g_indexer_tc_error, 3);
-        } else if (warp == 1 && lane == 0) {
-            // ---------------- MMA issuer ----------------
-            bool ok = tc::mbar_wait(bfull, 0, abort_flag, &g_indexer_tc_error, 4);
-            // Only the group's valid tokens are multiplied: N = 64 heads x ntok.
-            const uint32_t idesc = FP8 ? tc::instr_desc(tc::kFmtE4M3, tc::kFmtE4M3, BM, HI * ntok, 0, 0)
-                                       : tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, BM, HI * ntok, 0, 0);
-            int issued = 0;
-            for (int i = 0; ok && i < mine; ++i) {
-                const int st = i % C::STAGES, acc = i & 1;
-                if (!tc::mbar_wait(&tempty[acc], ((i >> 1) & 1) ^ 1, abort_flag, &g_indexer_tc_error, 5)) break;
-                if (!tc::mbar_wait(&full[st], (i / C::STAGES) & 1, abort_flag, &g_indexer_tc_error, 6)) break;
-                tc::tc_fence_after();
-                const uint32_t d = tmem + acc * BN;
-                const uint32_t a0 = tc::smem_u32(As + st * C::A_BYTES), b0 = tc::smem_u32(Bt);
-#pragma unroll
-                for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                    // 32 bytes of K per step: 16 bf16 or 32 e4m3 values.
-                    const int slab = FP8 ? 0 : kk / 4, off = (FP8 ? kk : kk % 4) * 32;
-                    const uint64_t ad = tc::smem_desc(a0 + slab * C::A_HALF + off, 16, 1024);
-                    const uint64_t bd = tc::smem_desc(b0 + slab * C::B_HALF + off, 16, 1024);
-                    if (FP8) tc::mma_f8(d, ad, bd, idesc, kk > 0);
-                    else tc::mma_f16(d, ad, bd, idesc, kk > 0);
-                }
-                tc::mma_commit(&empty[st]);
-                tc::mma_commit(&tfull[acc]);
-                ++issued;
-            }
-            // No MMA may still be running when the tensor memory is released.
-            if (issued > 0) {
-                tc::mma_commit(mmadone);
-                tc::mbar_wait(mmadone, 0, (volatile int *)&never, &g_indexer_tc_error, 7);
-            }
-        } else if (warp >= EPI_WARP0) {
-            // ---------------- epilogue ----------------
-            // bf16: warp (q, tt) reduces token tt for the keys of lane quarter q.  FP8: the two
-            // warps of lane quarter q take tokens hf and hf + 2.  Absent tokens are skipped.
-            const int q = warp & 3, t_first = (warp - EPI_WARP0) >> 2, t_step = FP8 ? 2 : 4;
-            float *out_base = scores + (int64_t)r0 * P.ld;
-            for (int i = 0; i < mine; ++i) {
-                const int acc = i & 1;
-                if (!tc::mbar_wait(&tfull[acc], (i >> 1) & 1, abort_flag, &g_indexer_tc_error, 8)) break;
-                tc::tc_fence_after();
-                const int key = (split + i * splits) * BM + q * 32 + lane;
-                const float ks = (FP8 && key < S) ? k_scale[kbase + key] : 1.0f;
-#pragma unroll 1
-                for (int tt = t_first; tt < ntok; tt += t_step) {
-                    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + tt * HI;
-                    float v0[32], v1[32];
-                    tc::tmem_ld32(taddr, v0);
-                    tc::tmem_ld32(taddr + 32, v1);
-                    tc::tmem_ld_wait();
-                    if (!FP8) {  // bf16: one token per warp, so the accumulator can go back at once
-                        tc::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&tempty[acc]);
-                    }
-                    const float4 *wv = (const float4 *)(wsm + tt * HI);
-                    float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-                    for (int h4 = 0; h4 < 8; ++h4) {
-                        const float4 a = wv[h4], c = wv[8 + h4];
-                        s0 = fmaf(a.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
-                        s1 = fmaf(c.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
-                        s0 = fmaf(a.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
-                        s1 = fmaf(c.y, fmaxf(v1[4 * h4 + 1], 0.0f), s1);
-                        s0 = fmaf(a.z, fmaxf(v0[4 * h4 + 2], 0.0f), s0);
-                        s1 = fmaf(c.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
-                        s0 = fmaf(a.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
-                        s1 = fmaf(c.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
-                    }
-                    if (key < S) out_base[(int64_t)tt * P.ld + key] = (key <= p0 + tt) ? (s0 + s1) * ks : -INFINITY;
-                }
-                if (FP8 || t_first >= ntok) {
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&tempty[acc]);
-                }
-            }
-        }
-    }
+    const uint32_t tmem = *sm.tmem_slot();
+    group_pipeline<FP8>(&tm_q, &tm_k, k_scale, P, G, split, splits, mine, scores + (int64_t)G.r0 * P.ld, sm, tmem,
+                        Phases(), (volatile int *)&never);
     __syncthreads();
     pdl_trigger();
     // Masked tail: keys past every computed block are future keys of all rows.
     if (P.fill_future && split == 0 && warp >= EPI_WARP0) {
-        const int start = nblk * BM;
-        for (int tt = 0; tt < ntok; ++tt)
-            for (int s = start + threadIdx.x - EPI_WARP0 * 32; s < S; s += num_threads<FP8>() - EPI_WARP0 * 32)
-                scores[(int64_t)(r0 + tt) * P.ld + s] = -INFINITY;
+        const int start = G.nblk * BM;
+        for (int tt = 0; tt < G.ntok; ++tt)
+            for (int s = start + threadIdx.x - EPI_WARP0 * 32; s < G.S; s += num_threads<FP8>() - EPI_WARP0 * 32)
+                scores[(int64_t)(G.r0 + tt) * P.ld + s] = -INFINITY;
     }
+    if (warp == 2) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// The indexer and the top-k fused: a persistent CTA per SM takes query groups heaviest first (in a
+// snake order over the CTAs, so the loads balance), computes a group's scores into its own slot of
+// 4 score rows (slots: [gridDim.x][4][P.ld] fp32, reused group after group, so they stay in L2),
+// then its epilogue warps select each row's top-k from the slot -- reading it back from L2 -- and
+// write the row's indices to idx [rows, P.topk].  No [rows, S] score buffer exists.  The key-block
+// ring and the query tile are free while the selection runs, so its histogram and candidate list
+// live there.  Groups whose rows all see at most k keys skip the MMAs and write their dense
+// selection (0 .. n-1, then -1).
+template <bool FP8>
+__global__ void __launch_bounds__(num_threads<FP8>(), 1)
+    indexer_topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const float *__restrict__ w, const float *__restrict__ q_scale,
+                        const float *__restrict__ k_scale, const __grid_constant__ IdxParams P,
+                        float *__restrict__ slots, int32_t *__restrict__ idx) {
+    using C = Cfg<FP8>;
+    constexpr int NT = num_threads<FP8>() - EPI_WARP0 * 32;  // the selecting threads (the epilogue warps)
+    static_assert(tk::MAX_BINS % NT == 0, "the bin scan gives each thread the same number of bins");
+    static_assert(16384 + 2 * 8192 * 4 <= C::B_BYTES + C::STAGES * C::A_BYTES, "selection scratch in the ring");
+    extern __shared__ uint8_t smem_raw[];
+    const Smem<FP8> sm(smem_raw);
+    __shared__ int never;
+
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        init_barriers(sm);
+        never = 0;
+    }
+    if (warp == 2) {
+        tc::tmem_alloc(sm.tmem_slot(), 512);
+        tc::tmem_relinquish();
+    }
+    pdl_wait();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *sm.tmem_slot();
+    float *slot = slots + (int64_t)blockIdx.x * TOK * P.ld;
+    // selection scratch over the query tile and the ring: histogram, warp sums, candidates
+    uint8_t *scratch = sm.Bt();
+    const tk::FilterSmem fs{(uint32_t *)scratch, (int *)(scratch + 8192), (int *)(scratch + 8192 + 256),
+                            (int *)(scratch + 8192 + 512), (uint32_t *)(scratch + 16384),
+                            (int32_t *)(scratch + 16384 + 8192 * 4), 8192};
+    Phases ph;
+    const int G_ = (int)gridDim.x;
+    for (int j = 0;; ++j) {
+        const int pos = j * G_ + ((j & 1) ? G_ - 1 - (int)blockIdx.x : (int)blockIdx.x);
+        if (pos >= P.total_groups) break;
+        const Group G = group_of(P, P.total_groups - 1 - pos);
+        const bool dense = G.p0 + G.ntok - 1 < P.topk;
+        const int mine = dense ? 0 : G.nblk;
+        if (warp >= EPI_WARP0 && !dense) load_weights(sm, w, q_scale, P, G);
+        tc::tc_fence_before();
+        __syncthreads();
+        tc::tc_fence_after();
+        group_pipeline<FP8>(&tm_q, &tm_k, k_scale, P, G, 0, 1, mine, slot, sm, tmem, ph, (volatile int *)&never);
+        tc::tc_fence_before();
+        __syncthreads();  // the slot's rows are written; every MMA and load of the group is done
+        if (*sm.abort_flag()) break;
+        if (warp >= EPI_WARP0) {
+            const int tid = (int)threadIdx.x - EPI_WARP0 * 32;
+            for (int tt = 0; tt < G.ntok; ++tt) {
+                const int n_live = min(G.p0 + tt + 1, G.S);
+                tk::filter_row<NT, 2, false, FP8 ? 16 : 8>(tid, slot + (int64_t)tt * P.ld, n_live, P.topk, true,
+                                             idx + (int64_t)(G.r0 + tt) * P.topk, fs);
+            }
+            // the next group's TMA loads (async proxy) overwrite the scratch these threads used
+            tc::fence_proxy_async_smem();
+        }
+        ph.advance(mine);
+        __syncthreads();
+    }
+    __syncthreads();
+    pdl_trigger();
     if (warp == 2) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, 512);
@@ -311,11 +459,10 @@ int indexer_tc_read_error(int *site) {
     return DSA_OK;
 }
 
-cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k, const float *k_scale, int dtype,
-                              const float *w, const SeqTab &st, int64_t total_k, float *scores, int64_t ld,
-                              bool fill_future, cudaStream_t s, int dense_k) {
-    const bool fp8 = dtype == DSA_E4M3;
-    static thread_local IdxParams P;  // ~10 KB: keep it off the host stack
+namespace {
+
+// The per-launch table of groups.  Returns the number of groups.
+unsigned fill_params(IdxParams &P, const SeqTab &st) {
     P.B = st.B;
     P.g_off[0] = 0;
     for (int i = 0; i < st.B; ++i) {
@@ -328,11 +475,46 @@ cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k
     }
     P.q_off[st.B] = st.q_off[st.B];
     P.total_groups = P.g_off[st.B];
-    if (P.total_groups == 0) return cudaSuccess;
     P.splits = 1;
     P.balanced = 0;
     P.n_tab = 0;
-    unsigned grid = (unsigned)P.total_groups;
+    P.fill_future = 0;
+    P.dense_k = 0;
+    P.topk = 0;
+    P.wait_limit = wait_limit_cycles();
+    P.c = 1.0f / sqrtf((float)(HI * DI));
+    return (unsigned)P.total_groups;
+}
+
+bool make_maps(CUtensorMap &tq, CUtensorMap &tk, const void *q, const void *k, bool fp8, int total_q,
+               int64_t total_k) {
+    const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t row_bytes = (uint64_t)DI * (fp8 ? 1 : 2);
+    const uint32_t inner = fp8 ? 128 : 64;
+    {
+        uint64_t dims[2] = {(uint64_t)DI, (uint64_t)total_q * HI};
+        uint64_t strides[1] = {row_bytes};
+        uint32_t box[2] = {inner, (uint32_t)BN};
+        if (!make_tmap(&tq, ty, 2, q, dims, strides, box)) return false;
+    }
+    {
+        uint64_t dims[2] = {(uint64_t)DI, (uint64_t)std::max<int64_t>(total_k, 1)};
+        uint64_t strides[1] = {row_bytes};
+        uint32_t box[2] = {inner, (uint32_t)BM};
+        if (!make_tmap(&tk, ty, 2, k, dims, strides, box)) return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k, const float *k_scale, int dtype,
+                              const float *w, const SeqTab &st, int64_t total_k, float *scores, int64_t ld,
+                              bool fill_future, cudaStream_t s, int dense_k) {
+    const bool fp8 = dtype == DSA_E4M3;
+    static thread_local IdxParams P;  // ~10 KB: keep it off the host stack
+    unsigned grid = fill_params(P, st);
+    if (grid == 0) return cudaSuccess;
     if (P.total_groups < SPLIT_TAB) {
         // Few groups of (possibly very) different lengths: about SPLIT_TAB CTAs of `target` key
         // blocks each, so that no CTA carries a long row's blocks alone.
@@ -365,25 +547,9 @@ cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k
     P.fill_future = fill_future ? 1 : 0;
     P.dense_k = dense_k;
     P.ld = ld;
-    P.c = 1.0f / sqrtf((float)(HI * DI));
 
-    const int total_q = st.q_off[st.B];
     CUtensorMap tq, tk;
-    const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const uint64_t row_bytes = (uint64_t)DI * (fp8 ? 1 : 2);
-    const uint32_t inner = fp8 ? 128 : 64;
-    {
-        uint64_t dims[2] = {(uint64_t)DI, (uint64_t)total_q * HI};
-        uint64_t strides[1] = {row_bytes};
-        uint32_t box[2] = {inner, (uint32_t)BN};
-        if (!make_tmap(&tq, ty, 2, q, dims, strides, box)) return cudaErrorInvalidValue;
-    }
-    {
-        uint64_t dims[2] = {(uint64_t)DI, (uint64_t)std::max<int64_t>(total_k, 1)};
-        uint64_t strides[1] = {row_bytes};
-        uint32_t box[2] = {inner, (uint32_t)BM};
-        if (!make_tmap(&tk, ty, 2, k, dims, strides, box)) return cudaErrorInvalidValue;
-    }
+    if (!make_maps(tq, tk, q, k, fp8, st.q_off[st.B], total_k)) return cudaErrorInvalidValue;
     cudaError_t e;
     if (fp8) {
         e = cudaFuncSetAttribute(indexer_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<true>::SMEM);
@@ -404,4 +570,63 @@ cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k
     return cudaGetLastError();
 }
 
+int indexer_topk_groups(const SeqTab &st) {
+    int g = 0;
+    for (int b = 0; b < st.B; ++b) g += (st.q_off[b + 1] - st.q_off[b] + TOK - 1) / TOK;
+    return g;
+}
+
+std::atomic<int> g_fused_topk{0};
+
+bool indexer_topk_fused_ok(int dtype, int H_I, int D_I, const SeqTab &st, int k) {
+    // Switched on, enough groups to fill the GPU (few groups -- decode -- split each group's key
+    // blocks over many CTAs instead, and select afterwards), and candidate lists that fit the scratch.
+    return g_fused_topk.load(std::memory_order_relaxed) != 0 && indexer_tc_supported(dtype, H_I, D_I) &&
+           indexer_topk_groups(st) >= SPLIT_TAB && k <= 8192;
+}
+
+size_t indexer_topk_slot_bytes(const SeqTab &st, int64_t ld) {
+    const int grid = std::min(indexer_topk_groups(st), device_sm_count());
+    return (size_t)grid * TOK * ld * sizeof(float);
+}
+
+cudaError_t launch_indexer_topk_tc(const void *q, const float *q_scale, const void *k, const float *k_scale, int dtype,
+                                   const float *w, const SeqTab &st, int64_t total_k, float *slots, int64_t ld,
+                                   int topk, int32_t *idx, cudaStream_t s) {
+    const bool fp8 = dtype == DSA_E4M3;
+    static thread_local IdxParams P;
+    const unsigned groups = fill_params(P, st);
+    if (groups == 0) return cudaSuccess;
+    P.ld = ld;
+    P.topk = topk;
+    P.dense_k = topk;
+    const unsigned grid = std::min<unsigned>(groups, (unsigned)device_sm_count());
+    CUtensorMap tq, tk;
+    if (!make_maps(tq, tk, q, k, fp8, st.q_off[st.B], total_k)) return cudaErrorInvalidValue;
+    cudaError_t e;
+    if (fp8) {
+        e = cudaFuncSetAttribute(indexer_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg<true>::SMEM);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(indexer_topk_kernel<true>, dim3(grid), dim3(num_threads<true>()), Cfg<true>::SMEM, s, tq, tk, w,
+                       q_scale, k_scale, P, slots, idx);
+        if (e != cudaSuccess) return e;
+        note_launch(DSA_KERNEL_INDEXER_FP8 | DSA_KERNEL_INDEXER_TOPK);
+    } else {
+        e = cudaFuncSetAttribute(indexer_topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg<false>::SMEM);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(indexer_topk_kernel<false>, dim3(grid), dim3(num_threads<false>()), Cfg<false>::SMEM, s, tq,
+                       tk, w, (const float *)nullptr, (const float *)nullptr, P, slots, idx);
+        if (e != cudaSuccess) return e;
+        note_launch(DSA_KERNEL_INDEXER_TC | DSA_KERNEL_INDEXER_TOPK);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace dsa
+
+extern "C" int dsa_set_fused_topk(int on) {
+    dsa::g_fused_topk.store(on ? 1 : 0, std::memory_order_relaxed);
+    return DSA_OK;
+}

@@ -41,6 +41,7 @@
 // wave fills the GPU; each split writes a normalised partial context and its
 // lse, and a small combine kernel merges them.
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <algorithm>
 
@@ -81,6 +82,7 @@ constexpr uint32_t COL_S = 0, COL_Q = 128, COL_O = 256;
 constexpr uint32_t IDESC_QK = tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, NH, BK, 0, 0);
 constexpr uint32_t IDESC_PV = tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, NH, 256, 0, 1);
 constexpr float RESCALE_LOG2 = 8.0f;
+constexpr long long kAbortQuietCycles = 1LL << 18;  // ~130 us: the wait before the final cluster barrier after an abort
 constexpr float LN2 = 0.69314718055994530942f;
 
 struct MlaParams {
@@ -94,6 +96,7 @@ struct MlaParams {
     int splits;        // clusters per row
     int prefix_valid;  // rows list their min(k, p+1) keys first (the top-k output)
     float scale_log2;  // softmax scale * log2(e)
+    long long wait_limit;  // SM cycles a wait may take before the CTA gives up (the drains keep the default)
 };
 
 __device__ __forceinline__ int find_seq(const MlaParams &P, int r) {
@@ -113,9 +116,14 @@ struct Bars {
 };
 static_assert(sizeof(Bars) + 8 <= 320, "barrier area");
 
+// KV8: the latent rows are e4m3 codes (ld_kv in bytes) with one power-of-two (ue8m0) scale per 128
+// values (kv_scale [rows, d_c / 128] fp32); the gathering warps load and dequantise them into the same
+// bf16 stage layout (e4m3 times a power of two is exact in bf16).  Otherwise the rows are bf16.
+template <bool KV8>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most 4 per SM sub-partition x 128 regs
     mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
-                  const __nv_bfloat16 *__restrict__ kv, int64_t ld_kv, const __nv_bfloat16 *__restrict__ kpe,
+                  const void *__restrict__ kv_rows, int64_t ld_kv, const float *__restrict__ kv_scale,
+                  const __nv_bfloat16 *__restrict__ kpe,
                   int64_t ld_pe, const __nv_bfloat16 *__restrict__ qt, const __nv_bfloat16 *__restrict__ qpe,
                   const int32_t *__restrict__ idx,
                   const __grid_constant__ MlaParams P, __nv_bfloat16 *__restrict__ olat, float *__restrict__ lse,
@@ -218,20 +226,65 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         fetch(0);
         for (int i = 0; i < n; ++i) {
             const int st = i % NSTAGE;
-            if (!tc::mbar_wait(&bar->kv_empty[st], ((i / NSTAGE) & 1) ^ 1, abort_flag, err, 21)) break;
+            if (!tc::mbar_wait(&bar->kv_empty[st], ((i / NSTAGE) & 1) ^ 1, abort_flag, err, 21, P.wait_limit)) break;
+            if constexpr (KV8) {
+                // Codes: thread c loads bytes 8c .. 8c+7 of each 64-value slab (the same columns its 16-byte
+                // chunk of the bf16 layout holds), every pass's loads issued before the first is used.
+                const uint8_t *kv8 = (const uint8_t *)kv_rows;
+                uint2 code[PASSES][NSLAB];
+                float scl[PASSES][2];
 #pragma unroll
-            for (int ps = 0; ps < PASSES; ++ps) {
-                const int j = ps * NPROD * 4 + jr;
-                const int64_t row = kbase + (rows[ps] >= 0 ? rows[ps] : 0);
-                const __nv_bfloat16 *lat = kv + row * ld_kv + rank * 256 + c * 8;
-                const uint32_t dst = kv_s + st * KV_STAGE + j * 128 + ((c ^ (j & 7)) << 4);
+                for (int ps = 0; ps < PASSES; ++ps) {
+                    const int64_t row = kbase + (rows[ps] >= 0 ? rows[ps] : 0);
+                    const uint8_t *lat = kv8 + row * ld_kv + rank * 256 + c * 8;
 #pragma unroll
-                for (int js = 0; js < NSLAB; ++js) tc::cp_async16(dst + js * SLAB_K, lat + js * 64);
-                // rope half: 64-byte rows, chunk c of row j at c ^ ((j >> 1) & 3)
-                if (c < 4)
-                    tc::cp_async16(kv_s + st * KV_STAGE + NSLAB * SLAB_K + j * 64 + ((c ^ ((j >> 1) & 3)) << 4),
-                                   kpe + row * ld_pe + rank * 32 + c * 8);
-                if (c == 0) kvalid[st * BK + j] = rows[ps] >= 0 ? 1 : 0;
+                    for (int js = 0; js < NSLAB; ++js) code[ps][js] = __ldg((const uint2 *)(lat + js * 64));
+                    scl[ps][0] = __ldg(kv_scale + row * (DC / 128) + rank * 2);
+                    scl[ps][1] = __ldg(kv_scale + row * (DC / 128) + rank * 2 + 1);
+                }
+#pragma unroll
+                for (int ps = 0; ps < PASSES; ++ps) {
+                    const int j = ps * NPROD * 4 + jr;
+                    const int64_t row = kbase + (rows[ps] >= 0 ? rows[ps] : 0);
+                    const uint32_t dst = kv_s + st * KV_STAGE + j * 128 + ((c ^ (j & 7)) << 4);
+#pragma unroll
+                    for (int js = 0; js < NSLAB; ++js) {
+                        const float sc = scl[ps][js >> 1];  // slabs 0, 1: block 2 * rank; 2, 3: block 2 * rank + 1
+                        const uint32_t wd[2] = {code[ps][js].x, code[ps][js].y};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int h2 = 0; h2 < 4; ++h2) {
+                            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                                (__nv_fp8x2_storage_t)((wd[h2 >> 1] >> (16 * (h2 & 1))) & 0xffffu), __NV_E4M3);
+                            const float2 f = __half22float2(*(const __half2 *)&hr);
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+                            o[h2] = *(const uint32_t *)&b2;
+                        }
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + js * SLAB_K), "r"(o[0]),
+                                     "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                     : "memory");
+                    }
+                    if (c < 4)
+                        tc::cp_async16(kv_s + st * KV_STAGE + NSLAB * SLAB_K + j * 64 + ((c ^ ((j >> 1) & 3)) << 4),
+                                       kpe + row * ld_pe + rank * 32 + c * 8);
+                    if (c == 0) kvalid[st * BK + j] = rows[ps] >= 0 ? 1 : 0;
+                }
+            } else {
+                const __nv_bfloat16 *kv = (const __nv_bfloat16 *)kv_rows;
+#pragma unroll
+                for (int ps = 0; ps < PASSES; ++ps) {
+                    const int j = ps * NPROD * 4 + jr;
+                    const int64_t row = kbase + (rows[ps] >= 0 ? rows[ps] : 0);
+                    const __nv_bfloat16 *lat = kv + row * ld_kv + rank * 256 + c * 8;
+                    const uint32_t dst = kv_s + st * KV_STAGE + j * 128 + ((c ^ (j & 7)) << 4);
+#pragma unroll
+                    for (int js = 0; js < NSLAB; ++js) tc::cp_async16(dst + js * SLAB_K, lat + js * 64);
+                    // rope half: 64-byte rows, chunk c of row j at c ^ ((j >> 1) & 3)
+                    if (c < 4)
+                        tc::cp_async16(kv_s + st * KV_STAGE + NSLAB * SLAB_K + j * 64 + ((c ^ ((j >> 1) & 3)) << 4),
+                                       kpe + row * ld_pe + rank * 32 + c * 8);
+                    if (c == 0) kvalid[st * BK + j] = rows[ps] >= 0 ? 1 : 0;
+                }
             }
             tc::cp_async_arrive_noinc(&bar->kv_full[st]);  // arrives when this thread's copies have landed
             tc::mbar_arrive(&bar->kv_full[st]);            // releases the mask bytes
@@ -243,12 +296,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         // QK^T(j) needs tile j gathered and its score buffer (j & 1) read by the group of tile j-2.
         // The PV products come from another thread (warp 2): an MMA issue blocks while the tensor
         // pipe is busy, so one thread for both streams would hold each up behind the other.
-        bool ok = tc::mbar_wait(&bar->q_ready, 0, abort_flag, err, 24);
+        bool ok = tc::mbar_wait(&bar->q_ready, 0, abort_flag, err, 24, P.wait_limit);
         const uint32_t kv0 = tc::smem_u32(KV), qr0 = tc::smem_u32(QR);
         for (int j = 0; ok && j < n; ++j) {
             const int st = j % NSTAGE;
-            if (j >= 2 && !(ok = tc::mbar_wait(&bar->s_empty[j & 1], ((j >> 1) - 1) & 1, abort_flag, err, 26))) break;
-            if (!(ok = tc::mbar_wait(&bar->kv_full[st], (j / NSTAGE) & 1, abort_flag, err, 25))) break;
+            if (j >= 2 && !(ok = tc::mbar_wait(&bar->s_empty[j & 1], ((j >> 1) - 1) & 1, abort_flag, err, 26, P.wait_limit))) break;
+            if (!(ok = tc::mbar_wait(&bar->kv_full[st], (j / NSTAGE) & 1, abort_flag, err, 25, P.wait_limit))) break;
             // the gathered rows were written by cp.async (generic proxy); the MMA reads them through
             // the async proxy
             tc::fence_proxy_async_smem();
@@ -282,7 +335,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         const uint32_t kv0 = tc::smem_u32(KV), x0 = tc::smem_u32(X);
         const uint16_t peer_mask = (uint16_t)(1u << peer);
         for (int j = 0; j < n; ++j) {
-            if (!tc::mbar_wait(&bar->p_full[j & 1], (j >> 1) & 1, abort_flag, err, 27)) break;
+            if (!tc::mbar_wait(&bar->p_full[j & 1], (j >> 1) & 1, abort_flag, err, 27, P.wait_limit)) break;
             tc::tc_fence_after();
             const int st = j % NSTAGE;
             const uint32_t pa = x0 + (j & 1) * X_BYTES;
@@ -300,6 +353,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         }
         tc::mma_commit(&bar->o_done);
         tc::mbar_wait(&bar->o_done, 0, nv, err, 28);
+        // The q~ staging load this thread issued must have landed before the CTA exits (after an
+        // abort nobody else may have waited for it).
+        tc::mbar_wait(&bar->q_stage, 0, nv, err, 29);
     } else if (warp >= 4 && warp < 12) {
         // ---------------- softmax: group g takes tiles g, g+2, ...; one thread per head row ----------------
         const int q = warp & 3, g = (warp - 4) >> 2, h = q * 32 + lane;
@@ -318,7 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
 #pragma unroll
                 for (int e = 0; e < 4; ++e) rq[e] = __ldg(rsrc + e);
             }
-            if (!tc::mbar_wait(&bar->q_stage, 0, abort_flag, err, 23)) done_ok = false;
+            if (!tc::mbar_wait(&bar->q_stage, 0, abort_flag, err, 23, P.wait_limit)) done_ok = false;
             if (done_ok) {
                 for (int js = g * 2; js < g * 2 + 2; ++js) {
                     const uint8_t *srow = X + js * Q_BOX + h * 128;
@@ -354,10 +410,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         const uint32_t hsw = (uint32_t)(h & 7);
         uint8_t *Xg = X + g * X_BYTES, *Yg = Y + g * X_BYTES;
         const int roff = h * 128, wblk = q * 32 * 128;  // this row; this warp's 32 rows (4 KB)
+        int sent = 0;  // tiles this group has copied into the peer's X[g]
         for (int t = g, k = 0; done_ok && t < n; t += 2, ++k) {
             const uint32_t ph = (uint32_t)k & 1u;
             // --- this CTA's partial scores of tile t -> fp16 of the log2-scaled values ---
-            if (!__all_sync(FULL, tc::mbar_wait(&bar->s_full[g], ph, abort_flag, err, 31))) { done_ok = false; break; }
+            if (!__all_sync(FULL, tc::mbar_wait(&bar->s_full[g], ph, abort_flag, err, 31, P.wait_limit))) { done_ok = false; break; }
             tc::tc_fence_after();
             uint32_t cur[32];
             {
@@ -378,7 +435,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             if (q == 0 && lane == 0) tc::mbar_arrive_expect_tx(&bar->xfull[g], X_BYTES);
             // Y[g] may be rewritten once the peer has received the group's previous tile from it (the
             // copy has then finished reading it).
-            if (k > 0 && !__all_sync(FULL, tc::mbar_wait_cluster(&bar->yfree[g], (k - 1) & 1, abort_flag, err, 38))) {
+            if (k > 0 && !__all_sync(FULL, tc::mbar_wait_cluster(&bar->yfree[g], (k - 1) & 1, abort_flag, err, 38, P.wait_limit))) {
                 done_ok = false;
                 break;
             }
@@ -389,12 +446,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             // The peer's X[g] is free once the peer has read its q~ staging (first tile of the group)
             // or its PV product of tile t-2 is done.
             bool ok = true;
-            if (lane == 0) ok = tc::mbar_wait_cluster(&bar->xempty[g], ph, abort_flag, err, 32);
+            if (lane == 0) ok = tc::mbar_wait_cluster(&bar->xempty[g], ph, abort_flag, err, 32, P.wait_limit);
             __syncwarp();
             if (!__shfl_sync(FULL, ok, 0)) { done_ok = false; break; }
             if (lane == 0)
                 tc::bulk_copy_to_peer(tc::map_peer(tc::smem_u32(Xg) + wblk, peer), Yg + wblk, 32 * 128,
                                       tc::map_peer(tc::smem_u32(&bar->xfull[g]), peer));
+            ++sent;
             // --- own half in fp32 and the mask (entries that are padding, future or outside the sequence),
             // while the peer's half is in flight ---
             float v[64];
@@ -404,7 +462,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
                 v[2 * j + 1] = tc::f16_to_f32((uint16_t)(cur[j] >> 16));
             }
             const int st = t % NSTAGE;
-            if (!__all_sync(FULL, tc::mbar_wait(&bar->kv_full[st], (t / NSTAGE) & 1, abort_flag, err, 34))) { done_ok = false; break; }
+            if (!__all_sync(FULL, tc::mbar_wait(&bar->kv_full[st], (t / NSTAGE) & 1, abort_flag, err, 34, P.wait_limit))) { done_ok = false; break; }
             {
                 const uint4 *kv4 = (const uint4 *)(kvalid + st * BK);
                 const uint4 m0 = kv4[0], m1 = kv4[1], m2 = kv4[2], m3 = kv4[3];
@@ -423,7 +481,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             }
             // --- + peer half, one rounding in fp32 (addition commutes: both CTAs get the same sum; a
             // masked entry stays -inf) ---
-            if (!__all_sync(FULL, tc::mbar_wait_cluster(&bar->xfull[g], ph, abort_flag, err, 33))) { done_ok = false; break; }
+            if (!__all_sync(FULL, tc::mbar_wait_cluster(&bar->xfull[g], ph, abort_flag, err, 33, P.wait_limit))) { done_ok = false; break; }
             // all four copies of the peer's half have landed: its Y[g] may be rewritten
             if (q == 0 && lane == 0) tc::mbar_arrive_remote(tc::map_peer(tc::smem_u32(&bar->yfree[g]), peer));
 #pragma unroll
@@ -451,7 +509,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             // --- running maximum: the one used for tile t-1 comes from the other group ---
             float m_prev = -INFINITY;
             if (t > 0) {
-                if (!__all_sync(FULL, tc::mbar_wait(&bar->hand[q][1 - g], ((t - 1) >> 1) & 1, abort_flag, err, 37))) {
+                if (!__all_sync(FULL, tc::mbar_wait(&bar->hand[q][1 - g], ((t - 1) >> 1) & 1, abort_flag, err, 37, P.wait_limit))) {
                     done_ok = false;
                     break;
                 }
@@ -494,7 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             // whole warp takes part when any of its rows moves (the others keep alpha = 1) ---
             if (__any_sync(FULL, rescale)) {
                 const float alpha = rescale ? tc::ex2_approx(m_prev - m_now) : 1.0f;
-                if (!__all_sync(FULL, tc::mbar_wait(&bar->p_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, err, 35))) {
+                if (!__all_sync(FULL, tc::mbar_wait(&bar->p_empty[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, err, 35, P.wait_limit))) {
                     done_ok = false;
                     break;
                 }
@@ -520,6 +578,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bar->p_full[g]);
         }
+        // The peer acknowledges every tile it has received (yfree); the acknowledgement of the last
+        // tile this group sent says that none of its copies is still landing in the peer's shared
+        // memory.  (A peer that aborted sends none: the wait then gives up, and the quiet period
+        // below covers the copies.)
+        if (sent > 0)
+            (void)__all_sync(FULL, tc::mbar_wait_cluster(&bar->yfree[g], (sent - 1) & 1, abort_flag, err, 40,
+                                                         P.wait_limit));
         // ---------------- epilogue: normalise and store this thread's 128 columns ----------------
         // The row sum of each group is relative to the last maximum that group used; the context is
         // relative to the last maximum of all (the running maximum never decreases).
@@ -531,7 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         const float lrow = (ma == -INFINITY ? 0.0f : la * tc::ex2_approx(ma - m_f)) +
                            (mb == -INFINITY ? 0.0f : lb * tc::ex2_approx(mb - m_f));
         const int64_t rh = (int64_t)r * NH + h;
-        const bool have = __all_sync(FULL, n > 0 && done_ok && tc::mbar_wait(&bar->o_done, 0, abort_flag, err, 36));
+        const bool have = __all_sync(FULL, n > 0 && done_ok && tc::mbar_wait(&bar->o_done, 0, abort_flag, err, 36, P.wait_limit));
         const float inv = (have && lrow > 0.0f) ? 1.0f / lrow : 0.0f;
         const float row_lse = (have && lrow > 0.0f) ? (m_f + log2f(lrow)) * LN2 : -INFINITY;
         if (have) tc::tc_fence_after();
@@ -587,6 +652,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(128)  // 14 warps: at most
         }
     }
     __syncthreads();
+    if (*abort_flag) {
+        // After an abort, a partial-score copy issued into the peer before its waits gave up may still
+        // be in flight, unacknowledged; such a copy lands within microseconds.  The CTA arrives at the
+        // cluster barrier (which lets the peer exit) only after a quiet period far longer than that.
+        const long long t0 = clock64();
+        while (clock64() - t0 < kAbortQuietCycles) {
+        }
+    }
     tc::cluster_sync();  // no DSMEM traffic may target a CTA that has exited
     if (warp == 2) {
         tc::tc_fence_after();
@@ -665,7 +738,8 @@ size_t mla_tc_partial_bytes(int M) {
 
 cudaError_t launch_mla_tc(const void *qt, const void *qpe, const void *kv, int64_t ld_kv, const void *kpe, int64_t ld_pe,
                           const int32_t *idx, int k, const SeqTab &st, int64_t total_k, int M, float scale,
-                          bool prefix_valid, void *olat, float *lse, void *part_ws, cudaStream_t s) {
+                          bool prefix_valid, void *olat, float *lse, void *part_ws, cudaStream_t s,
+                          const float *kv_scale) {
     if (M == 0) return cudaSuccess;
     static thread_local MlaParams P;
     P.B = st.B;
@@ -681,6 +755,7 @@ cudaError_t launch_mla_tc(const void *qt, const void *qpe, const void *kv, int64
     P.splits = mla_tc_splits(M);
     P.prefix_valid = prefix_valid ? 1 : 0;
     P.scale_log2 = scale * 1.4426950408889634f;
+    P.wait_limit = wait_limit_cycles();
     float *opart = nullptr, *lpart = nullptr;
     if (P.splits > 1) {
         opart = (float *)part_ws;
@@ -696,10 +771,11 @@ cudaError_t launch_mla_tc(const void *qt, const void *qpe, const void *kv, int64
         if (!make_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, qt, dims, strides, box)) return cudaErrorInvalidValue;
         if (!make_tmap(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, olat, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)M * P.splits * 2;
-    e = launch_pdl(mla_tc_kernel, dim3(grid), dim3(NUM_THREADS), SMEM, s, tq, to, (const __nv_bfloat16 *)kv, ld_kv,
+    auto kern = kv_scale ? mla_tc_kernel<true> : mla_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(kern, dim3(grid), dim3(NUM_THREADS), SMEM, s, tq, to, kv, ld_kv, kv_scale,
                    (const __nv_bfloat16 *)kpe, ld_pe, (const __nv_bfloat16 *)qt, (const __nv_bfloat16 *)qpe, idx, P,
                    (__nv_bfloat16 *)olat, lse, opart, lpart);
     if (e != cudaSuccess) return e;

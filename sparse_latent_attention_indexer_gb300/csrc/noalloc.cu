@@ -12,11 +12,18 @@
 // of scratch that the library reserves once per device.
 //
 // The scratch is a file-scope __device__ array.  In host code its name is
-// only a host-side stand-in for the symbol, not a device address, so the
-// device address is looked up with cudaGetSymbolAddress once per device,
-// with that device current, on the first call that runs on it, and cached.
-#include <mutex>
-
+// only a host-side stand-in for the symbol, not a device address, so every
+// call looks up the device address with cudaGetSymbolAddress, with the call's
+// device current.  Once the module is loaded on a device that lookup is a
+// host-side table read; looking it up per call (instead of caching it) keeps
+// the address right after the caller resets the device.
+//
+// When the array is reserved: it is part of this library's device code, which
+// CUDA loads on a device lazily by default -- at the first use of the module
+// there, i.e. the first call of this entry point on that device (a call with no
+// query rows does this set-up too and launches nothing).  A caller that hands
+// the rest of HBM to its own pool must make that first call before carving the
+// pool, or run with CUDA_MODULE_LOADING=EAGER (modules loaded with the context).
 #include "dsa_common.cuh"
 
 namespace dsa {
@@ -24,25 +31,12 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (set-up on the
-// first call per device).
+// Device address of the scratch array on the current device.
 int scratch_on_current_device(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return fail_cuda(e);
-    if (dev < 0 || dev >= kMaxDevices) return DSA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return fail_cuda(e);
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return DSA_OK;
 }
 
@@ -60,12 +54,13 @@ extern "C" int dsa_sparse_mla_fwd_noalloc(const void *q_nope, const void *q_pe, 
     Batch bt;
     int rc = validate_mla_call(q_nope, q_pe, dtype, kv_cache, ld_kv, k_pe, ld_pe, W_UK, W_UV, H, d_n, d_r, d_c, d_v,
                                idx, k, seqs, out, bt);
-    if (rc || bt.total_q == 0) return rc;
+    if (rc) return rc;
     // Every byte of the scratch that the attention reads is written earlier in
     // the same call, so nothing has to be cleared between calls.
     if (mla_workspace_bytes(H, d_c, bt.total_q) > (size_t)DSA_NOALLOC_SCRATCH_BYTES) return DSA_ERR_WORKSPACE;
     void *scratch = nullptr;
     if ((rc = scratch_on_current_device(&scratch))) return rc;
+    if (bt.total_q == 0) return DSA_OK;  // set-up only
     return run_mla(q_nope, q_pe, dtype, kv_cache, ld_kv, k_pe, ld_pe, W_UK, W_UV, H, d_n, d_r, d_c, d_v, idx, k, bt,
                    softmax_scale, out, lse, (char *)scratch, (cudaStream_t)stream);
 }

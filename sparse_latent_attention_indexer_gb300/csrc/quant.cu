@@ -15,17 +15,6 @@
 namespace dsa {
 namespace {
 
-// Smallest integer e with amax <= 448 * 2^e, clamped to the ue8m0 range.
-// With amax = m * 2^E, m in [0.5, 1) and 448 = 0.875 * 2^9: e = E - 9 when
-// m <= 0.875, else E - 8.  Exact for every finite fp32 amax.
-__device__ __forceinline__ int ue8m0_exponent(float amax) {
-    if (!(amax > 0.0f)) return 0;
-    int E;
-    float m = frexpf(amax, &E);
-    int e = (m <= 0.875f) ? E - 9 : E - 8;
-    return max(-127, min(127, e));
-}
-
 template <typename T>
 __global__ void __launch_bounds__(256) quant_e4m3_kernel(const T *__restrict__ x, int64_t n_blocks,
                                                          uint8_t *__restrict__ codes, float *__restrict__ scales) {

@@ -62,8 +62,8 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// About two seconds at the GB300's 2.07 GHz SM clock.
-constexpr long long kWaitLimitCycles = 4LL << 30;
+// About two seconds at the GB300's 2.07 GHz SM clock (the same value as kDefaultWaitLimitCycles).
+constexpr long long kWaitLimitCycles = kDefaultWaitLimitCycles;
 
 // Bounded wait on phase `parity` of `bar`.  Gives up (returns false) when the
 // CTA-wide abort flag is raised or after limit_cycles (default kWaitLimitCycles); in the second case
@@ -108,6 +108,12 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
                  "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -322,13 +328,13 @@ __device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t addr, uint32_
 }
 // Bounded wait that also acquires writes released at cluster scope.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                                  int *err_word, int site) {
+                                                  int *err_word, int site, long long limit_cycles = kWaitLimitCycles) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait_acq_cluster(a, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait_acq_cluster(a, parity)) {
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit_cycles) {
             atomicCAS(err_word, 0, site);
             *abort_flag = 1;
             return false;

@@ -22,12 +22,13 @@
 //     memory): 1024 threads per row, eight loads in flight per thread in the
 //     histogram passes, eight consecutive keys per thread in the ordered pass,
 //     the output row assembled in shared memory and written out coalesced.
-#include "dsa_common.cuh"
+#include "topk_row.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int MAX_BINS = 2048;
+using tk::MAX_BINS;
+using tk::SPT;
 
 // ---------------------------------------------------------------------------
 // Many rows (prefill): one CTA per row, two streaming passes over the row.
@@ -45,137 +46,6 @@ constexpr int MAX_BINS = 2048;
 constexpr int TF_THREADS = 256;
 constexpr int TF_WARPS = TF_THREADS / 32;
 constexpr int CAND_CAP = 8192;  // candidates per row kept in shared memory (64 KB)
-constexpr int SPT = 16;         // consecutive scores per thread per streaming step
-
-// Scores s0 .. s0+15 of a row (keys of absent positions are 0 and masked by `valid`).
-__device__ __forceinline__ void load_keys16(const float *__restrict__ row, int s0, int n, bool vec,
-                                            uint32_t (&u)[SPT], uint32_t &valid) {
-    if (vec && s0 + SPT <= n) {
-        const float4 *p = (const float4 *)(row + s0);
-#pragma unroll
-        for (int j = 0; j < SPT / 4; ++j) {
-            const float4 f = __ldg(p + j);
-            u[4 * j] = ordered_key(f.x);
-            u[4 * j + 1] = ordered_key(f.y);
-            u[4 * j + 2] = ordered_key(f.z);
-            u[4 * j + 3] = ordered_key(f.w);
-        }
-        valid = 0xffffu;
-    } else {
-        valid = 0;
-#pragma unroll
-        for (int j = 0; j < SPT; ++j) {
-            const bool ok = s0 + j < n;
-            u[j] = ok ? ordered_key(__ldg(row + s0 + j)) : 0u;
-            valid |= ok ? (1u << j) : 0u;
-        }
-    }
-}
-
-// The bin b of hist[0..nb) (nb a multiple of TF_THREADS) holding the need-th
-// largest key, counted from the top: keys in bins above b number `above` <
-// need <= above + hist[b].  Every thread of the CTA calls it and receives
-// {b, above, above + hist[b]} in res[0..2].  Thread t owns nb / TF_THREADS
-// consecutive bins from the top, so the search is one block-wide scan.
-__device__ __forceinline__ void find_bin_from_top(const uint32_t *hist, int nb, int need, int *res, int *warp_sum) {
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int per = nb / TF_THREADS, hi = nb - tid * per;
-    int mine = 0;
-    for (int b = hi - 1; b >= hi - per; --b) mine += (int)hist[b];
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_sum[wid] = incl;
-    __syncthreads();
-    int before = 0;
-#pragma unroll
-    for (int w = 0; w < TF_WARPS; ++w) before += w < wid ? warp_sum[w] : 0;
-    const int excl = before + incl - mine;
-    if (excl < need && need <= excl + mine) {
-        int cum = excl;
-        for (int b = hi - 1; b >= hi - per; --b) {
-            const int h = (int)hist[b];
-            if (cum + h >= need) {
-                res[0] = b;
-                res[1] = cum;
-                res[2] = cum + h;
-                break;
-            }
-            cum += h;
-        }
-    }
-    __syncthreads();
-}
-
-// Exact top-k of n keys (key_at(j), j in index order), written as
-// [keys above the k-th key T, in order][the first keys equal to T, in order];
-// out_at(j) is the row index stored for entry j.  All threads of the CTA call it.
-template <class KeyAt, class IdxAt>
-__device__ __forceinline__ void radix_select_write(KeyAt key_at, IdxAt idx_at, int n, int k, int32_t *__restrict__ out,
-                                                   uint32_t *hist, int *warp_gt, int *warp_eq, int *shared3) {
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int &sel_bin = shared3[0], &sel_above = shared3[1];
-    uint32_t prefix = 0, pmask = 0;
-    int remaining = k;
-#pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const int width = pass == 2 ? 10 : 11;
-        const int nb = 1 << width;
-        for (int b = tid; b < nb; b += TF_THREADS) hist[b] = 0;
-        __syncthreads();
-        for (int s = tid; s < n; s += TF_THREADS) {
-            const uint32_t u = key_at(s);
-            if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
-        }
-        __syncthreads();
-        find_bin_from_top(hist, nb, remaining, shared3, warp_eq);
-        remaining -= sel_above;
-        prefix |= (uint32_t)sel_bin << shift;
-        pmask |= (uint32_t)(nb - 1) << shift;
-        __syncthreads();  // sel_* are rewritten by the next pass
-    }
-    // prefix is now the k-th largest key T; (k - remaining) keys are above it.
-    const uint32_t T = prefix;
-    const int n_gt = k - remaining;
-    int base_gt = 0, base_eq = 0;
-    for (int s0 = 0; s0 < n; s0 += TF_THREADS) {
-        if (base_gt >= n_gt && base_eq >= remaining) break;  // block-uniform: every slot is written
-        const int s = s0 + tid;
-        const uint32_t u = s < n ? key_at(s) : 0u;
-        const bool gt = s < n && u > T;
-        const bool eq = s < n && u == T;
-        const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
-        const uint32_t lt_mask = (1u << lane) - 1u;
-        if (lane == 0) {
-            warp_gt[wid] = __popc(bg);
-            warp_eq[wid] = __popc(be);
-        }
-        __syncthreads();
-        int off_gt = 0, off_eq = 0, tot_gt = 0, tot_eq = 0;
-#pragma unroll
-        for (int w = 0; w < TF_WARPS; ++w) {
-            off_gt += w < wid ? warp_gt[w] : 0;
-            off_eq += w < wid ? warp_eq[w] : 0;
-            tot_gt += warp_gt[w];
-            tot_eq += warp_eq[w];
-        }
-        if (gt) {
-            const int rank = base_gt + off_gt + __popc(bg & lt_mask);
-            if (rank < n_gt) out[rank] = idx_at(s);
-        }
-        if (eq) {
-            const int rank = base_eq + off_eq + __popc(be & lt_mask);
-            if (rank < remaining) out[n_gt + rank] = idx_at(s);
-        }
-        base_gt += tot_gt;
-        base_eq += tot_eq;
-        __syncthreads();  // warp_gt / warp_eq are rewritten by the next chunk
-    }
-}
 
 __global__ void __launch_bounds__(TF_THREADS) topk_filter_kernel(const float *__restrict__ scores, int64_t ld,
                                                                  const __grid_constant__ SeqTab st, int k,
@@ -184,82 +54,14 @@ __global__ void __launch_bounds__(TF_THREADS) topk_filter_kernel(const float *__
     __shared__ uint32_t hist[MAX_BINS];
     __shared__ int warp_gt[TF_WARPS], warp_eq[TF_WARPS];
     __shared__ int shared3[3];
-    int32_t *cand_idx = (int32_t *)(cand + cap);
     pdl_wait();  // everything below reads or writes global memory
 
     const int r = blockIdx.x;
     const RowInfo ri = row_info(st, r);
     const int n_live = min(ri.p + 1, ri.S);
-    const float *row = scores + (int64_t)r * ld;
-    int32_t *out = idx + (int64_t)r * k;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-
-    if (n_live <= k) {
-        for (int j = tid; j < k; j += TF_THREADS) out[j] = j < n_live ? j : -1;
-        return;
-    }
-
-    // ---- A: histogram of the top 11 key bits ----
-    for (int b = tid; b < MAX_BINS; b += TF_THREADS) hist[b] = 0;
-    __syncthreads();
-    // The loop bounds are block-uniform: every lane reaches each __match_any_sync.
-#pragma unroll 1
-    for (int base = 0; base < n_live; base += TF_THREADS * SPT) {
-        uint32_t u[SPT], valid;
-        load_keys16(row, base + tid * SPT, n_live, vec != 0, u, valid);
-#pragma unroll
-        for (int j = 0; j < SPT; ++j)
-            if ((valid >> j) & 1u) atomicAdd(&hist[u[j] >> 21], 1u);
-    }
-    __syncthreads();
-    find_bin_from_top(hist, MAX_BINS, k, shared3, warp_eq);
-    const uint32_t bsel = (uint32_t)shared3[0];
-    const int n_cand = shared3[2];  // keys in the threshold bin or above
-    __syncthreads();  // shared3 is reused by the select
-
-    if (n_cand <= cap) {
-        // ---- B: compact the candidates (top bits >= bsel) in index order ----
-        int base = 0;
-#pragma unroll 1
-        for (int s0 = 0; s0 < n_live; s0 += TF_THREADS * SPT) {
-            const int first = s0 + tid * SPT;
-            uint32_t u[SPT], valid = 0;
-            if (first < n_live) load_keys16(row, first, n_live, vec != 0, u, valid);
-            uint32_t take = 0;
-#pragma unroll
-            for (int j = 0; j < SPT; ++j) take |= (((valid >> j) & 1u) && (u[j] >> 21) >= bsel) ? (1u << j) : 0u;
-            const int c = __popc(take);
-            int incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            if (lane == 31) warp_gt[wid] = incl;
-            __syncthreads();
-            int before = 0, total = 0;
-#pragma unroll
-            for (int w = 0; w < TF_WARPS; ++w) {
-                before += w < wid ? warp_gt[w] : 0;
-                total += warp_gt[w];
-            }
-            int pos = base + before + incl - c;
-#pragma unroll
-            for (int j = 0; j < SPT; ++j)
-                if ((take >> j) & 1u) {
-                    cand[pos] = u[j];
-                    cand_idx[pos] = first + j;
-                    ++pos;
-                }
-            base += total;
-            __syncthreads();  // warp_gt is rewritten by the next step
-        }
-        radix_select_write([&](int j) { return cand[j]; }, [&](int j) { return cand_idx[j]; }, n_cand, k, out, hist,
-                           warp_gt, warp_eq, shared3);
-    } else {
-        radix_select_write([&](int j) { return ordered_key(__ldg(row + j)); }, [&](int j) { return j; }, n_live, k,
-                           out, hist, warp_gt, warp_eq, shared3);
-    }
+    const tk::FilterSmem sm{hist, warp_gt, warp_eq, shared3, cand, (int32_t *)(cand + cap), cap};
+    tk::filter_row<TF_THREADS, 0, true>((int)threadIdx.x, scores + (int64_t)r * ld, n_live, k, vec != 0,
+                                        idx + (int64_t)r * k, sm);
 }
 
 constexpr int KPT = 8;                // consecutive keys per thread in the ordered pass
@@ -447,7 +249,6 @@ constexpr int CL = 8;              // CTAs per row
 constexpr int LONG_ROW = 8192;     // causal keys from which a few rows take the cluster kernel
 constexpr int CT = 256;            // threads per CTA
 constexpr int CT_WARPS = CT / 32;
-static_assert(CT == TF_THREADS, "find_bin_from_top assumes the filter kernel's block size");
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -547,7 +348,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(CT)
             *(uint4 *)(merged + 4 * q4) = acc;
         }
         __syncthreads();
-        find_bin_from_top(merged, (int)nb, remaining, sel, warp_sum);
+        tk::find_bin_from_top<CT, 0>(tid, merged, (int)nb, remaining, sel, warp_sum);
         remaining -= sel[1];
         prefix |= (uint32_t)sel[0] << shift;
         pmask |= (nb - 1) << shift;

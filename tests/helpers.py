@@ -2,12 +2,15 @@
 running the oracle on a subset of rows, and the acceptance rules.
 
 Acceptance rules (the tolerances the path is held to):
-  * indexer scores: |gpu - ref| <= 1e-3 * max(|ref|, A) where A is the
-    absolute-term sum 1/sqrt(H_I D_I) sum_h |w| ReLU(q.k) (so the band does
-    not vanish when cancellation makes the score ~0); masked keys must be
-    exactly -inf;
+  * indexer scores: |gpu - ref| <= 1e-3 * |ref| + 1e-5 * A, where A is the
+    absolute-term sum 1/sqrt(H_I D_I) sum_h |w| ReLU(q.k).  The first term is
+    the stated "1e-3 relative"; the second is a floor of the size of the fp32
+    accumulation error (the kernels add the exact input products and the 64
+    weighted heads in fp32, whose rounding is a few 1e-7 of A), so that a
+    score that cancels to ~0 is not held to an impossible relative bound.
+    Masked keys must be exactly -inf;
   * top-k: the GPU set equals the oracle set except for keys whose oracle
-    score lies within tau = 1e-3 * max(|S_n|, A_n) of the oracle's n-th
+    score lies within tau = 1e-3 * |S_n| + 1e-5 * A_n of the oracle's n-th
     score S_n; the GPU row holds exactly n = min(k, p+1) distinct causal keys
     followed by -1 padding;
   * attention output: max |gpu - ref| <= 2e-2 (unit-scale bf16 data);
@@ -22,6 +25,7 @@ import oracle
 import sparse_latent_attention_indexer_gb300 as dsa
 
 SCORE_RTOL = 1e-3
+SCORE_ATOL_A = 1e-5  # times the absolute-term sum A of the same score
 OUT_ATOL_BF16 = 2e-2
 OUT_ATOL_F32 = 1e-4
 # The stated tolerances bound the outputs only; the lse (natural log) bound is derived from the
@@ -104,18 +108,38 @@ def oracle_rows(wl, rows, with_attention=True):
     return res
 
 
+def score_band(ref, absterm):
+    """The allowed |gpu - ref| of each score."""
+    return SCORE_RTOL * np.abs(ref) + SCORE_ATOL_A * absterm
+
+
 def check_score_row(gpu_row, ref_row, abs_row, p, S):
-    """gpu_row: the first S columns of the GPU score row."""
+    """gpu_row: the first S columns of the GPU score row.  Returns the row's
+    error statistics: the largest error over its band ("ratio", <= 1), over A
+    ("err_over_A") and relative to |ref| where |ref| >= 1e-2 A ("rel")."""
     gpu_row = np.asarray(gpu_row, np.float64)
     causal = slice(0, p + 1)
     fut = gpu_row[p + 1:S]
     assert np.all(np.isneginf(fut)), "future keys must be -inf"
     g, r, a = gpu_row[causal], ref_row[causal], abs_row[causal]
     assert np.all(np.isfinite(g)), "causal scores must be finite"
-    band = SCORE_RTOL * np.maximum(np.abs(r), a)
+    band = score_band(r, a)
     err = np.abs(g - r)
     bad = err > band
-    assert not bad.any(), f"{bad.sum()} scores out of tolerance; worst err {err.max():.3e} at {int(err.argmax())}"
+    assert not bad.any(), (f"{bad.sum()} scores out of tolerance; worst err {err[bad].max():.3e} "
+                           f"(band {band[bad][err[bad].argmax()]:.3e})")
+    pos = a > 0
+    big = np.abs(r) >= 1e-2 * a
+    big &= pos
+    return {"ratio": float((err[pos] / band[pos]).max()) if pos.any() else 0.0,
+            "err_over_A": float((err[pos] / a[pos]).max()) if pos.any() else 0.0,
+            "rel": float((err[big] / np.abs(r[big])).max()) if big.any() else 0.0}
+
+
+def merge_stats(acc, st):
+    for key, v in st.items():
+        acc[key] = max(acc.get(key, 0.0), v)
+    return acc
 
 
 def check_selection_row(gpu_idx, ref_scores, ref_abs, p, k):
@@ -132,7 +156,7 @@ def check_selection_row(gpu_idx, ref_scores, ref_abs, p, k):
     if ref_set == gpu_set:
         return 0
     s_n = causal[order[n - 1]]
-    tau = SCORE_RTOL * max(abs(s_n), ref_abs[order[n - 1]])
+    tau = SCORE_RTOL * abs(s_n) + SCORE_ATOL_A * ref_abs[order[n - 1]]
     diff = ref_set ^ gpu_set
     far = [s for s in diff if abs(causal[s] - s_n) > tau]
     assert not far, f"selection differs outside the tie band: keys {far[:8]}"

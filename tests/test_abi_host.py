@@ -111,3 +111,28 @@ def test_bounded_wait_selftest_rejects_out_of_range_limits():
     lib = _abi.load()
     assert lib.dsa_selftest_bounded_wait(0, None, None) == _abi.DSA_ERR_INVALID_ARG
     assert lib.dsa_selftest_bounded_wait((1 << 32) + 1, None, None) == _abi.DSA_ERR_INVALID_ARG
+
+
+def test_noalloc_scratch_holds_the_documented_batch():
+    """dsa_sparse_mla_fwd_noalloc accepts a call while the attention scratch
+    (dsa_sparse_mla_workspace_size) fits DSA_NOALLOC_SCRATCH_BYTES; the header
+    promises every decode batch of up to 128 query rows at the 671B head shapes.
+    Host-side sizes only, so a later change of the scratch layout or of the key
+    split count that breaks the promise fails here."""
+    lib = _abi.load()
+
+    def need(rows):
+        s = _seqs([1] * rows, [4096] * rows, [4095] * rows)
+        return lib.dsa_sparse_mla_workspace_size(_abi.DSA_BF16, 128, 128, 64, 512, 128, 2048, s.ref())
+
+    for rows in range(1, 129):
+        assert 0 < need(rows) <= _abi.DSA_NOALLOC_SCRATCH_BYTES, rows
+    assert need(129) > _abi.DSA_NOALLOC_SCRATCH_BYTES
+
+
+def test_wait_limit_range():
+    lib = _abi.load()
+    assert lib.dsa_set_wait_limit(-1) == _abi.DSA_ERR_INVALID_ARG
+    assert lib.dsa_set_wait_limit((1 << 32) + 1) == _abi.DSA_ERR_INVALID_ARG
+    assert lib.dsa_set_wait_limit(1000) == _abi.DSA_OK
+    assert lib.dsa_set_wait_limit(0) == _abi.DSA_OK  # back to the default

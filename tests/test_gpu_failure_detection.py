@@ -27,3 +27,40 @@ def test_bounded_wait_runs_out_and_reports_its_site():
     torch.cuda.synchronize()
     assert idx.shape == (3, 8) and bool((idx >= 0).all())
     assert dsa.dsa_check_device_error() == (_abi.DSA_OK, 0)
+
+
+def test_production_kernels_give_up_and_recover():
+    """The failure path of the production tensor-core kernels (indexer, top-k
+    input, absorption, sparse attention): with a wait limit of 64 SM cycles the
+    first wait that is not already satisfied gives up, the CTA records its site,
+    drains what it has in flight, frees its tensor memory and exits.  The host
+    reads DSA_ERR_TIMEOUT and a production site; with the limit restored the
+    same call matches the oracle."""
+    import numpy as np
+
+    import dsa_inputs as di
+    from tests import helpers as H
+
+    wl = di.generate("abort-path", di.Shape(k=64), 5, [96, 40], [96, 300], [0, 260])
+    t = H.to_device(wl)
+    assert dsa.dsa_check_device_error() == (_abi.DSA_OK, 0)
+    try:
+        dsa.dsa_set_wait_limit(64)
+        H.gpu_forward(wl, t)
+        launched = dsa.last_kernels()
+        st, site = dsa.dsa_check_device_error()
+    finally:
+        dsa.dsa_set_wait_limit(0)
+    assert {"indexer_tc", "absorb_tc", "mla_tc"} <= launched, launched
+    assert st == _abi.DSA_ERR_TIMEOUT, st
+    assert 1 <= site <= 40, site  # a production kernel's site (the self-test uses 90 and 91)
+    assert dsa.dsa_check_device_error() == (_abi.DSA_OK, 0)
+    out, lse, idx = H.gpu_forward(wl, t)
+    assert dsa.dsa_check_device_error() == (_abi.DSA_OK, 0)
+    ref = H.oracle_rows(wl, list(range(wl.total_q)))
+    out_np, idx_np = out.float().cpu().numpy(), idx.cpu().numpy()
+    for r, o in ref.items():
+        H.check_selection_row(idx_np[r], o["scores"], o["absterm"], o["pos"], wl.shape.k)
+        assert float(np.abs(out_np[r] - o["out"]).max()) <= H.OUT_ATOL_BF16
+    with pytest.raises(dsa.DSAError):
+        dsa.dsa_set_wait_limit(-1)

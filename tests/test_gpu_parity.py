@@ -280,7 +280,7 @@ def test_forward_dense_when_k_covers_the_sequence():
     assert np.abs(out.float().cpu().numpy()[rows] - ref).max() <= H.OUT_ATOL_BF16
 
 
-INDEXER_AND_TOPK = {"quant", "indexer_simt", "indexer_tc", "indexer_fp8", "topk"}
+INDEXER_AND_TOPK = {"quant", "indexer_simt", "indexer_tc", "indexer_fp8", "topk", "indexer_topk"}
 
 
 @pytest.mark.parametrize("shape", ["bf16", "fp8", "f32"])

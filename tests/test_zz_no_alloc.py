@@ -22,11 +22,11 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 
-def _decode_batch(seed):
-    """A decode step: 24 sequences with one query each, at the 671B head
+def _decode_batch(seed, n=24):
+    """A decode step: n sequences with one query each, at the 671B head
     shapes, and a seeded selection of up to 2048 keys per query."""
     g = torch.Generator().manual_seed(seed)
-    S = [int(x) for x in torch.randint(200, 5000, (24,), generator=g)]
+    S = [int(x) for x in torch.randint(200, 5000, (n,), generator=g)]
     wl = di.generate(f"noalloc-{seed}", di.FULL, seed, [1] * len(S), S, [s - 1 for s in S])
     sel = di.random_selection(wl, seed=seed + 1, density=0.6)
     return wl, H.to_device(wl), sel.cuda()
@@ -45,8 +45,18 @@ def _noalloc(wl, t, sel, out, lse):
         ctypes.c_float(sh.softmax_scale), ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()), stream)
 
 
+def test_noalloc_zero_rows_is_set_up_only():
+    """A call with no query rows does the per-device set-up and launches nothing."""
+    wl, t, sel = _decode_batch(40, n=2)
+    empty = di.Workload("empty", wl.shape, 0, [0], [16], [0], {})
+    st = _noalloc(empty, t, sel, torch.empty(0, device="cuda"), torch.empty(0, device="cuda"))
+    assert st == _abi.DSA_OK, _abi.load().dsa_status_string(st)
+    assert _abi.load().dsa_last_launch_count() == 0
+
+
 def test_noalloc_matches_workspace_entry_point_twice_in_a_row():
-    batches = [_decode_batch(41), _decode_batch(42)]
+    # two calls in a row; the second is the largest batch the scratch holds (128 rows)
+    batches = [_decode_batch(41), _decode_batch(42, n=128)]
     for wl, t, sel in batches:  # two calls in a row, different inputs
         sh = wl.shape
         ref_out, ref_lse = dsa.dsa_sparse_mla_fwd(t["q_nope"], t["q_pe"], t["ckv"], t["kpe"], t["W_UK"], t["W_UV"],
