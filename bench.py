@@ -61,6 +61,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the steps around the path and the FP8 latent cache")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="keep only the first ROWS query rows of each workload (a small case of the same kernels, "
+                         "for profiling); the sequences keep their whole caches")
+    ap.add_argument("--fused-topk", type=int, choices=[0, 1], default=None,
+                    help="1: the fused indexer + top-k kernel; 0: indexer then top-k; default: the library's")
     return ap.parse_args()
 
 
@@ -366,6 +371,34 @@ def roofline_of(stage, ms, flops, hbm, peaks, peak_src, wl_name, fp8=False):
             "algorithmic": alg}
 
 
+def first_rows(wl, n):
+    """The workload cut to its first n query rows: the sequences that hold them (the last one with
+    fewer queries), each keeping its whole key cache."""
+    if n is None or n >= wl.total_q:
+        return wl
+    import dsa_inputs as di
+    T, S, P, cut = [], [], [], 0
+    for b in range(wl.B):
+        if cut >= n:
+            break
+        t = min(wl.T[b], n - cut)
+        T.append(t)
+        S.append(wl.S[b])
+        P.append(wl.start_pos[b])
+        cut += t
+    nb, nk = len(T), wl.cu_k[len(T)]
+    q_rows = [r for b in range(nb) for r in range(wl.cu_q[b], wl.cu_q[b] + T[b])]
+    ten = {}
+    for k, v in wl.tensors.items():
+        if k in ("qI", "w", "q_nope", "q_pe"):
+            ten[k] = v[q_rows]
+        elif k in ("kI", "kv_cache"):
+            ten[k] = v[:nk]
+        else:
+            ten[k] = v
+    return di.Workload(wl.name + f"-first{n}", wl.shape, wl.seed, T, S, P, ten)
+
+
 def measure_workload(cfg, args, world, rank, local, with_cpu):
     """Times whole dsa_forward steps of workload `cfg`, then its indexer and
     top-k kernels on their own, then the end-to-end step from host buffers."""
@@ -375,9 +408,9 @@ def measure_workload(cfg, args, world, rank, local, with_cpu):
     import sparse_latent_attention_indexer_gb300 as dsa
 
     dev = torch.device("cuda", local)
-    wl = di.workload(cfg)
+    wl = first_rows(di.workload(cfg), args.rows)
     sh = wl.shape
-    name = CONFIG_NAMES[cfg]
+    name = CONFIG_NAMES[cfg] + (f" (first {args.rows} rows)" if args.rows else "")
     seqs = dsa.Seqs(wl.cu_q, wl.cu_k, wl.start_pos)
     host = wl.tensors
     t = {k: v.to(dev) for k, v in host.items()}
@@ -521,6 +554,9 @@ def measure_indexer_topk(args, dsa, torch, wl, t, flush, peaks, peak_src):
 
 
 def run_ours(args, world, rank, local):
+    if args.fused_topk is not None:
+        import sparse_latent_attention_indexer_gb300 as dsa
+        dsa.dsa_set_fused_topk(bool(args.fused_topk))
     extra = [int(x) for x in args.extra.split(",") if x.strip() != ""] if args.extra else []
     extra = [c for c in extra if c != args.config]
     main = measure_workload(args.config, args, world, rank, local, with_cpu=True)

@@ -395,12 +395,15 @@ int dsa_selftest_bounded_wait(int64_t limit_cycles, int *completed_ok, void *str
 int dsa_set_wait_limit(int64_t cycles);
 /* Selects, for dsa_forward calls that follow, between the two implementations
  * of the indexer + top-k on batches of at least 304 groups of 4 query rows
- * (no counterpart on the pages: a choice of this library).  on = 1: one
+ * (no counterpart on the pages: a choice of this library).  Fused: one
  * persistent kernel scores a group into a per-SM slot and selects its rows'
- * top-k from it, with no [rows, S] score buffer; on = 0 (default): the indexer
- * writes chunks of fp32 score rows and a separate top-k kernel selects from
- * them.  Both give identical selections.  Process-wide; returns DSA_OK. */
-int dsa_set_fused_topk(int on);
+ * top-k from it while the next group is scored, with no [rows, S] score
+ * buffer; two kernels: the indexer writes chunks of fp32 score rows and a
+ * separate top-k kernel selects from them.  Both give identical selections.
+ * mode 1: fused wherever it applies; 0: never; -1 (default): where it measured
+ * faster, the FP8 indexer over rows that see on average >= 16384 keys.
+ * Process-wide.  Returns DSA_ERR_INVALID_ARG for another mode. */
+int dsa_set_fused_topk(int mode);
 /* Bit mask of the kernels the last entry point launched on this host thread
  * (DSA_KERNEL_* bits), and how many kernel launches it made. */
 uint32_t dsa_last_kernels(void);

@@ -123,10 +123,11 @@ def dsa_set_wait_limit(cycles: int):
     _check("dsa_set_wait_limit", _abi.load().dsa_set_wait_limit(int(cycles)))
 
 
-def dsa_set_fused_topk(on: bool):
-    """Fused indexer + top-k (one persistent kernel, per-SM score slots) for the
-    dsa_forward calls that follow on large batches; off by default."""
-    _check("dsa_set_fused_topk", _abi.load().dsa_set_fused_topk(1 if on else 0))
+def dsa_set_fused_topk(mode):
+    """Fused indexer + top-k for the dsa_forward calls that follow on large batches:
+    True/1 wherever it applies, False/0 never, -1 the library's choice (default)."""
+    m = -1 if mode == -1 else (1 if mode else 0)
+    _check("dsa_set_fused_topk", _abi.load().dsa_set_fused_topk(m))
 
 
 def dsa_quant_e4m3_ue8m0(x: torch.Tensor, codes=None, scales=None, stream=None):

@@ -43,15 +43,22 @@ constexpr int TOK = 4;          // query tokens per group
 constexpr int HI = 64;          // indexer heads
 constexpr int DI = 128;         // indexer head dim
 constexpr int BN = TOK * HI;    // 256 (MMA N)
-// Warps 0-3: TMA producer, MMA issuer, tensor-memory owner, idle; then the epilogue warps.  bf16:
-// 16 of them, one per (TMEM lane quarter, token) pair, four per SM sub-partition.  FP8: 8, each
-// taking two tokens of its lane quarter (measured faster for the shorter FP8 MMA).
+// Warps 0-3: TMA producer, MMA issuer, tensor-memory owner, idle; then the epilogue warps.  One-shot
+// kernel, bf16: 16 of them, one per (TMEM lane quarter, token) pair, four per SM sub-partition; FP8:
+// 8, each taking two tokens of its lane quarter (measured faster for the shorter FP8 MMA).  The
+// fused kernel (F) has 8 epilogue warps in both precisions, then the selecting warps: 4 for FP8
+// (whose epilogue needs the 128 registers a 512-thread CTA leaves), 8 for bf16 (measured: 7.86
+// against 8.61 ms of indexer + top-k on the 32K prefill).
 constexpr int EPI_WARP0 = 4;
-template <bool FP8> constexpr int num_epi() { return FP8 ? 8 : 16; }
-template <bool FP8> constexpr int num_threads() { return (EPI_WARP0 + num_epi<FP8>()) * 32; }
+template <bool FP8, bool F = false> constexpr int num_epi() { return (FP8 || F) ? 8 : 16; }
+template <bool FP8> constexpr int sel_warps() { return FP8 ? 4 : 8; }
+template <bool FP8, bool F = false> constexpr int sel_warp0() { return EPI_WARP0 + num_epi<FP8, F>(); }
+template <bool FP8, bool F = false> constexpr int num_threads() {
+    return (EPI_WARP0 + num_epi<FP8, F>() + (F ? sel_warps<FP8>() : 0)) * 32;
+}
 constexpr int SPLIT_TAB = 2 * 152;  // launches with fewer query groups split each group's key blocks
 
-template <bool FP8>
+template <bool FP8, bool F = false>
 struct Cfg {
     static constexpr int ELT = FP8 ? 1 : 2;
     static constexpr int HALVES = FP8 ? 1 : 2;              // 128-byte column slabs per row
@@ -59,9 +66,16 @@ struct Cfg {
     static constexpr int A_BYTES = BM * DI * ELT;           // 32 KB / 16 KB
     static constexpr int B_HALF = BN * 128;                 // bytes of one 128-byte slab of B
     static constexpr int A_HALF = BM * 128;
-    static constexpr int STAGES = FP8 ? 6 : 4;
+    // the fused bf16 kernel gives one stage to the selection's candidate list
+    static constexpr int STAGES = FP8 ? 6 : (F ? 3 : 4);
     static constexpr int KSTEPS = FP8 ? 4 : 8;              // MMAs per block (K = 32 / 16 each)
-    static constexpr int SMEM = 1024 /*align slack*/ + B_BYTES + STAGES * A_BYTES + TOK * HI * 4 + 256;
+    static constexpr int BAR_BYTES = 256;
+    // the fused kernel's selection scratch: histogram + warp sums, then the candidate list
+    static constexpr int SEL_HEAD = tk::MAX_BINS * 4 + 512;
+    static constexpr int CAND_CAP = F ? (FP8 ? 8192 : 6144) : 0;
+    static constexpr int SMEM = 1024 /*align slack*/ + B_BYTES + STAGES * A_BYTES + TOK * HI * 4 + BAR_BYTES +
+                                (F ? SEL_HEAD + CAND_CAP * 8 : 0);
+    static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 struct IdxParams {
@@ -111,9 +125,9 @@ __device__ __forceinline__ Group group_of(const IdxParams &P, int g) {
 }
 
 // Shared-memory layout of both indexer kernels: addresses computed from one base pointer.
-template <bool FP8>
+template <bool FP8, bool F = false>
 struct Smem {
-    using C = Cfg<FP8>;
+    using C = Cfg<FP8, F>;
     uint8_t *base;
     __device__ __forceinline__ explicit Smem(uint8_t *raw)
         : base((uint8_t *)(((uintptr_t)raw + 1023) & ~(uintptr_t)1023)) {}
@@ -127,8 +141,13 @@ struct Smem {
     __device__ __forceinline__ uint64_t *tfull(int i) const { return bars() + 2 * C::STAGES + 1 + i; }
     __device__ __forceinline__ uint64_t *tempty(int i) const { return bars() + 2 * C::STAGES + 3 + i; }
     __device__ __forceinline__ uint64_t *mmadone() const { return bars() + 2 * C::STAGES + 5; }
-    __device__ __forceinline__ uint32_t *tmem_slot() const { return (uint32_t *)(bars() + 2 * C::STAGES + 6); }
+    // fused kernel: the query tile is free again / a slot holds a group's scores / a slot was read
+    __device__ __forceinline__ uint64_t *bfree() const { return bars() + 2 * C::STAGES + 6; }
+    __device__ __forceinline__ uint64_t *slot_full(int i) const { return bars() + 2 * C::STAGES + 7 + i; }
+    __device__ __forceinline__ uint64_t *slot_free(int i) const { return bars() + 2 * C::STAGES + 9 + i; }
+    __device__ __forceinline__ uint32_t *tmem_slot() const { return (uint32_t *)(bars() + 2 * C::STAGES + 11); }
     __device__ __forceinline__ volatile int *abort_flag() const { return (volatile int *)(tmem_slot() + 1); }
+    __device__ __forceinline__ uint8_t *sel() const { return (uint8_t *)bars() + C::BAR_BYTES; }
 };
 
 // Barrier phases carried from group to group by a CTA that takes several groups: loads issued
@@ -143,9 +162,10 @@ struct Phases {
     }
 };
 
-template <bool FP8>
-__device__ __forceinline__ void init_barriers(const Smem<FP8> &sm) {
-    using C = Cfg<FP8>;
+template <bool FP8, bool F = false>
+__device__ __forceinline__ void init_barriers(const Smem<FP8, F> &sm) {
+    using C = Cfg<FP8, F>;
+    static_assert((2 * C::STAGES + 12) * 8 <= C::BAR_BYTES, "barrier area");
     for (int i = 0; i < C::STAGES; ++i) {
         tc::mbar_init(sm.full(i), 1);
         tc::mbar_init(sm.empty(i), 1);
@@ -153,19 +173,27 @@ __device__ __forceinline__ void init_barriers(const Smem<FP8> &sm) {
     tc::mbar_init(sm.bfull(), 1);
     for (int i = 0; i < 2; ++i) {
         tc::mbar_init(sm.tfull(i), 1);
-        tc::mbar_init(sm.tempty(i), num_epi<FP8>());
+        tc::mbar_init(sm.tempty(i), num_epi<FP8, F>());
     }
     tc::mbar_init(sm.mmadone(), 1);
+    if (F) {
+        tc::mbar_init(sm.bfree(), 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(sm.slot_full(i), num_epi<FP8, F>() * 32);
+            tc::mbar_init(sm.slot_free(i), sel_warps<FP8>() * 32);
+        }
+    }
     *sm.abort_flag() = 0;
     tc::fence_mbar_init();
 }
 
 // The weights of the group's rows, with the constant 1/sqrt(H_I D_I) and (FP8) the q block scale
 // folded in; written by the epilogue threads.
-template <bool FP8>
-__device__ __forceinline__ void load_weights(const Smem<FP8> &sm, const float *__restrict__ w,
+template <bool FP8, bool F = false>
+__device__ __forceinline__ void load_weights(const Smem<FP8, F> &sm, const float *__restrict__ w,
                                              const float *__restrict__ q_scale, const IdxParams &P, const Group &G) {
-    for (int i = threadIdx.x - EPI_WARP0 * 32; i < TOK * HI; i += (num_threads<FP8>() - EPI_WARP0 * 32)) {
+    constexpr int NE = num_epi<FP8, F>() * 32;
+    for (int i = threadIdx.x - EPI_WARP0 * 32; i < TOK * HI; i += NE) {
         const int tt = i / HI, h = i % HI;
         float v = 0.0f;
         if (tt < G.ntok) {
@@ -173,6 +201,53 @@ __device__ __forceinline__ void load_weights(const Smem<FP8> &sm, const float *_
             v = w[qi] * P.c * (FP8 ? q_scale[qi] : 1.0f);
         }
         sm.wsm()[i] = v;
+    }
+}
+
+// The epilogue of one key block held in accumulator `acc`: warp (q, first token) reduces its
+// tokens for the keys of TMEM lane quarter q (key = this thread's key of the block, keyed from 0
+// within the sequence) and writes row tt of the group to out_base + tt * ld.  Releases the
+// accumulator to the MMA issuer.
+template <bool FP8, bool F>
+__device__ __forceinline__ void epilogue_block(const Smem<FP8, F> &sm, uint32_t tmem, int acc, int key,
+                                               const Group &G, const float *__restrict__ k_scale, float *out_base,
+                                               int64_t ld) {
+    constexpr int EPI = num_epi<FP8, F>();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3, t_first = (warp - EPI_WARP0) >> 2, t_step = EPI / 4;
+    const float ks = (FP8 && key < G.S) ? k_scale[G.kbase + key] : 1.0f;
+#pragma unroll 1
+    for (int tt = t_first; tt < G.ntok; tt += t_step) {
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + tt * HI;
+        float v0[32], v1[32];
+        tc::tmem_ld32(taddr, v0);
+        tc::tmem_ld32(taddr + 32, v1);
+        tc::tmem_ld_wait();
+        if (EPI == 16) {  // one token per warp, so the accumulator can go back at once
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(sm.tempty(acc));
+        }
+        const float4 *wv = (const float4 *)(sm.wsm() + tt * HI);
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 a4 = wv[h4], c4 = wv[8 + h4];
+            s0 = fmaf(a4.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
+            s1 = fmaf(c4.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
+            s0 = fmaf(a4.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
+            s1 = fmaf(c4.y, fmaxf(v1[4 * h4 + 1], 0.0f), s1);
+            s0 = fmaf(a4.z, fmaxf(v0[4 * h4 + 2], 0.0f), s0);
+            s1 = fmaf(c4.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
+            s0 = fmaf(a4.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
+            s1 = fmaf(c4.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
+        }
+        if (key < G.S) out_base[(int64_t)tt * ld + key] = (key <= G.p0 + tt) ? (s0 + s1) * ks : -INFINITY;
+    }
+    if (EPI == 8 || t_first >= G.ntok) {
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(sm.tempty(acc));
     }
 }
 
@@ -251,47 +326,13 @@ __device__ __forceinline__ void group_pipeline(const CUtensorMap *tm_q, const CU
         // ---------------- epilogue ----------------
         // bf16: warp (q, tt) reduces token tt for the keys of lane quarter q.  FP8: the two
         // warps of lane quarter q take tokens hf and hf + 2.  Absent tokens are skipped.
-        const int q = warp & 3, t_first = (warp - EPI_WARP0) >> 2, t_step = FP8 ? 2 : 4;
+        const int q = warp & 3;
         for (int i = 0; i < mine; ++i) {
             const int a = ph.ai + i, acc = a & 1;
             if (!tc::mbar_wait(sm.tfull(acc), (a >> 1) & 1, abort_flag, &g_indexer_tc_error, 8, P.wait_limit)) break;
             tc::tc_fence_after();
-            const int key = (split + i * splits) * BM + q * 32 + lane;
-            const float ks = (FP8 && key < G.S) ? k_scale[G.kbase + key] : 1.0f;
-#pragma unroll 1
-            for (int tt = t_first; tt < G.ntok; tt += t_step) {
-                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + tt * HI;
-                float v0[32], v1[32];
-                tc::tmem_ld32(taddr, v0);
-                tc::tmem_ld32(taddr + 32, v1);
-                tc::tmem_ld_wait();
-                if (!FP8) {  // bf16: one token per warp, so the accumulator can go back at once
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(sm.tempty(acc));
-                }
-                const float4 *wv = (const float4 *)(sm.wsm() + tt * HI);
-                float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-                for (int h4 = 0; h4 < 8; ++h4) {
-                    const float4 a4 = wv[h4], c4 = wv[8 + h4];
-                    s0 = fmaf(a4.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
-                    s1 = fmaf(c4.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
-                    s0 = fmaf(a4.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
-                    s1 = fmaf(c4.y, fmaxf(v1[4 * h4 + 1], 0.0f), s1);
-                    s0 = fmaf(a4.z, fmaxf(v0[4 * h4 + 2], 0.0f), s0);
-                    s1 = fmaf(c4.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
-                    s0 = fmaf(a4.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
-                    s1 = fmaf(c4.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
-                }
-                if (key < G.S)
-                    out_base[(int64_t)tt * P.ld + key] = (key <= G.p0 + tt) ? (s0 + s1) * ks : -INFINITY;
-            }
-            if (FP8 || t_first >= G.ntok) {
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(sm.tempty(acc));
-            }
+            epilogue_block<FP8, false>(sm, tmem, acc, (split + i * splits) * BM + q * 32 + lane, G, k_scale, out_base,
+                                       P.ld);
         }
     }
 }
@@ -361,29 +402,57 @@ __global__ void __launch_bounds__(num_threads<FP8>(), 1)
     }
 }
 
-// The indexer and the top-k fused: a persistent CTA per SM takes query groups heaviest first (in a
-// snake order over the CTAs, so the loads balance), computes a group's scores into its own slot of
-// 4 score rows (slots: [gridDim.x][4][P.ld] fp32, reused group after group, so they stay in L2),
-// then its epilogue warps select each row's top-k from the slot -- reading it back from L2 -- and
-// write the row's indices to idx [rows, P.topk].  No [rows, S] score buffer exists.  The key-block
-// ring and the query tile are free while the selection runs, so its histogram and candidate list
-// live there.  Groups whose rows all see at most k keys skip the MMAs and write their dense
-// selection (0 .. n-1, then -1).
+// Named barrier ID over N threads that also ANDs `v` over them (so the group takes one decision).
+template <int ID, int N>
+__device__ __forceinline__ bool bar_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(ID), "n"(N)
+        : "memory");
+    return r != 0;
+}
+
+// Position j of a CTA's walk over the groups, heaviest first: the CTAs take positions in a snake
+// order (0 .. G-1, then G-1 .. 0, ...), so each gets a similar mix of heavy and light groups.
+__device__ __forceinline__ int walk_group(const IdxParams &P, int j) {
+    const int G = (int)gridDim.x;
+    const int pos = j * G + ((j & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    return pos < P.total_groups ? P.total_groups - 1 - pos : -1;
+}
+
+// The indexer and the top-k fused.  A persistent CTA per SM walks query groups (walk_group).  The
+// producer, the MMA issuer and the epilogue run the indexer of group after group without draining in
+// between: the epilogue writes a group's 4 score rows into one of the CTA's two slots (slots:
+// [gridDim.x][2][4][P.ld] fp32), and four selecting warps take each filled slot, select every row's
+// top-k from it (reading it back from L2) and write the indices to idx [rows, P.topk] -- while the
+// tensor cores already compute the next group.  No [rows, S] score buffer exists.  Groups whose rows
+// all see at most k keys skip the MMAs; their selection is the dense one (0 .. n-1, then -1).
+// Hand-offs: bfree (the MMAs of a group are done, its query tile may be replaced), slot_full (the
+// epilogue's rows of a group are in the slot) and slot_free (the selecting warps are done with it).
 template <bool FP8>
-__global__ void __launch_bounds__(num_threads<FP8>(), 1)
+__global__ void __launch_bounds__(num_threads<FP8, true>(), 1)
     indexer_topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const float *__restrict__ w, const float *__restrict__ q_scale,
                         const float *__restrict__ k_scale, const __grid_constant__ IdxParams P,
                         float *__restrict__ slots, int32_t *__restrict__ idx) {
-    using C = Cfg<FP8>;
-    constexpr int NT = num_threads<FP8>() - EPI_WARP0 * 32;  // the selecting threads (the epilogue warps)
-    static_assert(tk::MAX_BINS % NT == 0, "the bin scan gives each thread the same number of bins");
-    static_assert(16384 + 2 * 8192 * 4 <= C::B_BYTES + C::STAGES * C::A_BYTES, "selection scratch in the ring");
+    using C = Cfg<FP8, true>;
+    constexpr int EPI = num_epi<FP8, true>();
+    constexpr int SEL0 = sel_warp0<FP8, true>();
+    constexpr int NS = sel_warps<FP8>() * 32;  // selecting threads
+    static_assert(tk::MAX_BINS % NS == 0, "the bin scan gives each thread the same number of bins");
     extern __shared__ uint8_t smem_raw[];
-    const Smem<FP8> sm(smem_raw);
+    const Smem<FP8, true> sm(smem_raw);
     __shared__ int never;
+    volatile int *nv = (volatile int *)&never;
+    volatile int *abort_flag = sm.abort_flag();
+    int *err = &g_indexer_tc_error;
 
-    const int warp = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         init_barriers(sm);
         never = 0;
@@ -397,40 +466,129 @@ __global__ void __launch_bounds__(num_threads<FP8>(), 1)
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *sm.tmem_slot();
-    float *slot = slots + (int64_t)blockIdx.x * TOK * P.ld;
-    // selection scratch over the query tile and the ring: histogram, warp sums, candidates
-    uint8_t *scratch = sm.Bt();
-    const tk::FilterSmem fs{(uint32_t *)scratch, (int *)(scratch + 8192), (int *)(scratch + 8192 + 256),
-                            (int *)(scratch + 8192 + 512), (uint32_t *)(scratch + 16384),
-                            (int32_t *)(scratch + 16384 + 8192 * 4), 8192};
-    Phases ph;
-    const int G_ = (int)gridDim.x;
-    for (int j = 0;; ++j) {
-        const int pos = j * G_ + ((j & 1) ? G_ - 1 - (int)blockIdx.x : (int)blockIdx.x);
-        if (pos >= P.total_groups) break;
-        const Group G = group_of(P, P.total_groups - 1 - pos);
-        const bool dense = G.p0 + G.ntok - 1 < P.topk;
-        const int mine = dense ? 0 : G.nblk;
-        if (warp >= EPI_WARP0 && !dense) load_weights(sm, w, q_scale, P, G);
-        tc::tc_fence_before();
-        __syncthreads();
-        tc::tc_fence_after();
-        group_pipeline<FP8>(&tm_q, &tm_k, k_scale, P, G, 0, 1, mine, slot, sm, tmem, ph, (volatile int *)&never);
-        tc::tc_fence_before();
-        __syncthreads();  // the slot's rows are written; every MMA and load of the group is done
-        if (*sm.abort_flag()) break;
-        if (warp >= EPI_WARP0) {
-            const int tid = (int)threadIdx.x - EPI_WARP0 * 32;
-            for (int tt = 0; tt < G.ntok; ++tt) {
-                const int n_live = min(G.p0 + tt + 1, G.S);
-                tk::filter_row<NT, 2, false, FP8 ? 16 : 8>(tid, slot + (int64_t)tt * P.ld, n_live, P.topk, true,
-                                             idx + (int64_t)(G.r0 + tt) * P.topk, fs);
+    float *slot0 = slots + (int64_t)blockIdx.x * 2 * TOK * P.ld;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_k);
+        int it = 0, nq = 0;
+        bool ok = true;
+        for (int j = 0; ok; ++j) {
+            const int g = walk_group(P, j);
+            if (g < 0) break;
+            const Group G = group_of(P, g);
+            if (G.p0 + G.ntok - 1 < P.topk) continue;  // dense: no scores
+            // the previous group's MMAs must be done reading the query tile
+            if (nq > 0 && !(ok = tc::mbar_wait(sm.bfree(), (nq - 1) & 1, abort_flag, err, 41, P.wait_limit))) break;
+            tc::mbar_arrive_expect_tx(sm.bfull(), C::B_BYTES);
+            for (int h = 0; h < C::HALVES; ++h)
+                tc::tma_load_2d(sm.Bt() + h * C::B_HALF, &tm_q, sm.bfull(), h * 64, G.r0 * HI);
+            ++nq;
+            for (int i = 0; i < G.nblk; ++i, ++it) {
+                const int st = it % C::STAGES;
+                if (!(ok = tc::mbar_wait(sm.empty(st), ((it / C::STAGES) & 1) ^ 1, abort_flag, err, 42, P.wait_limit)))
+                    break;
+                tc::mbar_arrive_expect_tx(sm.full(st), C::A_BYTES);
+                for (int h = 0; h < C::HALVES; ++h)
+                    tc::tma_load_2d(sm.As() + st * C::A_BYTES + h * C::A_HALF, &tm_k, sm.full(st), h * 64,
+                                    G.kbase + i * BM);
             }
-            // the next group's TMA loads (async proxy) overwrite the scratch these threads used
-            tc::fence_proxy_async_smem();
         }
-        ph.advance(mine);
-        __syncthreads();
+        // Drain: nothing may still be landing in shared memory when the CTA exits.
+        if (nq > 0) tc::mbar_wait(sm.bfull(), (nq - 1) & 1, nv, err, 43);
+        for (int i = max(0, it - C::STAGES); i < it; ++i)
+            tc::mbar_wait(sm.full(i % C::STAGES), (i / C::STAGES) & 1, nv, err, 44);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        int it = 0, ai = 0, nq = 0, issued = 0;
+        bool ok = true;
+        for (int j = 0; ok; ++j) {
+            const int g = walk_group(P, j);
+            if (g < 0) break;
+            const Group G = group_of(P, g);
+            if (G.p0 + G.ntok - 1 < P.topk) continue;
+            if (!(ok = tc::mbar_wait(sm.bfull(), nq & 1, abort_flag, err, 45, P.wait_limit))) break;
+            ++nq;
+            const uint32_t idesc = FP8 ? tc::instr_desc(tc::kFmtE4M3, tc::kFmtE4M3, BM, HI * G.ntok, 0, 0)
+                                       : tc::instr_desc(tc::kFmtBF16, tc::kFmtBF16, BM, HI * G.ntok, 0, 0);
+            for (int i = 0; i < G.nblk; ++i, ++it, ++ai) {
+                const int st = it % C::STAGES, acc = ai & 1;
+                if (!(ok = tc::mbar_wait(sm.tempty(acc), ((ai >> 1) & 1) ^ 1, abort_flag, err, 46, P.wait_limit)))
+                    break;
+                if (!(ok = tc::mbar_wait(sm.full(st), (it / C::STAGES) & 1, abort_flag, err, 47, P.wait_limit)))
+                    break;
+                tc::tc_fence_after();
+                const uint32_t d = tmem + acc * BN;
+                const uint32_t a0 = tc::smem_u32(sm.As() + st * C::A_BYTES), b0 = tc::smem_u32(sm.Bt());
+#pragma unroll
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    const int slab = FP8 ? 0 : kk / 4, off = (FP8 ? kk : kk % 4) * 32;
+                    const uint64_t ad = tc::smem_desc(a0 + slab * C::A_HALF + off, 16, 1024);
+                    const uint64_t bd = tc::smem_desc(b0 + slab * C::B_HALF + off, 16, 1024);
+                    if (FP8) tc::mma_f8(d, ad, bd, idesc, kk > 0);
+                    else tc::mma_f16(d, ad, bd, idesc, kk > 0);
+                }
+                tc::mma_commit(sm.empty(st));
+                tc::mma_commit(sm.tfull(acc));
+                ++issued;
+            }
+            if (!ok) break;
+            tc::mma_commit(sm.bfree());  // arrives once this group's MMAs are done: the query tile is free
+        }
+        // No MMA may still be running when the tensor memory is released.
+        if (issued > 0) {
+            tc::mma_commit(sm.mmadone());
+            tc::mbar_wait(sm.mmadone(), 0, nv, err, 48);
+        }
+    } else if (warp >= EPI_WARP0 && warp < SEL0) {
+        // ---------------- epilogue: scores into the slots ----------------
+        const int q = warp & 3;
+        int ai = 0;
+        for (int j = 0;; ++j) {
+            const int g = walk_group(P, j);
+            if (g < 0) break;
+            const Group G = group_of(P, g);
+            const bool dense = G.p0 + G.ntok - 1 < P.topk;
+            const int sb = j & 1;
+            // the selecting warps are done with this slot's previous group; all epilogue warps take
+            // the same decision (and have finished the previous group, whose weights are replaced next)
+            bool ok = j < 2 || tc::mbar_wait(sm.slot_free(sb), ((j >> 1) - 1) & 1, abort_flag, err, 49, P.wait_limit);
+            if (!bar_and<1, EPI * 32>(ok)) break;
+            if (!dense) {
+                load_weights<FP8, true>(sm, w, q_scale, P, G);
+                asm volatile("bar.sync 1, %0;" ::"n"(EPI * 32) : "memory");
+                float *out = slot0 + (int64_t)sb * TOK * P.ld;
+                for (int i = 0; i < G.nblk; ++i, ++ai) {
+                    const int acc = ai & 1;
+                    if (!(ok = tc::mbar_wait(sm.tfull(acc), (ai >> 1) & 1, abort_flag, err, 50, P.wait_limit))) break;
+                    tc::tc_fence_after();
+                    epilogue_block<FP8, true>(sm, tmem, acc, i * BM + q * 32 + lane, G, k_scale, out, P.ld);
+                }
+            }
+            tc::mbar_arrive(sm.slot_full(sb));  // releases this thread's score writes
+        }
+    } else if (warp >= SEL0) {
+        // ---------------- selection: the top-k of each filled slot ----------------
+        const int tid = (int)threadIdx.x - SEL0 * 32;
+        uint8_t *sc = sm.sel();
+        const tk::FilterSmem fs{(uint32_t *)sc, (int *)(sc + tk::MAX_BINS * 4), (int *)(sc + tk::MAX_BINS * 4 + 128),
+                                (int *)(sc + tk::MAX_BINS * 4 + 256), (uint32_t *)(sc + C::SEL_HEAD),
+                                (int32_t *)(sc + C::SEL_HEAD + C::CAND_CAP * 4), C::CAND_CAP};
+        for (int j = 0;; ++j) {
+            const int g = walk_group(P, j);
+            if (g < 0) break;
+            const Group G = group_of(P, g);
+            const int sb = j & 1;
+            // one decision for the four selecting warps (their selection synchronises on barrier 2)
+            if (!bar_and<2, NS>(tc::mbar_wait(sm.slot_full(sb), (j >> 1) & 1, abort_flag, err, 51, P.wait_limit)))
+                break;
+            const float *slot = slot0 + (int64_t)sb * TOK * P.ld;
+            for (int tt = 0; tt < G.ntok; ++tt)
+                tk::sampled_row<NS, 2, false>(tid, slot + (int64_t)tt * P.ld, min(G.p0 + tt + 1, G.S), P.topk, true,
+                                             idx + (int64_t)(G.r0 + tt) * P.topk, fs);
+            tc::mbar_arrive(sm.slot_free(sb));  // the reads of this slot are done
+        }
     }
     __syncthreads();
     pdl_trigger();
@@ -576,18 +734,32 @@ int indexer_topk_groups(const SeqTab &st) {
     return g;
 }
 
-std::atomic<int> g_fused_topk{0};
+// -1: automatic (default), 0: never, 1: wherever the fused kernel applies.
+std::atomic<int> g_fused_topk{-1};
 
 bool indexer_topk_fused_ok(int dtype, int H_I, int D_I, const SeqTab &st, int k) {
-    // Switched on, enough groups to fill the GPU (few groups -- decode -- split each group's key
-    // blocks over many CTAs instead, and select afterwards), and candidate lists that fit the scratch.
-    return g_fused_topk.load(std::memory_order_relaxed) != 0 && indexer_tc_supported(dtype, H_I, D_I) &&
-           indexer_topk_groups(st) >= SPLIT_TAB && k <= 8192;
+    // Applies with enough groups to fill the GPU (few groups -- decode -- split each group's key
+    // blocks over many CTAs instead, and select afterwards) and candidate lists that fit the scratch.
+    const int mode = g_fused_topk.load(std::memory_order_relaxed);
+    if (mode == 0 || !indexer_tc_supported(dtype, H_I, D_I) || indexer_topk_groups(st) < SPLIT_TAB || k > 8192)
+        return false;
+    if (mode == 1) return true;
+    // Automatic: where it measured faster on the GB300 -- the FP8 indexer over rows that see on
+    // average at least 16K keys (the chunked prefill: 24.0 against 25.2 ms of indexer + top-k).  The
+    // bf16 variant runs 8 epilogue warps and 3 stages (16 and 4 in the one-shot kernel, which the
+    // selection's shared memory and registers leave no room for) and was slower.
+    double live = 0.0, rows = 0.0;
+    for (int b = 0; b < st.B; ++b) {
+        const double T = st.q_off[b + 1] - st.q_off[b], p0 = st.start_pos[b];
+        live += T * p0 + T * (T + 1) / 2;
+        rows += T;
+    }
+    return dtype == DSA_E4M3 && rows > 0 && live >= 16384.0 * rows;
 }
 
 size_t indexer_topk_slot_bytes(const SeqTab &st, int64_t ld) {
     const int grid = std::min(indexer_topk_groups(st), device_sm_count());
-    return (size_t)grid * TOK * ld * sizeof(float);
+    return (size_t)grid * 2 * TOK * ld * sizeof(float);
 }
 
 cudaError_t launch_indexer_topk_tc(const void *q, const float *q_scale, const void *k, const float *k_scale, int dtype,
@@ -606,18 +778,19 @@ cudaError_t launch_indexer_topk_tc(const void *q, const float *q_scale, const vo
     cudaError_t e;
     if (fp8) {
         e = cudaFuncSetAttribute(indexer_topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg<true>::SMEM);
+                                 Cfg<true, true>::SMEM);
         if (e != cudaSuccess) return e;
-        e = launch_pdl(indexer_topk_kernel<true>, dim3(grid), dim3(num_threads<true>()), Cfg<true>::SMEM, s, tq, tk, w,
-                       q_scale, k_scale, P, slots, idx);
+        e = launch_pdl(indexer_topk_kernel<true>, dim3(grid), dim3(num_threads<true, true>()), Cfg<true, true>::SMEM, s,
+                       tq, tk, w, q_scale, k_scale, P, slots, idx);
         if (e != cudaSuccess) return e;
         note_launch(DSA_KERNEL_INDEXER_FP8 | DSA_KERNEL_INDEXER_TOPK);
     } else {
         e = cudaFuncSetAttribute(indexer_topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg<false>::SMEM);
+                                 Cfg<false, true>::SMEM);
         if (e != cudaSuccess) return e;
-        e = launch_pdl(indexer_topk_kernel<false>, dim3(grid), dim3(num_threads<false>()), Cfg<false>::SMEM, s, tq,
-                       tk, w, (const float *)nullptr, (const float *)nullptr, P, slots, idx);
+        e = launch_pdl(indexer_topk_kernel<false>, dim3(grid), dim3(num_threads<false, true>()),
+                       Cfg<false, true>::SMEM, s, tq, tk, w, (const float *)nullptr, (const float *)nullptr, P, slots,
+                       idx);
         if (e != cudaSuccess) return e;
         note_launch(DSA_KERNEL_INDEXER_TC | DSA_KERNEL_INDEXER_TOPK);
     }
@@ -626,7 +799,8 @@ cudaError_t launch_indexer_topk_tc(const void *q, const float *q_scale, const vo
 
 }  // namespace dsa
 
-extern "C" int dsa_set_fused_topk(int on) {
-    dsa::g_fused_topk.store(on ? 1 : 0, std::memory_order_relaxed);
+extern "C" int dsa_set_fused_topk(int mode) {
+    if (mode < -1 || mode > 1) return DSA_ERR_INVALID_ARG;
+    dsa::g_fused_topk.store(mode, std::memory_order_relaxed);
     return DSA_OK;
 }

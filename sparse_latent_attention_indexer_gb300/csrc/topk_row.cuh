@@ -31,7 +31,8 @@ __device__ __forceinline__ void group_sync() {
 }
 
 // One score: through the read-only path (NC, for rows written before the kernel started) or from
-// L2, bypassing L1 (rows the same CTA has just written, after a barrier that orders the writes).
+// L2, bypassing L1 (rows the same CTA has just written, after a barrier or an mbarrier wait that
+// orders the writes; volatile with a memory clobber, so the compiler keeps them after it).
 template <bool NC>
 __device__ __forceinline__ float ld_score(const float *p) {
     if constexpr (NC) {
@@ -124,8 +125,9 @@ __device__ __forceinline__ void find_bin_from_top(int tid, const uint32_t *hist,
 
 // Exact top-k of n keys (key_at(j), j in index order); idx_at(j) is the row index stored for
 // entry j.  Three histogram passes (11 + 11 + 10 bits) find the k-th key T, then one ordered pass
-// writes the keys above T and the first keys equal to T.
-template <int NT, int BAR, class KeyAt, class IdxAt>
+// writes the keys above T and the first keys equal to T.  In the ordered pass each thread takes LO
+// consecutive keys per step, so a group of few threads needs fewer barriers.
+template <int NT, int BAR, class KeyAt, class IdxAt, int LO = 1>
 __device__ __forceinline__ void radix_select_write(int tid, KeyAt key_at, IdxAt idx_at, int n, int k,
                                                    int32_t *__restrict__ out, uint32_t *hist, int *warp_gt,
                                                    int *warp_eq, int *shared3) {
@@ -156,17 +158,30 @@ __device__ __forceinline__ void radix_select_write(int tid, KeyAt key_at, IdxAt 
     const uint32_t T = prefix;
     const int n_gt = k - remaining;
     int base_gt = 0, base_eq = 0;
-    for (int s0 = 0; s0 < n; s0 += NT) {
+    for (int s0 = 0; s0 < n; s0 += NT * LO) {
         if (base_gt >= n_gt && base_eq >= remaining) break;  // group-uniform: every slot is written
-        const int s = s0 + tid;
-        const uint32_t u = s < n ? key_at(s) : 0u;
-        const bool gt = s < n && u > T;
-        const bool eq = s < n && u == T;
-        const uint32_t bg = __ballot_sync(0xffffffffu, gt), be = __ballot_sync(0xffffffffu, eq);
-        const uint32_t lt_mask = (1u << lane) - 1u;
-        if (lane == 0) {
-            warp_gt[wid] = __popc(bg);
-            warp_eq[wid] = __popc(be);
+        const int s = s0 + tid * LO;
+        uint32_t fg = 0, fe = 0;  // bit j: key s + j is above T / equal to T
+#pragma unroll
+        for (int j = 0; j < LO; ++j)
+            if (s + j < n) {
+                const uint32_t u = key_at(s + j);
+                fg |= (u > T ? 1u : 0u) << j;
+                fe |= (u == T ? 1u : 0u) << j;
+            }
+        const int cg = __popc(fg), ce = __popc(fe);
+        int ig = cg, ie = ce;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int vg = __shfl_up_sync(0xffffffffu, ig, o), ve = __shfl_up_sync(0xffffffffu, ie, o);
+            if (lane >= o) {
+                ig += vg;
+                ie += ve;
+            }
+        }
+        if (lane == 31) {
+            warp_gt[wid] = ig;
+            warp_eq[wid] = ie;
         }
         group_sync<NT, BAR>();
         int off_gt = 0, off_eq = 0, tot_gt = 0, tot_eq = 0;
@@ -177,13 +192,17 @@ __device__ __forceinline__ void radix_select_write(int tid, KeyAt key_at, IdxAt 
             tot_gt += warp_gt[w];
             tot_eq += warp_eq[w];
         }
-        if (gt) {
-            const int rank = base_gt + off_gt + __popc(bg & lt_mask);
-            if (rank < n_gt) out[rank] = idx_at(s);
-        }
-        if (eq) {
-            const int rank = base_eq + off_eq + __popc(be & lt_mask);
-            if (rank < remaining) out[n_gt + rank] = idx_at(s);
+        int rg = base_gt + off_gt + ig - cg, re = base_eq + off_eq + ie - ce;
+#pragma unroll
+        for (int j = 0; j < LO; ++j) {
+            if ((fg >> j) & 1u) {
+                if (rg < n_gt) out[rg] = idx_at(s + j);
+                ++rg;
+            }
+            if ((fe >> j) & 1u) {
+                if (re < remaining) out[n_gt + re] = idx_at(s + j);
+                ++re;
+            }
         }
         base_gt += tot_gt;
         base_eq += tot_eq;
@@ -279,6 +298,131 @@ __device__ __forceinline__ void filter_row(int tid, const float *__restrict__ ro
         radix_select_write<NT, BAR>(tid, [&](int j) { return ordered_key(ld_score<NC>(row + j)); },
                                     [&](int j) { return j; }, n_live, k, out, hist, sm.warp_gt, sm.warp_eq,
                                     sm.shared3);
+    }
+}
+
+// The r-th largest (1-based) of n keys key_at(0 .. n-1): three histogram passes of 11 + 11 + 10 bits.
+template <int NT, int BAR, class KeyAt>
+__device__ __forceinline__ uint32_t kth_largest_key(int tid, KeyAt key_at, int n, int r, uint32_t *hist,
+                                                    int *warp_sum, int *shared3) {
+    uint32_t prefix = 0, pmask = 0;
+    int remaining = r;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int nb = pass == 2 ? 1024 : 2048;
+        for (int b = tid; b < nb; b += NT) hist[b] = 0;
+        group_sync<NT, BAR>();
+        for (int s = tid; s < n; s += NT) {
+            const uint32_t u = key_at(s);
+            if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
+        }
+        group_sync<NT, BAR>();
+        find_bin_from_top<NT, BAR>(tid, hist, nb, remaining, shared3, warp_sum);
+        remaining -= shared3[1];
+        prefix |= (uint32_t)shared3[0] << shift;
+        pmask |= (uint32_t)(nb - 1) << shift;
+        group_sync<NT, BAR>();
+    }
+    return prefix;
+}
+
+// Compacts, in index order, the keys of row[0 .. n_live) whose ordered key is >= thr into the
+// candidate list (at most sm.cap of them are stored); returns how many there are.
+template <int NT, int BAR, bool NC, int L>
+__device__ __forceinline__ int compact_at_least(int tid, const float *__restrict__ row, int n_live, bool vec,
+                                                uint32_t thr, const FilterSmem &sm) {
+    constexpr int WARPS = NT / 32;
+    const int lane = tid & 31, wid = tid >> 5;
+    int base = 0;
+#pragma unroll 1
+    for (int s0 = 0; s0 < n_live; s0 += NT * L) {
+        const int first = s0 + tid * L;
+        uint32_t u[L], valid = 0;
+        if (first < n_live) load_keys<NC, L>(row, first, n_live, vec, u, valid);
+        uint32_t take = 0;
+#pragma unroll
+        for (int j = 0; j < L; ++j) take |= (((valid >> j) & 1u) && u[j] >= thr) ? (1u << j) : 0u;
+        const int c = __popc(take);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) sm.warp_gt[wid] = incl;
+        group_sync<NT, BAR>();
+        int before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) {
+            before += w < wid ? sm.warp_gt[w] : 0;
+            total += sm.warp_gt[w];
+        }
+        int pos = base + before + incl - c;
+#pragma unroll
+        for (int j = 0; j < L; ++j)
+            if ((take >> j) & 1u) {
+                if (pos < sm.cap) {
+                    sm.cand[pos] = u[j];
+                    sm.cand_idx[pos] = first + j;
+                }
+                ++pos;
+            }
+        base += total;
+        group_sync<NT, BAR>();  // warp_gt is rewritten by the next step
+    }
+    return base;
+}
+
+// The same output as filter_row, for a group of few threads that selects right after the scores
+// were written (the fused indexer): a row that fits the candidate list is copied in whole; a longer
+// row gets its threshold from a strided sample of SAMPLE keys -- the r-th largest sample with r a
+// few standard deviations above the expected count of sampled keys among the top k -- so that one
+// streaming pass (no histogram of the whole row) keeps every key at or above it.  That set holds
+// the top k whenever it has at least k keys, and the exact radix select runs on it; otherwise (or
+// when it overflows the list) the select runs on the whole row.
+template <int NT, int BAR, bool NC, int L = SPT>
+__device__ __forceinline__ void sampled_row(int tid, const float *__restrict__ row, int n_live, int k, bool vec,
+                                            int32_t *__restrict__ out, const FilterSmem &sm) {
+    constexpr int SAMPLE = 1024;
+    if (n_live <= k) {
+        for (int j = tid; j < k; j += NT) out[j] = j < n_live ? j : -1;
+        return;
+    }
+    uint32_t thr = 0;  // every finite or -inf score maps above 0
+    if (n_live > sm.cap) {
+        constexpr int PER = (SAMPLE + NT - 1) / NT;
+        float v[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {  // every load in flight before the first is used
+            const int j = tid + i * NT;
+            v[i] = j < SAMPLE ? ld_score<NC>(row + (int)(((int64_t)j * n_live) / SAMPLE)) : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+            if (tid + i * NT < SAMPLE) sm.cand[tid + i * NT] = ordered_key(v[i]);
+        group_sync<NT, BAR>();
+        const float mu = (float)SAMPLE * (float)k / (float)n_live;
+        const int r = min(SAMPLE, (int)ceilf(mu + 4.0f * sqrtf(mu) + 8.0f));
+        const uint32_t *smp = sm.cand;
+        thr = kth_largest_key<NT, BAR>(tid, [&](int j) { return smp[j]; }, SAMPLE, r, sm.hist, sm.warp_eq,
+                                       sm.shared3);
+    }
+    const int n_cand = compact_at_least<NT, BAR, NC, L>(tid, row, n_live, vec, thr, sm);
+    if (n_cand >= k && n_cand <= sm.cap) {
+        const uint32_t *cand = sm.cand;
+        const int32_t *cidx = sm.cand_idx;
+        auto key_at = [&](int j) { return cand[j]; };
+        auto idx_at = [&](int j) { return cidx[j]; };
+        radix_select_write<NT, BAR, decltype(key_at), decltype(idx_at), 8>(tid, key_at, idx_at, n_cand, k, out,
+                                                                            sm.hist, sm.warp_gt, sm.warp_eq,
+                                                                            sm.shared3);
+    } else {
+        auto key_at = [&](int j) { return ordered_key(ld_score<NC>(row + j)); };
+        auto idx_at = [&](int j) { return j; };
+        radix_select_write<NT, BAR, decltype(key_at), decltype(idx_at), 8>(tid, key_at, idx_at, n_live, k, out,
+                                                                            sm.hist, sm.warp_gt, sm.warp_eq,
+                                                                            sm.shared3);
     }
 }
 

@@ -136,3 +136,11 @@ def test_wait_limit_range():
     assert lib.dsa_set_wait_limit((1 << 32) + 1) == _abi.DSA_ERR_INVALID_ARG
     assert lib.dsa_set_wait_limit(1000) == _abi.DSA_OK
     assert lib.dsa_set_wait_limit(0) == _abi.DSA_OK  # back to the default
+
+
+def test_fused_topk_modes():
+    lib = _abi.load()
+    for m in (1, 0, -1):
+        assert lib.dsa_set_fused_topk(m) == _abi.DSA_OK
+    assert lib.dsa_set_fused_topk(2) == _abi.DSA_ERR_INVALID_ARG
+    assert lib.dsa_set_fused_topk(-2) == _abi.DSA_ERR_INVALID_ARG

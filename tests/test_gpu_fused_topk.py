@@ -44,7 +44,7 @@ def test_fused_selection_equals_unfused(fp8):
         out, lse, idx = H.gpu_forward(wl, t)
         kern = dsa.last_kernels()
     finally:
-        dsa.dsa_set_fused_topk(False)
+        dsa.dsa_set_fused_topk(-1)
     assert dsa.dsa_check_device_error() == (0, 0)
     assert "indexer_topk" in kern and "topk" not in kern, kern
     ref = _unfused_idx(wl, t)
