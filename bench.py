@@ -87,8 +87,11 @@ def ncu_traffic(stage: str, workload: str):
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        entry = json.load(f).get(stage)
-    if not entry or entry.get("workload") != workload:
+        entries = json.load(f).get(stage) or []
+    if isinstance(entries, dict):
+        entries = [entries]
+    entry = next((e for e in entries if e.get("workload") == workload), None)
+    if entry is None:
         return None
     srcs = entry["sources"]
     if not all(os.path.exists(os.path.join(ROOT, p)) for p in srcs) or source_digest(srcs) != entry["sha256"]:

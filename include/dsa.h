@@ -60,7 +60,7 @@ typedef enum dsa_dtype {
 } dsa_dtype;
 
 /* Largest number of sequences in one call. */
-#define DSA_MAX_SEQS 512
+#define DSA_MAX_SEQS 1024
 
 /* A batch of sequences.  All three arrays are HOST memory, read during the
  * call only (the library copies what the kernels need into their launch

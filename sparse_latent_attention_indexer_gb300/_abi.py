@@ -9,7 +9,7 @@ LIB_PATH = os.path.join(HERE, "libdsa.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR_WORKSPACE = range(6)
 DSA_F32, DSA_BF16, DSA_E4M3 = 0, 1, 2
-DSA_MAX_SEQS = 512
+DSA_MAX_SEQS = 1024
 DSA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 KERNEL_BITS = {

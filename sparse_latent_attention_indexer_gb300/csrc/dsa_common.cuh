@@ -19,6 +19,7 @@ struct SeqTab {
     int k_len[DSA_MAX_SEQS];      // keys of each sequence
     int start_pos[DSA_MAX_SEQS];  // position of each sequence's first row in this launch
 };
+static_assert(sizeof(SeqTab) + 1024 <= 32764, "a sequence table travels in a kernel's launch parameters");
 
 // Largest b with q_off[b] <= r: the sequence that owns query row r (empty
 // sequences are skipped because their successor has the same offset).

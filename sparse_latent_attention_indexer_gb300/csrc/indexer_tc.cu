@@ -100,6 +100,7 @@ struct IdxParams {
     float c;
     int topk;  // the fused kernel: k of the selection
 };
+static_assert(sizeof(IdxParams) + 256 <= 32764, "launch parameters");
 
 // One group: 4 consecutive query rows of one sequence.
 struct Group {

@@ -98,6 +98,7 @@ struct MlaParams {
     float scale_log2;  // softmax scale * log2(e)
     long long wait_limit;  // SM cycles a wait may take before the CTA gives up (the drains keep the default)
 };
+static_assert(sizeof(MlaParams) + 256 <= 32764, "launch parameters");
 
 __device__ __forceinline__ int find_seq(const MlaParams &P, int r) {
     int lo = 0, hi = P.B - 1;

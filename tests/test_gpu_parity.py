@@ -428,3 +428,22 @@ def test_attention_stage_tensor_core_matches_generic(name, monkeypatch):
     monkeypatch.delenv("DSA_FORCE_GENERIC")
     assert (fast.float() - gen.float()).abs().max().item() <= H.OUT_ATOL_BF16
     assert (lf - lg).abs().max().item() <= H.LSE_ATOL_BF16
+
+
+def test_forward_decode_batch_beyond_512_sequences():
+    """A decode step of 700 sequences (one query each, caches of 300..3000 keys, top-256): more
+    sequences than one launch carried before; sampled rows match the oracle's whole path."""
+    g = torch.Generator().manual_seed(77)
+    S = [int(x) for x in torch.randint(300, 3000, (700,), generator=g)]
+    wl = di.generate("decode-700", di.Shape(k=256), 77, [1] * len(S), S, [s - 1 for s in S])
+    t = H.to_device(wl)
+    out, lse, idx = H.gpu_forward(wl, t)
+    st, site = dsa.dsa_check_device_error()
+    assert st == 0, (st, site)
+    rows = di.sample_rows(wl, 24)
+    ref = H.oracle_rows(wl, rows)
+    out_np, idx_np = out.float().cpu().numpy(), idx.cpu().numpy()
+    for r in rows:
+        o = ref[r]
+        H.check_selection_row(idx_np[r], o["scores"], o["absterm"], o["pos"], wl.shape.k)
+        assert np.abs(out_np[r] - o["out"]).max() <= H.OUT_ATOL_BF16
