@@ -356,6 +356,45 @@ typedef struct dsa_problem {
 size_t dsa_forward_workspace_size(const dsa_problem *p, const dsa_seqs *seqs);
 int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, size_t ws_bytes, void *stream);
 
+/* The forward from HOST buffers: the end-to-end call of one step.  On `stream`
+ * it copies the step's inputs from host memory into the device buffers that
+ * `p` names, runs dsa_forward, and copies the results back -- one
+ * cudaMemcpyAsync per contiguous piece, in the order listed here.  With
+ * page-locked (pinned) host buffers every copy is asynchronous and the call
+ * returns once all the work is enqueued; the caller synchronises `stream`
+ * before reading the host outputs.  Pageable host memory also works, but then
+ * the copies block the calling thread.
+ *
+ * Host inputs (NULL: the device buffer already holds that data):
+ *   q_idx, w, q_nope, q_pe   the step's queries, laid out as the device tensors
+ *                            of `p` ([sum T, ...] rows, dense);
+ *   kv_new                   the cache rows the step appends: for every
+ *                            sequence b in order, its rows start_pos[b] ..
+ *                            S_b - 1 (S_b = cu_k[b+1] - cu_k[b]), each a full
+ *                            row of ld_kv elements (bytes for an e4m3 cache),
+ *                            written to cache rows cu_k[b] + start_pos[b] ..;
+ *   k_pe_new                 the same rows of k_pe (ld_pe elements each); NULL
+ *                            when k_pe lies inside the kv_cache rows that
+ *                            kv_new already carries;
+ *   k_idx_new                the same rows of the indexer key cache (D_I each);
+ *   kv_scale_new             e4m3 cache: the same rows' d_c / 128 scales.
+ * Host outputs (NULL: not copied back): out (y when p->wo is set: the
+ * projected output), lse, idx (requires p->idx_out).
+ * Returns what dsa_forward returns, DSA_ERR_INVALID_ARG when a sequence has
+ * start_pos[b] > S_b with kv_new, k_pe_new, k_idx_new or kv_scale_new given, or
+ * when a requested output has no device buffer in `p`, and DSA_ERR_CUDA when
+ * a copy cannot be enqueued. */
+typedef struct dsa_host_io {
+    const void *q_idx, *w, *q_nope, *q_pe;
+    const void *kv_new, *k_pe_new, *k_idx_new;
+    const float *kv_scale_new;
+    void *out;
+    float *lse;
+    int32_t *idx;
+} dsa_host_io;
+int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_io *io, void *workspace,
+                     size_t ws_bytes, void *stream);
+
 /* ------------------------------------------------------------------------
  * Status and diagnostics.
  * ---------------------------------------------------------------------- */

@@ -20,7 +20,7 @@ __all__ = [
     "Seqs", "DSAError", "dsa_quant_e4m3_ue8m0", "dsa_indexer_scores", "dsa_topk_select",
     "dsa_sparse_mla_workspace_size", "dsa_sparse_mla_fwd", "dsa_forward_workspace_size", "dsa_forward",
     "dsa_check_device_error", "dsa_selftest_bounded_wait", "dsa_set_wait_limit", "dsa_set_fused_topk", "dsa_kv_prologue",
-    "dsa_output_proj", "dsa_sparse_mla_fwd_fp8kv", "last_kernels", "last_launch_count", "build",
+    "dsa_output_proj", "dsa_sparse_mla_fwd_fp8kv", "dsa_forward_host", "last_kernels", "last_launch_count", "build",
 ]
 
 
@@ -314,6 +314,36 @@ def dsa_forward(q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, seqs:
     if wo is not None:
         return out, lse, idx_out, y
     return out, lse, idx_out
+
+
+def dsa_forward_host(host: dict, q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, seqs: Seqs, top_k: int,
+                     softmax_scale: float, idx_fp8: bool = False, out=None, lse=None, idx_out=None, workspace=None,
+                     stream=None, wo=None, y=None, kv_scale=None):
+    """One step from HOST tensors (the end-to-end call).  ``host`` maps names to CPU
+    tensors (pinned for asynchronous copies): inputs ``q_idx``, ``w``, ``q_nope``,
+    ``q_pe`` (the step's queries) and ``kv_new``, ``k_pe_new``, ``k_idx_new``,
+    ``kv_scale_new`` (the cache rows the step appends: rows start_pos[b] .. S_b - 1
+    of every sequence, concatenated), outputs ``out`` (y with wo), ``lse``, ``idx``;
+    a missing name is not copied.  The device tensors are the buffers the copies fill
+    and the forward reads and writes.  Everything is enqueued on ``stream``; returns
+    without synchronising."""
+    lib = _abi.load()
+    p = _problem(q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, top_k, softmax_scale, idx_fp8, out, lse,
+                 idx_out, wo, y, kv_scale)
+    io = _abi.dsa_host_io()
+    for name in ("q_idx", "w", "q_nope", "q_pe", "kv_new", "k_pe_new", "k_idx_new", "kv_scale_new", "out", "lse",
+                 "idx"):
+        ten = host.get(name)
+        if ten is not None:
+            if ten.device.type != "cpu" or not ten.is_contiguous():
+                raise ValueError(f"host tensor {name} must be a contiguous CPU tensor")
+            setattr(io, name, ten.data_ptr())
+    need = dsa_forward_workspace_size(p, seqs)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q_nope.device)
+    st = lib.dsa_forward_host(ctypes.byref(p), seqs.ref(), ctypes.byref(io), _ptr(workspace), workspace.numel(),
+                              _stream(stream))
+    _check("dsa_forward_host", st)
 
 
 def set_stage_events(events):

@@ -41,6 +41,15 @@ class dsa_problem(ctypes.Structure):
     ]
 
 
+class dsa_host_io(ctypes.Structure):
+    _fields_ = [
+        ("q_idx", ctypes.c_void_p), ("w", ctypes.c_void_p), ("q_nope", ctypes.c_void_p), ("q_pe", ctypes.c_void_p),
+        ("kv_new", ctypes.c_void_p), ("k_pe_new", ctypes.c_void_p), ("k_idx_new", ctypes.c_void_p),
+        ("kv_scale_new", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("idx", ctypes.c_void_p),
+    ]
+
+
 # (name, restype, argtypes) of every exported function
 P, I, I64, F, SZ, U32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint32
 SEQS = ctypes.POINTER(dsa_seqs)
@@ -58,6 +67,7 @@ SIGNATURES = [
     ("dsa_output_proj", I, [P, P, I, I, I, P, P]),
     ("dsa_forward_workspace_size", SZ, [PROB, SEQS]),
     ("dsa_forward", I, [PROB, SEQS, P, SZ, P]),
+    ("dsa_forward_host", I, [PROB, SEQS, ctypes.POINTER(dsa_host_io), P, SZ, P]),
     ("dsa_status_string", ctypes.c_char_p, [I]),
     ("dsa_last_cuda_error", I, []),
     ("dsa_check_device_error", I, [P, ctypes.POINTER(ctypes.c_int)]),

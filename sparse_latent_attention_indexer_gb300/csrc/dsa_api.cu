@@ -571,4 +571,60 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
                    true, true, p->wo, p->d_model, p->y, ws + L.obuf, p->kv_fp8 ? p->kv_scale : nullptr);
 }
 
+int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_io *io, void *workspace,
+                     size_t ws_bytes, void *stream) {
+    if (!io) return DSA_ERR_INVALID_ARG;
+    int rc = check_problem(p);
+    if (rc) return rc;
+    Batch bt;
+    if ((rc = build_batch(seqs, bt))) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t esz = p->dtype == DSA_F32 ? 4 : 2;
+    const size_t T = (size_t)bt.total_q;
+    const bool appends = io->kv_new || io->k_pe_new || io->k_idx_new || io->kv_scale_new;
+    if (appends)
+        for (int b = 0; b < bt.st.B; ++b)
+            if (bt.st.start_pos[b] > bt.st.k_len[b]) return DSA_ERR_INVALID_ARG;
+    if ((io->kv_new && !p->kv_cache) || (io->k_pe_new && !p->k_pe) || (io->k_idx_new && !p->k_idx) ||
+        (io->kv_scale_new && (!p->kv_fp8 || !p->kv_scale)) || (io->lse && !p->lse) || (io->idx && !p->idx_out) ||
+        (io->out && !(p->wo ? p->y : p->out)))
+        return DSA_ERR_INVALID_ARG;
+    cudaError_t e = cudaSuccess;
+    auto put = [&](const void *dev, const void *host, size_t bytes) {
+        if (e == cudaSuccess && host && bytes) e = cudaMemcpyAsync((void *)dev, host, bytes, cudaMemcpyHostToDevice, s);
+    };
+    put(p->q_idx, io->q_idx, T * p->H_I * p->D_I * esz);
+    put(p->w, io->w, T * p->H_I * sizeof(float));
+    put(p->q_nope, io->q_nope, T * p->H * p->d_n * esz);
+    put(p->q_pe, io->q_pe, T * p->H * p->d_r * esz);
+    // Appended cache rows: one contiguous piece per sequence and array.
+    const size_t kv_row = (size_t)p->ld_kv * (p->kv_fp8 ? 1 : esz), pe_row = (size_t)p->ld_pe * esz,
+                 ki_row = (size_t)p->D_I * esz, sc_row = (size_t)(p->d_c / 128) * sizeof(float);
+    size_t done = 0;  // appended rows before sequence b
+    for (int b = 0; b < bt.st.B && appends; ++b) {
+        const size_t r0 = (size_t)bt.st.k_base[b] + bt.st.start_pos[b];
+        const size_t n = (size_t)(bt.st.k_len[b] - bt.st.start_pos[b]);
+        if (io->kv_new) put((const char *)p->kv_cache + r0 * kv_row, (const char *)io->kv_new + done * kv_row, n * kv_row);
+        if (io->k_pe_new)
+            put((const char *)p->k_pe + r0 * pe_row, (const char *)io->k_pe_new + done * pe_row, n * pe_row);
+        if (io->k_idx_new)
+            put((const char *)p->k_idx + r0 * ki_row, (const char *)io->k_idx_new + done * ki_row, n * ki_row);
+        if (io->kv_scale_new)
+            put((const char *)p->kv_scale + r0 * sc_row, (const char *)io->kv_scale_new + done * sc_row, n * sc_row);
+        done += n;
+    }
+    if (e != cudaSuccess) return fail_cuda(e);
+    if ((rc = dsa_forward(p, seqs, workspace, ws_bytes, stream))) return rc;
+    auto get = [&](void *host, const void *dev, size_t bytes) {
+        if (e == cudaSuccess && host && bytes) e = cudaMemcpyAsync(host, dev, bytes, cudaMemcpyDeviceToHost, s);
+    };
+    if (p->wo)
+        get(io->out, p->y, T * p->d_model * esz);
+    else
+        get(io->out, p->out, T * p->H * p->d_v * esz);
+    get(io->lse, p->lse, T * p->H * sizeof(float));
+    get(io->idx, p->idx_out, T * p->top_k * sizeof(int32_t));
+    return e == cudaSuccess ? DSA_OK : fail_cuda(e);
+}
+
 }  // extern "C"

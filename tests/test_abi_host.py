@@ -144,3 +144,29 @@ def test_fused_topk_modes():
         assert lib.dsa_set_fused_topk(m) == _abi.DSA_OK
     assert lib.dsa_set_fused_topk(2) == _abi.DSA_ERR_INVALID_ARG
     assert lib.dsa_set_fused_topk(-2) == _abi.DSA_ERR_INVALID_ARG
+
+
+def test_forward_host_validates_before_any_copy():
+    """dsa_forward_host checks its host/device pairing and the appended-row
+    ranges on the host and returns before enqueueing a copy (no GPU here)."""
+    lib = _abi.load()
+    H = ctypes.c_void_p(1 << 16)
+    s = _seqs([4], [8], [4])
+    p = _problem()
+    assert lib.dsa_forward_host(ctypes.byref(p), s.ref(), None, None, 0, None) == _abi.DSA_ERR_INVALID_ARG
+    # an lse or idx copy-back needs the device buffer it reads
+    io = _abi.dsa_host_io(lse=H.value)
+    assert lib.dsa_forward_host(ctypes.byref(p), s.ref(), ctypes.byref(io), None, 0, None) == _abi.DSA_ERR_INVALID_ARG
+    io = _abi.dsa_host_io(idx=H.value)
+    assert lib.dsa_forward_host(ctypes.byref(p), s.ref(), ctypes.byref(io), None, 0, None) == _abi.DSA_ERR_INVALID_ARG
+    # scales only for an e4m3 latent cache
+    io = _abi.dsa_host_io(kv_scale_new=H.value)
+    assert lib.dsa_forward_host(ctypes.byref(p), s.ref(), ctypes.byref(io), None, 0, None) == _abi.DSA_ERR_INVALID_ARG
+    # appended rows start_pos .. S-1 need start_pos <= S
+    bad = _seqs([1], [3], [5])
+    io = _abi.dsa_host_io(kv_new=H.value)
+    assert lib.dsa_forward_host(ctypes.byref(p), bad.ref(), ctypes.byref(io), None, 0, None) == _abi.DSA_ERR_INVALID_ARG
+    # the problem itself is checked as dsa_forward checks it
+    io = _abi.dsa_host_io()
+    p_bad = _problem(dtype=_abi.DSA_E4M3)
+    assert lib.dsa_forward_host(ctypes.byref(p_bad), s.ref(), ctypes.byref(io), None, 0, None) != _abi.DSA_OK

@@ -1,0 +1,86 @@
+"""dsa_forward_host: one step from host buffers.  The step's queries and the
+cache rows it appends are copied in from pinned host memory, the forward runs,
+and the outputs come back to host memory.  On the same inputs the host outputs
+must equal, bit for bit, the outputs of dsa_forward on device-resident inputs,
+and the appended rows must land in the device caches at rows
+cu_k[b] + start_pos[b] .. cu_k[b+1] - 1 while the rows before them (the cache
+earlier steps left) are untouched."""
+import pytest
+import torch
+
+import dsa_inputs as di
+import sparse_latent_attention_indexer_gb300 as dsa
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+def _appended(wl, x):
+    """The rows start_pos[b] .. S_b - 1 of every sequence of a [sum S, ...] host tensor, in order."""
+    return torch.cat([x[wl.cu_k[b] + wl.start_pos[b]:wl.cu_k[b + 1]] for b in range(wl.B)]).contiguous()
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_forward_from_host_buffers_equals_device_forward(fp8):
+    shape = di.Shape(k=128, idx_fp8=fp8)
+    # chunked prefill: three sequences with resident prefixes and new rows; one decode-like row
+    wl = di.generate(f"host-io-{fp8}", shape, 71, [300, 96, 1], [1500, 96, 2200], [1200, 0, 2199])
+    sh = wl.shape
+    ref = H.to_device(wl)
+    out_r, lse_r, idx_r = H.gpu_forward(wl, ref)
+    assert dsa.dsa_check_device_error() == (0, 0)
+
+    host = wl.tensors
+    # device buffers: the cache rows before start_pos are resident, the appended rows and the
+    # queries hold garbage until the call copies them in
+    dev = {k: torch.full_like(ref[k], 7.0) for k in ("qI", "w", "q_nope", "q_pe")}
+    for k in ("kv_cache", "kI"):
+        buf = ref[k].clone()
+        for b in range(wl.B):
+            buf[wl.cu_k[b] + wl.start_pos[b]:wl.cu_k[b + 1]] = -3.0
+        dev[k] = buf
+    d_c = sh.d_c
+    pinned = {
+        "q_idx": host["qI"].pin_memory(), "w": host["w"].pin_memory(), "q_nope": host["q_nope"].pin_memory(),
+        "q_pe": host["q_pe"].pin_memory(),
+        "kv_new": _appended(wl, host["kv_cache"]).pin_memory(),  # k_pe is inside the latent rows
+        "k_idx_new": _appended(wl, host["kI"]).pin_memory(),
+        "out": torch.empty(out_r.shape, dtype=out_r.dtype).pin_memory(),
+        "lse": torch.empty(lse_r.shape, dtype=lse_r.dtype).pin_memory(),
+        "idx": torch.empty(idx_r.shape, dtype=idx_r.dtype).pin_memory(),
+    }
+    out_d = torch.empty_like(out_r)
+    lse_d = torch.empty_like(lse_r)
+    idx_d = torch.empty_like(idx_r)
+    stream = torch.cuda.current_stream()
+    dsa.dsa_forward_host(pinned, dev["qI"], dev["kI"], dev["w"], dev["q_nope"], dev["q_pe"],
+                         dev["kv_cache"][:, :d_c], dev["kv_cache"][:, d_c:], ref["W_UK"], ref["W_UV"], H.seqs_of(wl),
+                         sh.k, sh.softmax_scale, idx_fp8=sh.idx_fp8, out=out_d, lse=lse_d, idx_out=idx_d,
+                         stream=stream)
+    stream.synchronize()
+    assert dsa.dsa_check_device_error() == (0, 0)
+    # the copies filled the device buffers: queries and appended rows as on the host, resident rows kept
+    for k in ("qI", "w", "q_nope", "q_pe", "kv_cache", "kI"):
+        assert torch.equal(dev[k], ref[k]), k
+    # the host outputs are the device forward's, bit for bit
+    assert torch.equal(pinned["idx"], idx_r.cpu())
+    assert torch.equal(pinned["out"], out_r.cpu())
+    assert torch.equal(pinned["lse"], lse_r.cpu())
+    assert torch.equal(out_d, out_r)
+
+
+def test_forward_from_host_pageable_and_partial_copies():
+    """Pageable host tensors work too (the copies then block), and an input left out
+    (NULL) is read from the device buffer as it stands."""
+    wl = di.generate("host-io-pageable", di.Shape(k=64), 72, [40, 9], [300, 9], [260, 0])
+    sh = wl.shape
+    ref = H.to_device(wl)
+    out_r, lse_r, idx_r = H.gpu_forward(wl, ref)
+    dev_q = torch.zeros_like(ref["q_nope"])
+    host = {"q_nope": wl.tensors["q_nope"].contiguous(), "out": torch.empty(out_r.shape, dtype=out_r.dtype)}
+    dsa.dsa_forward_host(host, ref["qI"], ref["kI"], ref["w"], dev_q, ref["q_pe"], ref["ckv"], ref["kpe"],
+                         ref["W_UK"], ref["W_UV"], H.seqs_of(wl), sh.k, sh.softmax_scale,
+                         out=torch.empty_like(out_r), lse=torch.empty_like(lse_r), idx_out=torch.empty_like(idx_r))
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_error() == (0, 0)
+    assert torch.equal(host["out"], out_r.cpu())
