@@ -714,10 +714,11 @@ def measure_e2e(args, dsa, torch, wl, host, t, seqs, out, lse, idx, ws, unit):
     rows start_pos .. S-1; the rows before start_pos are the cache the earlier
     steps left resident) -- runs the forward and copies the output back, all
     inside the timed events.  Two pipeline slots, each with its own stream and
-    device buffers, take alternate steps, so one step's copies overlap the other
-    slot's kernels (the copy engines and the SMs work at the same time); the
-    per-step time of one slot alone (copies and kernels back to back) is
-    reported beside it."""
+    device buffers, take alternate steps: the forwards run one after the other
+    (each call waits for the previous step's forward through the call's
+    compute events) while one step's copies overlap the other slot's kernels
+    (the copy engines and the SMs work at the same time); the per-step time of
+    one slot alone (copies and kernels back to back) is reported beside it."""
     sh = wl.shape
     cu_k = wl.cu_k
     new_rows = torch.cat([torch.arange(cu_k[b] + wl.start_pos[b], cu_k[b + 1]) for b in range(wl.B)])
@@ -738,24 +739,30 @@ def measure_e2e(args, dsa, torch, wl, host, t, seqs, out, lse, idx, ws, unit):
         slots.append({"dev": dev, "out": o, "lse": l, "idx": ix, "ws": w, "stream": torch.cuda.Stream(),
                       "host": dict(inputs, out=torch.empty(out.shape, dtype=out.dtype).pin_memory())})
 
-    def step(sl):
+    done = [torch.cuda.Event(), torch.cuda.Event()]  # the forward of the slot's last step is enqueued
+
+    def step(i, n_slots):
+        sl = slots[i % n_slots]
         d = sl["dev"]
+        # with two slots the forwards run one after the other (each waits for the previous step's),
+        # while the copies of one step overlap the kernels of the other
+        chain = {} if n_slots == 1 else {"compute_done": done[i % 2], "compute_after": done[(i + 1) % 2] if i else None}
         dsa.dsa_forward_host(sl["host"], d["qI"], d["kI"], d["w"], d["q_nope"], d["q_pe"], d["kv_cache"][:, :d_c],
                              d["kv_cache"][:, d_c:], d["W_UK"], d["W_UV"], seqs, sh.k, sh.softmax_scale,
                              idx_fp8=sh.idx_fp8, out=sl["out"], lse=sl["lse"], idx_out=sl["idx"], workspace=sl["ws"],
-                             stream=sl["stream"])
+                             stream=sl["stream"], **chain)
 
     def run(n_slots, steps, warmup):
         cur = torch.cuda.current_stream()
         for i in range(warmup):
-            step(slots[i % n_slots])
+            step(i, n_slots)
         torch.cuda.synchronize()
         s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s_ev.record(cur)
         for sl in slots[:n_slots]:
             sl["stream"].wait_event(s_ev)
-        for i in range(steps):
-            step(slots[i % n_slots])
+        for i in range(warmup, warmup + steps):
+            step(i, n_slots)
         for sl in slots[:n_slots]:
             cur.wait_stream(sl["stream"])
         e_ev.record(cur)
@@ -768,7 +775,7 @@ def measure_e2e(args, dsa, torch, wl, host, t, seqs, out, lse, idx, ws, unit):
     return {"value": wl.total_q / (ms / 1e3), "unit": unit, "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "serial_ms_per_step": serial, "serial_value": wl.total_q / (serial / 1e3),
-            "call": "dsa_forward_host (pinned host buffers), two pipeline slots on their own streams",
+            "call": "dsa_forward_host (pinned host buffers), two pipeline slots on their own streams, forwards chained",
             "inputs": "the step's queries (q^I, w, q_nope, q_pe) and the cache rows they append "
                       "(latent + k_pe, k^I); the earlier cache rows stay resident"}
 

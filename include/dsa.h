@@ -380,6 +380,12 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
  *   kv_scale_new             e4m3 cache: the same rows' d_c / 128 scales.
  * Host outputs (NULL: not copied back): out (y when p->wo is set: the
  * projected output), lse, idx (requires p->idx_out).
+ * Pipelining (both NULL: none): compute_after, a cudaEvent_t the forward
+ * waits for once the input copies are enqueued (cudaStreamWaitEvent), and
+ * compute_done, a cudaEvent_t recorded once the forward's kernels are
+ * enqueued, before the output copies.  Calls on two streams with their own
+ * device buffers can so chain their forwards (each waits for the other's
+ * compute_done) while one call's copies overlap the other's kernels.
  * Returns what dsa_forward returns, DSA_ERR_INVALID_ARG when a sequence has
  * start_pos[b] > S_b with kv_new, k_pe_new, k_idx_new or kv_scale_new given, or
  * when a requested output has no device buffer in `p`, and DSA_ERR_CUDA when
@@ -391,6 +397,7 @@ typedef struct dsa_host_io {
     void *out;
     float *lse;
     int32_t *idx;
+    void *compute_after, *compute_done;
 } dsa_host_io;
 int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_io *io, void *workspace,
                      size_t ws_bytes, void *stream);

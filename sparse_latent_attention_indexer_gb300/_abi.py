@@ -47,6 +47,7 @@ class dsa_host_io(ctypes.Structure):
         ("kv_new", ctypes.c_void_p), ("k_pe_new", ctypes.c_void_p), ("k_idx_new", ctypes.c_void_p),
         ("kv_scale_new", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("idx", ctypes.c_void_p),
+        ("compute_after", ctypes.c_void_p), ("compute_done", ctypes.c_void_p),
     ]
 
 

@@ -613,8 +613,10 @@ int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_
             put((const char *)p->kv_scale + r0 * sc_row, (const char *)io->kv_scale_new + done * sc_row, n * sc_row);
         done += n;
     }
+    if (e == cudaSuccess && io->compute_after) e = cudaStreamWaitEvent(s, (cudaEvent_t)io->compute_after, 0);
     if (e != cudaSuccess) return fail_cuda(e);
     if ((rc = dsa_forward(p, seqs, workspace, ws_bytes, stream))) return rc;
+    if (io->compute_done && (e = cudaEventRecord((cudaEvent_t)io->compute_done, s)) != cudaSuccess) return fail_cuda(e);
     auto get = [&](void *host, const void *dev, size_t bytes) {
         if (e == cudaSuccess && host && bytes) e = cudaMemcpyAsync(host, dev, bytes, cudaMemcpyDeviceToHost, s);
     };

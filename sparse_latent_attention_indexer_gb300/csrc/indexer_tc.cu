@@ -686,10 +686,20 @@ cudaError_t launch_indexer_tc(const void *q, const float *q_scale, const void *k
                 nblk[g] = (st.start_pos[b] + t0 + ntok - 1) / BM + 1;
                 total_blocks += nblk[g];
             }
-        const int target = (int)std::max<int64_t>(1, (total_blocks + SPLIT_TAB - 1) / SPLIT_TAB);
+        // One CTA per SM at a time: the CTA count must not pass SPLIT_TAB (two full waves), or a
+        // third, nearly empty wave of full-size CTAs would follow.  Rounding each group up can
+        // overshoot, so the blocks per CTA grow until the count fits.
+        int target = (int)std::max<int64_t>(1, (total_blocks + SPLIT_TAB - 1) / SPLIT_TAB);
         int per_cta[SPLIT_TAB], sp[SPLIT_TAB];
+        for (;; ++target) {
+            int ctas = 0;
+            for (int g = 0; g < P.total_groups; ++g) {
+                sp[g] = std::max(1, std::min(nblk[g], (nblk[g] + target - 1) / target));
+                ctas += sp[g];
+            }
+            if (ctas <= SPLIT_TAB) break;
+        }
         for (int g = 0; g < P.total_groups; ++g) {
-            sp[g] = std::max(1, std::min(nblk[g], (nblk[g] + target - 1) / target));
             per_cta[g] = (nblk[g] + sp[g] - 1) / sp[g];
             order[g] = g;
         }

@@ -84,3 +84,35 @@ def test_forward_from_host_pageable_and_partial_copies():
     torch.cuda.synchronize()
     assert dsa.dsa_check_device_error() == (0, 0)
     assert torch.equal(host["out"], out_r.cpu())
+
+
+def test_two_streams_chained_by_compute_events():
+    """Two calls per slot on two streams, each forward waiting for the previous
+    step's (compute_after / compute_done): every host output still equals the
+    device forward's, bit for bit."""
+    wl = di.generate("host-io-chain", di.Shape(k=64), 73, [70, 30], [500, 30], [430, 0])
+    sh = wl.shape
+    ref = H.to_device(wl)
+    out_r, lse_r, idx_r = H.gpu_forward(wl, ref)
+    torch.cuda.synchronize()
+    host_in = {"q_idx": wl.tensors["qI"].pin_memory(), "w": wl.tensors["w"].pin_memory(),
+               "q_nope": wl.tensors["q_nope"].pin_memory(), "q_pe": wl.tensors["q_pe"].pin_memory()}
+    slots = []
+    for _ in range(2):
+        dev = {k: ref[k].clone() for k in ("qI", "kI", "w", "q_nope", "q_pe", "kv_cache")}
+        slots.append({"dev": dev, "stream": torch.cuda.Stream(),
+                      "outs": [torch.empty(out_r.shape, dtype=out_r.dtype).pin_memory() for _ in range(2)]})
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    for i in range(4):
+        sl = slots[i % 2]
+        d = sl["dev"]
+        dsa.dsa_forward_host(dict(host_in, out=sl["outs"][i // 2]), d["qI"], d["kI"], d["w"], d["q_nope"],
+                             d["q_pe"], d["kv_cache"][:, :sh.d_c], d["kv_cache"][:, sh.d_c:], ref["W_UK"],
+                             ref["W_UV"], H.seqs_of(wl), sh.k, sh.softmax_scale, out=torch.empty_like(out_r),
+                             lse=torch.empty_like(lse_r), idx_out=torch.empty_like(idx_r), stream=sl["stream"],
+                             compute_done=done[i % 2], compute_after=done[(i + 1) % 2] if i else None)
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_error() == (0, 0)
+    for sl in slots:
+        for o in sl["outs"]:
+            assert torch.equal(o, out_r.cpu())
