@@ -309,6 +309,8 @@ def dsa_forward(q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, seqs:
         raise DSAError("dsa_forward_workspace_size", _abi.DSA_ERR_INVALID_ARG)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        if stream is not None:  # freed on return while the call's kernels may still run on `stream`
+            workspace.record_stream(stream)
     st = _abi.load().dsa_forward(ctypes.byref(p), seqs.ref(), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("dsa_forward", st)
     if wo is not None:
@@ -348,6 +350,8 @@ def dsa_forward_host(host: dict, q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, 
     need = dsa_forward_workspace_size(p, seqs)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q_nope.device)
+        if stream is not None:  # freed on return while the call's kernels may still run on `stream`
+            workspace.record_stream(stream)
     st = lib.dsa_forward_host(ctypes.byref(p), seqs.ref(), ctypes.byref(io), _ptr(workspace), workspace.numel(),
                               _stream(stream))
     _check("dsa_forward_host", st)

@@ -100,7 +100,9 @@ def test_two_streams_chained_by_compute_events():
     slots = []
     for _ in range(2):
         dev = {k: ref[k].clone() for k in ("qI", "kI", "w", "q_nope", "q_pe", "kv_cache")}
-        slots.append({"dev": dev, "stream": torch.cuda.Stream(),
+        # device outputs kept for the whole test: the calls run on side streams
+        slots.append({"dev": dev, "stream": torch.cuda.Stream(), "o": torch.empty_like(out_r),
+                      "l": torch.empty_like(lse_r), "i": torch.empty_like(idx_r),
                       "outs": [torch.empty(out_r.shape, dtype=out_r.dtype).pin_memory() for _ in range(2)]})
     done = [torch.cuda.Event(), torch.cuda.Event()]
     for i in range(4):
@@ -108,8 +110,8 @@ def test_two_streams_chained_by_compute_events():
         d = sl["dev"]
         dsa.dsa_forward_host(dict(host_in, out=sl["outs"][i // 2]), d["qI"], d["kI"], d["w"], d["q_nope"],
                              d["q_pe"], d["kv_cache"][:, :sh.d_c], d["kv_cache"][:, sh.d_c:], ref["W_UK"],
-                             ref["W_UV"], H.seqs_of(wl), sh.k, sh.softmax_scale, out=torch.empty_like(out_r),
-                             lse=torch.empty_like(lse_r), idx_out=torch.empty_like(idx_r), stream=sl["stream"],
+                             ref["W_UV"], H.seqs_of(wl), sh.k, sh.softmax_scale, out=sl["o"], lse=sl["l"],
+                             idx_out=sl["i"], stream=sl["stream"],
                              compute_done=done[i % 2], compute_after=done[(i + 1) % 2] if i else None)
     torch.cuda.synchronize()
     assert dsa.dsa_check_device_error() == (0, 0)
