@@ -358,8 +358,12 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
 
 /* The forward from HOST buffers: the end-to-end call of one step.  On `stream`
  * it copies the step's inputs from host memory into the device buffers that
- * `p` names, runs dsa_forward, and copies the results back -- one
- * cudaMemcpyAsync per contiguous piece, in the order listed here.  With
+ * `p` names, runs dsa_forward, and copies the results back, in the order
+ * listed here: one cudaMemcpyAsync per input and output; the appended cache
+ * rows of each array go in one copy to the start of `workspace` and a small
+ * kernel puts them in their rows (the workspace is free until the forward
+ * starts) -- or, when that staging does not fit the workspace or a row is not
+ * a multiple of 16 bytes, one copy per sequence and array.  With
  * page-locked (pinned) host buffers every copy is asynchronous and the call
  * returns once all the work is enqueued; the caller synchronises `stream`
  * before reading the host outputs.  Pageable host memory also works, but then
@@ -481,6 +485,7 @@ int dsa_set_stage_events(void *const *events, int n_events);
 #define DSA_KERNEL_GEMM_TC      (1u << 12)
 #define DSA_KERNEL_PROLOGUE     (1u << 13)
 #define DSA_KERNEL_INDEXER_TOPK (1u << 14)  /* the indexer launch also selected the top-k (fused) */
+#define DSA_KERNEL_APPEND       (1u << 15)  /* dsa_forward_host put staged cache rows in place */
 
 #ifdef __cplusplus
 }

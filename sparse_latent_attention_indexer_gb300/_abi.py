@@ -16,7 +16,7 @@ KERNEL_BITS = {
     "quant": 1 << 0, "indexer_simt": 1 << 1, "indexer_tc": 1 << 2, "indexer_fp8": 1 << 3, "topk": 1 << 4,
     "absorb_simt": 1 << 5, "absorb_tc": 1 << 6, "mla_simt": 1 << 7, "mla_tc": 1 << 8, "combine": 1 << 9,
     "selftest": 1 << 10, "dense_idx": 1 << 11, "gemm_tc": 1 << 12, "prologue": 1 << 13,
-    "indexer_topk": 1 << 14,
+    "indexer_topk": 1 << 14, "append": 1 << 15,
 }
 
 

@@ -473,6 +473,42 @@ FwdWs fwd_ws_layout(const dsa_problem *p, const Batch &bt) {
     return w;
 }
 
+// The cache rows a host-buffer call appends, staged in one piece in the workspace, go to their rows:
+// appended row r (counted over the batch) of sequence b lands at dst0[b] + r - app_off[b].
+struct AppendParams {
+    int B;
+    int app_off[DSA_MAX_SEQS + 1];
+    int64_t dst0[DSA_MAX_SEQS];
+};
+static_assert(sizeof(AppendParams) + 256 <= 32764, "launch parameters");
+
+// One warp per row, 16-byte chunks (row_bytes a multiple of 16, both sides 16-byte aligned).
+__global__ void __launch_bounds__(256) append_rows_kernel(const __grid_constant__ AppendParams P,
+                                                          const uint4 *__restrict__ src, char *__restrict__ dst,
+                                                          int64_t row_bytes, int64_t rows) {
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    int lo = 0, hi = P.B - 1;  // the sequence that owns row r: the last b with app_off[b] <= r
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P.app_off[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    const int64_t chunks = row_bytes / 16;
+    const uint4 *in = src + r * chunks;
+    uint4 *out = (uint4 *)(dst + (P.dst0[lo] + (r - P.app_off[lo])) * row_bytes);
+    for (int64_t c = threadIdx.x & 31; c < chunks; c += 32) out[c] = in[c];
+}
+
+cudaError_t launch_append_rows(const AppendParams &P, const void *src, void *dst, int64_t row_bytes, int64_t rows,
+                               cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    append_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(P, (const uint4 *)src, (char *)dst, row_bytes, rows);
+    note_launch(DSA_KERNEL_APPEND);
+    return cudaGetLastError();
+}
+
+int forward_impl(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, size_t ws_bytes, void *stream);
+
 }  // namespace
 }  // namespace dsa
 
@@ -486,6 +522,15 @@ size_t dsa_forward_workspace_size(const dsa_problem *p, const dsa_seqs *seqs) {
 
 int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, size_t ws_bytes, void *stream) {
     reset_trace();
+    return dsa::forward_impl(p, seqs, workspace, ws_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace dsa {
+namespace {
+
+int forward_impl(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, size_t ws_bytes, void *stream) {
     int rc = check_problem(p);
     if (rc) return rc;
     Batch bt;
@@ -571,8 +616,14 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
                    true, true, p->wo, p->d_model, p->y, ws + L.obuf, p->kv_fp8 ? p->kv_scale : nullptr);
 }
 
+}  // namespace
+}  // namespace dsa
+
+extern "C" {
+
 int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_io *io, void *workspace,
                      size_t ws_bytes, void *stream) {
+    reset_trace();
     if (!io) return DSA_ERR_INVALID_ARG;
     int rc = check_problem(p);
     if (rc) return rc;
@@ -597,11 +648,46 @@ int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_
     put(p->w, io->w, T * p->H_I * sizeof(float));
     put(p->q_nope, io->q_nope, T * p->H * p->d_n * esz);
     put(p->q_pe, io->q_pe, T * p->H * p->d_r * esz);
-    // Appended cache rows: one contiguous piece per sequence and array.
+    // Appended cache rows.  Staged: each array in one copy into the workspace (free until the forward
+    // starts), then a kernel puts the rows in place -- a decode batch appends one row per sequence, and
+    // a copy per row would cost more than the rows.  Otherwise one copy per sequence and array.
     const size_t kv_row = (size_t)p->ld_kv * (p->kv_fp8 ? 1 : esz), pe_row = (size_t)p->ld_pe * esz,
                  ki_row = (size_t)p->D_I * esz, sc_row = (size_t)(p->d_c / 128) * sizeof(float);
+    struct Arr {
+        const void *host;
+        void *dev;
+        size_t row;
+    } arrs[4] = {{io->kv_new, (void *)p->kv_cache, kv_row},
+                 {io->k_pe_new, (void *)p->k_pe, pe_row},
+                 {io->k_idx_new, (void *)p->k_idx, ki_row},
+                 {io->kv_scale_new, (void *)p->kv_scale, sc_row}};
+    size_t app_rows = 0, stage_bytes = 0;
+    bool staged = appends && workspace && aligned(workspace, 256);
+    for (int b = 0; b < bt.st.B && appends; ++b) app_rows += (size_t)(bt.st.k_len[b] - bt.st.start_pos[b]);
+    for (const Arr &a : arrs)
+        if (a.host) {
+            staged = staged && a.row % 16 == 0 && aligned(a.dev, 16);
+            stage_bytes += (a.row * app_rows + 255) / 256 * 256;
+        }
+    staged = staged && stage_bytes <= ws_bytes;
+    if (staged && app_rows > 0) {
+        static thread_local AppendParams AP;  // ~12 KB: keep it off the host stack
+        AP.B = bt.st.B;
+        AP.app_off[0] = 0;
+        for (int b = 0; b < bt.st.B; ++b) {
+            AP.app_off[b + 1] = AP.app_off[b] + (bt.st.k_len[b] - bt.st.start_pos[b]);
+            AP.dst0[b] = (int64_t)bt.st.k_base[b] + bt.st.start_pos[b];
+        }
+        char *stage = (char *)workspace;
+        for (const Arr &a : arrs)
+            if (a.host) {
+                put(stage, a.host, a.row * app_rows);
+                if (e == cudaSuccess) e = launch_append_rows(AP, stage, a.dev, (int64_t)a.row, (int64_t)app_rows, s);
+                stage += (a.row * app_rows + 255) / 256 * 256;
+            }
+    }
     size_t done = 0;  // appended rows before sequence b
-    for (int b = 0; b < bt.st.B && appends; ++b) {
+    for (int b = 0; b < bt.st.B && appends && !staged; ++b) {
         const size_t r0 = (size_t)bt.st.k_base[b] + bt.st.start_pos[b];
         const size_t n = (size_t)(bt.st.k_len[b] - bt.st.start_pos[b]);
         if (io->kv_new) put((const char *)p->kv_cache + r0 * kv_row, (const char *)io->kv_new + done * kv_row, n * kv_row);
@@ -615,7 +701,7 @@ int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_
     }
     if (e == cudaSuccess && io->compute_after) e = cudaStreamWaitEvent(s, (cudaEvent_t)io->compute_after, 0);
     if (e != cudaSuccess) return fail_cuda(e);
-    if ((rc = dsa_forward(p, seqs, workspace, ws_bytes, stream))) return rc;
+    if ((rc = forward_impl(p, seqs, workspace, ws_bytes, stream))) return rc;
     if (io->compute_done && (e = cudaEventRecord((cudaEvent_t)io->compute_done, s)) != cudaSuccess) return fail_cuda(e);
     auto get = [&](void *host, const void *dev, size_t bytes) {
         if (e == cudaSuccess && host && bytes) e = cudaMemcpyAsync(host, dev, bytes, cudaMemcpyDeviceToHost, s);

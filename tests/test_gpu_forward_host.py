@@ -118,3 +118,37 @@ def test_two_streams_chained_by_compute_events():
     for sl in slots:
         for o in sl["outs"]:
             assert torch.equal(o, out_r.cpu())
+
+
+@pytest.mark.parametrize("many_rows", [False, True])
+def test_appended_rows_staged_or_per_sequence(many_rows):
+    """Appended rows land in their cache rows both ways: staged through the workspace and put in place
+    by a kernel (decode: one row per sequence), and copied per sequence when the staging does not fit
+    the workspace (a query at position 10 of a 20000-key cache appends 19990 rows, more bytes than its
+    forward's workspace)."""
+    if many_rows:
+        T, S, P = [1, 2], [20000, 40], [10, 38]
+    else:
+        T, S, P = [1] * 40, [300 + 37 * i for i in range(40)], [299 + 37 * i for i in range(40)]
+    wl = di.generate(f"host-io-append-{many_rows}", di.Shape(k=64), 74, T, S, P)
+    sh = wl.shape
+    ref = H.to_device(wl)
+    out_r, lse_r, idx_r = H.gpu_forward(wl, ref)
+    dev = {k: ref[k].clone() for k in ("kv_cache", "kI")}
+    for k in dev:
+        for b in range(wl.B):
+            dev[k][wl.cu_k[b] + wl.start_pos[b]:wl.cu_k[b + 1]] = 5.0
+    host = {"kv_new": _appended(wl, wl.tensors["kv_cache"]).pin_memory(),
+            "k_idx_new": _appended(wl, wl.tensors["kI"]).pin_memory(),
+            "out": torch.empty(out_r.shape, dtype=out_r.dtype).pin_memory()}
+    dsa.dsa_forward_host(host, ref["qI"], dev["kI"], ref["w"], ref["q_nope"], ref["q_pe"],
+                         dev["kv_cache"][:, :sh.d_c], dev["kv_cache"][:, sh.d_c:], ref["W_UK"], ref["W_UV"],
+                         H.seqs_of(wl), sh.k, sh.softmax_scale, out=torch.empty_like(out_r),
+                         lse=torch.empty_like(lse_r), idx_out=torch.empty_like(idx_r))
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_error() == (0, 0)
+    staged = "append" in dsa.last_kernels()
+    assert staged != many_rows, dsa.last_kernels()
+    for k in dev:
+        assert torch.equal(dev[k], ref[k]), k
+    assert torch.equal(host["out"], out_r.cpu())
