@@ -170,3 +170,17 @@ def test_forward_host_validates_before_any_copy():
     io = _abi.dsa_host_io()
     p_bad = _problem(dtype=_abi.DSA_E4M3)
     assert lib.dsa_forward_host(ctypes.byref(p_bad), s.ref(), ctypes.byref(io), None, 0, None) != _abi.DSA_OK
+
+
+def test_batch_of_max_sequences_accepted_one_more_rejected():
+    """A launch carries up to DSA_MAX_SEQS sequences in its parameters: a decode batch of exactly that
+    many is sized, one more is refused (workspace size 0, INVALID_ARG from the call)."""
+    lib = _abi.load()
+    p = _problem(idx_out=8192)
+    for B, ok in ((_abi.DSA_MAX_SEQS, True), (_abi.DSA_MAX_SEQS + 1, False)):
+        s = _seqs([1] * B, [4096] * B, [4095] * B)
+        ws = lib.dsa_forward_workspace_size(ctypes.byref(p), s.ref())
+        assert (ws > 0) == ok, (B, ws)
+        if not ok:
+            assert lib.dsa_forward(ctypes.byref(p), s.ref(), ctypes.c_void_p(1 << 20), 1 << 30, None) == \
+                _abi.DSA_ERR_INVALID_ARG

@@ -430,12 +430,14 @@ def test_attention_stage_tensor_core_matches_generic(name, monkeypatch):
     assert (lf - lg).abs().max().item() <= H.LSE_ATOL_BF16
 
 
-def test_forward_decode_batch_beyond_512_sequences():
-    """A decode step of 700 sequences (one query each, caches of 300..3000 keys, top-256): more
-    sequences than one launch carried before; sampled rows match the oracle's whole path."""
+@pytest.mark.parametrize("B", [700, dsa._abi.DSA_MAX_SEQS])
+def test_forward_decode_batch_beyond_512_sequences(B):
+    """A decode step of 700 and of the maximum 1024 sequences (one query each, caches of 300..3000
+    keys, top-256): more sequences than one launch carried before; sampled rows match the oracle's
+    whole path."""
     g = torch.Generator().manual_seed(77)
-    S = [int(x) for x in torch.randint(300, 3000, (700,), generator=g)]
-    wl = di.generate("decode-700", di.Shape(k=256), 77, [1] * len(S), S, [s - 1 for s in S])
+    S = [int(x) for x in torch.randint(300, 3000, (B,), generator=g)]
+    wl = di.generate(f"decode-{B}", di.Shape(k=256), 77, [1] * len(S), S, [s - 1 for s in S])
     t = H.to_device(wl)
     out, lse, idx = H.gpu_forward(wl, t)
     st, site = dsa.dsa_check_device_error()
