@@ -301,45 +301,50 @@ __device__ __forceinline__ void filter_row(int tid, const float *__restrict__ ro
     }
 }
 
-// The r-th largest (1-based) of n keys key_at(0 .. n-1): three histogram passes of 11 + 11 + 10 bits.
+// The r-th largest (1-based) of n keys key_at(0 .. n-1), for small n (a sample): four histogram passes
+// of 8 bits, each over 256 bins, so clearing and scanning the histogram stays short.
 template <int NT, int BAR, class KeyAt>
 __device__ __forceinline__ uint32_t kth_largest_key(int tid, KeyAt key_at, int n, int r, uint32_t *hist,
                                                     int *warp_sum, int *shared3) {
+    static_assert(256 % NT == 0, "the bin scan gives each thread the same number of the 256 bins");
     uint32_t prefix = 0, pmask = 0;
     int remaining = r;
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const int nb = pass == 2 ? 1024 : 2048;
-        for (int b = tid; b < nb; b += NT) hist[b] = 0;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int b = tid; b < 256; b += NT) hist[b] = 0;
         group_sync<NT, BAR>();
         for (int s = tid; s < n; s += NT) {
             const uint32_t u = key_at(s);
-            if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
+            if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
         }
         group_sync<NT, BAR>();
-        find_bin_from_top<NT, BAR>(tid, hist, nb, remaining, shared3, warp_sum);
+        find_bin_from_top<NT, BAR>(tid, hist, 256, remaining, shared3, warp_sum);
         remaining -= shared3[1];
         prefix |= (uint32_t)shared3[0] << shift;
-        pmask |= (uint32_t)(nb - 1) << shift;
+        pmask |= 255u << shift;
         group_sync<NT, BAR>();
     }
     return prefix;
 }
 
 // Compacts, in index order, the keys of row[0 .. n_live) whose ordered key is >= thr into the
-// candidate list (at most sm.cap of them are stored); returns how many there are.
+// candidate list (at most sm.cap of them are stored); returns how many there are.  Each step's loads
+// are issued before the previous step is compacted, so their latency hides behind its scan and
+// barriers.
 template <int NT, int BAR, bool NC, int L>
 __device__ __forceinline__ int compact_at_least(int tid, const float *__restrict__ row, int n_live, bool vec,
                                                 uint32_t thr, const FilterSmem &sm) {
     constexpr int WARPS = NT / 32;
     const int lane = tid & 31, wid = tid >> 5;
     int base = 0;
+    uint32_t u[L], valid = 0;
+    if (tid * L < n_live) load_keys<NC, L>(row, tid * L, n_live, vec, u, valid);
 #pragma unroll 1
     for (int s0 = 0; s0 < n_live; s0 += NT * L) {
-        const int first = s0 + tid * L;
-        uint32_t u[L], valid = 0;
-        if (first < n_live) load_keys<NC, L>(row, first, n_live, vec, u, valid);
+        const int first = s0 + tid * L, next = first + NT * L;
+        uint32_t un[L], vn = 0;
+        if (next < n_live) load_keys<NC, L>(row, next, n_live, vec, un, vn);
         uint32_t take = 0;
 #pragma unroll
         for (int j = 0; j < L; ++j) take |= (((valid >> j) & 1u) && u[j] >= thr) ? (1u << j) : 0u;
@@ -370,6 +375,9 @@ __device__ __forceinline__ int compact_at_least(int tid, const float *__restrict
             }
         base += total;
         group_sync<NT, BAR>();  // warp_gt is rewritten by the next step
+#pragma unroll
+        for (int j = 0; j < L; ++j) u[j] = un[j];
+        valid = vn;
     }
     return base;
 }
