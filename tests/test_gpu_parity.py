@@ -449,3 +449,42 @@ def test_forward_decode_batch_beyond_512_sequences(B):
         o = ref[r]
         H.check_selection_row(idx_np[r], o["scores"], o["absterm"], o["pos"], wl.shape.k)
         assert np.abs(out_np[r] - o["out"]).max() <= H.OUT_ATOL_BF16
+
+
+def _documented_order(row, p, k):
+    """The selection's documented order: the keys above the k-th score T in increasing key index, then
+    the first keys equal to T in increasing key index."""
+    sel = H.cpu_topk_same_buffer(row, p, k)
+    causal = np.asarray(row[:p + 1], np.float32).astype(np.float64) + 0.0
+    T = causal[sel[-1]]
+    above = np.sort(sel[causal[sel] > T])
+    equal = np.sort(sel[causal[sel] == T])
+    return np.concatenate([above, equal])
+
+
+@pytest.mark.parametrize("kind", ["random", "coarse", "equal", "rising"])
+def test_topk_cluster_rows_exact_order(kind):
+    """Few long rows (the cluster kernel: eight CTAs per row, 9K to 62K keys) with random scores, a
+    coarse grid (ties at the k-th score), all-equal scores and rising scores (every top key in the last
+    CTA's slice): the output is the documented order exactly -- keys above the k-th score in increasing
+    index, then the first keys equal to it -- ties to the lower key index."""
+    g = torch.Generator().manual_seed(11)
+    rows, k = 24, 2048
+    S = [9000 + 2300 * r for r in range(rows)]
+    cu = np.concatenate([[0], np.cumsum(S)]).tolist()
+    seqs = dsa.Seqs(list(range(rows + 1)), cu, [s - 1 for s in S])
+    ld = max(S)
+    if kind == "random":
+        scores = torch.randn((rows, ld), generator=g)
+    elif kind == "coarse":
+        scores = torch.randint(-30, 30, (rows, ld), generator=g).float() / 4
+    elif kind == "equal":
+        scores = torch.full((rows, ld), 0.5)
+    else:
+        scores = torch.arange(ld, dtype=torch.float32).repeat(rows, 1) / ld
+    idx = dsa.dsa_topk_select(scores.cuda(), seqs, k).cpu().numpy()
+    assert "topk" in dsa.last_kernels()
+    sc = scores.numpy()
+    for r in range(rows):
+        want = _documented_order(sc[r], S[r] - 1, k)
+        assert np.array_equal(idx[r], want), f"row {r}"
