@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--rows", type=int, default=None,
                     help="keep only the first ROWS query rows of each workload (a small case of the same kernels, "
                          "for profiling); the sequences keep their whole caches")
+    ap.add_argument("--last-rows", type=int, default=None,
+                    help="keep only the last LAST_ROWS query rows of the longest sequence (the heaviest rows), "
+                         "for profiling")
     ap.add_argument("--fused-topk", type=int, choices=[0, 1], default=None,
                     help="1: the fused indexer + top-k kernel; 0: indexer then top-k; default: the library's")
     return ap.parse_args()
@@ -402,6 +405,26 @@ def first_rows(wl, n):
     return di.Workload(wl.name + f"-first{n}", wl.shape, wl.seed, T, S, P, ten)
 
 
+def last_rows(wl, n):
+    """The workload cut to the last n query rows of its longest sequence (the longest causal
+    prefixes: the heaviest rows), with that sequence's whole key cache."""
+    if n is None:
+        return wl
+    import dsa_inputs as di
+    b = max(range(wl.B), key=lambda i: wl.S[i])
+    t = min(n, wl.T[b])
+    q_rows = list(range(wl.cu_q[b + 1] - t, wl.cu_q[b + 1]))
+    ten = {}
+    for k, v in wl.tensors.items():
+        if k in ("qI", "w", "q_nope", "q_pe"):
+            ten[k] = v[q_rows]
+        elif k in ("kI", "kv_cache"):
+            ten[k] = v[wl.cu_k[b]:wl.cu_k[b + 1]]
+        else:
+            ten[k] = v
+    return di.Workload(wl.name + f"-last{t}", wl.shape, wl.seed, [t], [wl.S[b]], [wl.start_pos[b] + wl.T[b] - t], ten)
+
+
 def measure_workload(cfg, args, world, rank, local, with_cpu):
     """Times whole dsa_forward steps of workload `cfg`, then its indexer and
     top-k kernels on their own, then the end-to-end step from host buffers."""
@@ -411,7 +434,7 @@ def measure_workload(cfg, args, world, rank, local, with_cpu):
     import sparse_latent_attention_indexer_gb300 as dsa
 
     dev = torch.device("cuda", local)
-    wl = first_rows(di.workload(cfg), args.rows)
+    wl = last_rows(first_rows(di.workload(cfg), args.rows), args.last_rows)
     sh = wl.shape
     name = CONFIG_NAMES[cfg] + (f" (first {args.rows} rows)" if args.rows else "")
     seqs = dsa.Seqs(wl.cu_q, wl.cu_k, wl.start_pos)
