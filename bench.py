@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--rows", type=int, default=None,
                     help="keep only the first ROWS query rows of each workload (a small case of the same kernels, "
                          "for profiling); the sequences keep their whole caches")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="tensor seed of the synthetic workloads (default: each workload's own)")
     ap.add_argument("--last-rows", type=int, default=None,
                     help="keep only the last LAST_ROWS query rows of the longest sequence (the heaviest rows), "
                          "for profiling")
@@ -266,7 +268,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     import dsa_inputs as di
-    wl = di.workload(args.config)
+    wl = di.workload(args.config, args.seed)
     n_rows = args.ref_rows if args.ref_rows is not None else REF_ROWS[args.config]
     for _ in range(args.warmup):
         oracle_sample(wl, max(1, n_rows // 8))
@@ -434,7 +436,7 @@ def measure_workload(cfg, args, world, rank, local, with_cpu):
     import sparse_latent_attention_indexer_gb300 as dsa
 
     dev = torch.device("cuda", local)
-    wl = last_rows(first_rows(di.workload(cfg), args.rows), args.last_rows)
+    wl = last_rows(first_rows(di.workload(cfg, args.seed), args.rows), args.last_rows)
     sh = wl.shape
     name = CONFIG_NAMES[cfg] + (f" (first {args.rows} rows)" if args.rows else "")
     seqs = dsa.Seqs(wl.cu_q, wl.cu_k, wl.start_pos)
@@ -507,7 +509,8 @@ def measure_workload(cfg, args, world, rank, local, with_cpu):
            "config": {"workload": name, "queries_per_step": M, "keys": wl.total_k, "top_k": sh.k,
                       "indexer": "fp8 e4m3 + ue8m0 block scales" if sh.idx_fp8 else sh.dtype,
                       "l2": "flushed (256 MiB write) before every timed step",
-                      "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+                      "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                      **({"seed": args.seed} if args.seed is not None else {})},
            "roofline": roofline, "stages": stages, "kernels": kernels, "gpu_launches": launches, "clocks": clk,
            "e2e": e2e, "cpu_baseline": cpu}
     del t, out, lse, idx, ws, flush

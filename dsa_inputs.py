@@ -157,20 +157,23 @@ def chunk_prefixes(seed: int = 2, B: int = 8, lo: int = 8192, hi: int = 57344) -
     return [int(x) for x in torch.randint(lo, hi + 1, (B,), generator=g)]
 
 
-def workload(cfg: int) -> Workload:
-    """Generate workload ``cfg`` (0..4) at its full size."""
+def workload(cfg: int, seed: int | None = None) -> Workload:
+    """Generate workload ``cfg`` (0..4) at its full size.  ``seed`` replaces the workload's own tensor
+    seed (the sequence lengths stay those of the configuration)."""
+    def sd(default):
+        return default if seed is None else seed
     if cfg == 0:
-        return generate("tiny", TINY, 0, [256], [256], [0])
+        return generate("tiny", TINY, sd(0), [256], [256], [0])
     if cfg == 1:
-        return generate("prefill-4k", FULL, 0, [4096], [4096], [0])
+        return generate("prefill-4k", FULL, sd(0), [4096], [4096], [0])
     if cfg == 2:
-        return generate("prefill-32k", FULL, 0, [32768], [32768], [0])
+        return generate("prefill-32k", FULL, sd(0), [32768], [32768], [0])
     if cfg == 3:
         S = decode_lengths()
-        return generate("decode-64", FULL, 1, [1] * len(S), S, [s - 1 for s in S])
+        return generate("decode-64", FULL, sd(1), [1] * len(S), S, [s - 1 for s in S])
     if cfg == 4:
         P = chunk_prefixes()
-        return generate("chunked-8x8192-fp8", FULL_FP8, 2, [8192] * len(P), [p + 8192 for p in P], P)
+        return generate("chunked-8x8192-fp8", FULL_FP8, sd(2), [8192] * len(P), [p + 8192 for p in P], P)
     raise ValueError(cfg)
 
 
