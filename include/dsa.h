@@ -390,6 +390,8 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
  * enqueued, before the output copies.  Calls on two streams with their own
  * device buffers can so chain their forwards (each waits for the other's
  * compute_done) while one call's copies overlap the other's kernels.
+ * Every check dsa_forward makes runs before the first copy is enqueued, so a
+ * refused call changes no device buffer.
  * Returns what dsa_forward returns, DSA_ERR_INVALID_ARG when a sequence has
  * start_pos[b] > S_b with kv_new, k_pe_new, k_idx_new or kv_scale_new given, or
  * when a requested output has no device buffer in `p`, and DSA_ERR_CUDA when

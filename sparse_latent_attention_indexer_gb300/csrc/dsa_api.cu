@@ -508,6 +508,7 @@ cudaError_t launch_append_rows(const AppendParams &P, const void *src, void *dst
 }
 
 int forward_impl(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, size_t ws_bytes, void *stream);
+int check_forward(const dsa_problem *p, const Batch &bt, const void *workspace, size_t ws_bytes);
 
 }  // namespace
 }  // namespace dsa
@@ -530,19 +531,26 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
 namespace dsa {
 namespace {
 
+// The checks of a forward call on a non-empty batch that need no GPU (the problem itself is checked by
+// check_problem first).
+int check_forward(const dsa_problem *p, const Batch &bt, const void *workspace, size_t ws_bytes) {
+    if (!p->q_idx || !p->k_idx || !p->w || !p->q_nope || !p->kv_cache || !p->W_UK || !p->W_UV ||
+        (!p->out && !p->wo) || (p->d_r > 0 && (!p->q_pe || !p->k_pe)))
+        return DSA_ERR_INVALID_ARG;
+    if (p->wo && (!p->y || !aligned(p->wo, 16) || !aligned(p->y, 16))) return DSA_ERR_INVALID_ARG;
+    if (p->kv_fp8 && (!p->kv_scale || !aligned(p->kv_cache, 16))) return DSA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, WS_ALIGN) || ws_bytes < fwd_ws_layout(p, bt).total) return DSA_ERR_WORKSPACE;
+    return DSA_OK;
+}
+
 int forward_impl(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, size_t ws_bytes, void *stream) {
     int rc = check_problem(p);
     if (rc) return rc;
     Batch bt;
     if ((rc = build_batch(seqs, bt))) return rc;
     if (bt.total_q == 0) return DSA_OK;
-    if (!p->q_idx || !p->k_idx || !p->w || !p->q_nope || !p->kv_cache || !p->W_UK || !p->W_UV ||
-        (!p->out && !p->wo) || (p->d_r > 0 && (!p->q_pe || !p->k_pe)))
-        return DSA_ERR_INVALID_ARG;
-    if (p->wo && (!p->y || !aligned(p->wo, 16) || !aligned(p->y, 16))) return DSA_ERR_INVALID_ARG;
-    if (p->kv_fp8 && (!p->kv_scale || !aligned(p->kv_cache, 16))) return DSA_ERR_INVALID_ARG;
+    if ((rc = check_forward(p, bt, workspace, ws_bytes))) return rc;
     const FwdWs L = fwd_ws_layout(p, bt);
-    if (!workspace || !aligned(workspace, WS_ALIGN) || ws_bytes < L.total) return DSA_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     char *ws = (char *)workspace;
     cudaError_t e;
@@ -640,6 +648,8 @@ int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_
         (io->kv_scale_new && (!p->kv_fp8 || !p->kv_scale)) || (io->lse && !p->lse) || (io->idx && !p->idx_out) ||
         (io->out && !(p->wo ? p->y : p->out)))
         return DSA_ERR_INVALID_ARG;
+    // everything the forward would refuse is refused before any copy is enqueued
+    if (bt.total_q > 0 && (rc = check_forward(p, bt, workspace, ws_bytes))) return rc;
     cudaError_t e = cudaSuccess;
     auto put = [&](const void *dev, const void *host, size_t bytes) {
         if (e == cudaSuccess && host && bytes) e = cudaMemcpyAsync((void *)dev, host, bytes, cudaMemcpyHostToDevice, s);

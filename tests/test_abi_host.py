@@ -184,3 +184,13 @@ def test_batch_of_max_sequences_accepted_one_more_rejected():
         if not ok:
             assert lib.dsa_forward(ctypes.byref(p), s.ref(), ctypes.c_void_p(1 << 20), 1 << 30, None) == \
                 _abi.DSA_ERR_INVALID_ARG
+
+
+def test_forward_host_refuses_a_short_workspace_before_copying():
+    """The forward's own checks (here: no workspace) run before the first copy, so the refusal needs no
+    GPU and leaves the device buffers as they were."""
+    lib = _abi.load()
+    s = _seqs([4], [8], [4])
+    p = _problem()
+    io = _abi.dsa_host_io(q_nope=1 << 16)
+    assert lib.dsa_forward_host(ctypes.byref(p), s.ref(), ctypes.byref(io), None, 0, None) == _abi.DSA_ERR_WORKSPACE
