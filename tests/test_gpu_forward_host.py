@@ -152,3 +152,39 @@ def test_appended_rows_staged_or_per_sequence(many_rows):
     for k in dev:
         assert torch.equal(dev[k], ref[k]), k
     assert torch.equal(host["out"], out_r.cpu())
+
+
+def test_forward_from_host_with_fp8_latent_cache():
+    """The e4m3 latent cache through the host-buffer call: the appended rows of all four arrays (latent
+    codes, k_pe, k^I, block scales; four row sizes) land in place, and the outputs equal the device
+    forward's bit for bit."""
+    wl = di.generate("host-io-fp8kv", di.Shape(k=64), 75, [120, 1, 30], [900, 1500, 30], [780, 1499, 0])
+    sh = wl.shape
+    ref = H.to_device(wl)
+    lat = ref["kv_cache"][:, :sh.d_c].contiguous()
+    codes, scales = dsa.dsa_quant_e4m3_ue8m0(lat)
+    codes = codes.view(-1, sh.d_c)
+    scales = scales.view(-1, sh.d_c // 128).contiguous()
+    kpe = ref["kv_cache"][:, sh.d_c:].contiguous()  # k_pe in a buffer of its own
+    out_r, lse_r, idx_r = dsa.dsa_forward(ref["qI"], ref["kI"], ref["w"], ref["q_nope"], ref["q_pe"], codes, kpe,
+                                          ref["W_UK"], ref["W_UV"], H.seqs_of(wl), sh.k, sh.softmax_scale,
+                                          kv_scale=scales)
+    torch.cuda.synchronize()
+    dev = {"codes": codes.clone(), "kpe": kpe.clone(), "kI": ref["kI"].clone(), "scales": scales.clone()}
+    for k, v in dev.items():
+        for b in range(wl.B):
+            v[wl.cu_k[b] + wl.start_pos[b]:wl.cu_k[b + 1]] = 3 if v.dtype == torch.uint8 else 3.0
+    host = {"kv_new": _appended(wl, codes.cpu()).pin_memory(), "k_pe_new": _appended(wl, kpe.cpu()).pin_memory(),
+            "k_idx_new": _appended(wl, ref["kI"].cpu()).pin_memory(),
+            "kv_scale_new": _appended(wl, scales.cpu()).pin_memory(),
+            "out": torch.empty(out_r.shape, dtype=out_r.dtype).pin_memory()}
+    dsa.dsa_forward_host(host, ref["qI"], dev["kI"], ref["w"], ref["q_nope"], ref["q_pe"], dev["codes"], dev["kpe"],
+                         ref["W_UK"], ref["W_UV"], H.seqs_of(wl), sh.k, sh.softmax_scale,
+                         out=torch.empty_like(out_r), lse=torch.empty_like(lse_r), idx_out=torch.empty_like(idx_r),
+                         kv_scale=dev["scales"])
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_error() == (0, 0)
+    assert "append" in dsa.last_kernels()
+    assert torch.equal(dev["codes"], codes) and torch.equal(dev["kpe"], kpe) and torch.equal(dev["kI"], ref["kI"])
+    assert torch.equal(dev["scales"], scales)
+    assert torch.equal(host["out"], out_r.cpu())
