@@ -47,11 +47,14 @@ constexpr int BN = TOK * HI;    // 256 (MMA N)
 // kernel, bf16: 16 of them, one per (TMEM lane quarter, token) pair, four per SM sub-partition; FP8:
 // 8, each taking two tokens of its lane quarter (measured faster for the shorter FP8 MMA).  The
 // fused kernel (F) has 8 epilogue warps in both precisions, then the selecting warps: 4 for FP8
-// (whose epilogue needs the 128 registers a 512-thread CTA leaves), 8 for bf16 (measured: 7.86
-// against 8.61 ms of indexer + top-k on the 32K prefill).
+// (whose epilogue needs the 128 registers a 512-thread CTA leaves), joined there by warps 2 and 3
+// once the tensor memory is allocated, and 8 for bf16 (measured: 7.86 against 8.61 ms of indexer +
+// top-k on the 32K prefill).
 constexpr int EPI_WARP0 = 4;
 template <bool FP8, bool F = false> constexpr int num_epi() { return (FP8 || F) ? 8 : 16; }
 template <bool FP8> constexpr int sel_warps() { return FP8 ? 4 : 8; }
+template <bool FP8> constexpr int sel_spare() { return FP8 ? 2 : 0; }  // warps 2, 3 select too
+template <bool FP8> constexpr int sel_threads() { return (sel_warps<FP8>() + sel_spare<FP8>()) * 32; }
 template <bool FP8, bool F = false> constexpr int sel_warp0() { return EPI_WARP0 + num_epi<FP8, F>(); }
 template <bool FP8, bool F = false> constexpr int num_threads() {
     return (EPI_WARP0 + num_epi<FP8, F>() + (F ? sel_warps<FP8>() : 0)) * 32;
@@ -181,7 +184,7 @@ __device__ __forceinline__ void init_barriers(const Smem<FP8, F> &sm) {
         tc::mbar_init(sm.bfree(), 1);
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(sm.slot_full(i), num_epi<FP8, F>() * 32);
-            tc::mbar_init(sm.slot_free(i), sel_warps<FP8>() * 32);
+            tc::mbar_init(sm.slot_free(i), sel_threads<FP8>());
         }
     }
     *sm.abort_flag() = 0;
@@ -444,8 +447,7 @@ __global__ void __launch_bounds__(num_threads<FP8, true>(), 1)
     using C = Cfg<FP8, true>;
     constexpr int EPI = num_epi<FP8, true>();
     constexpr int SEL0 = sel_warp0<FP8, true>();
-    constexpr int NS = sel_warps<FP8>() * 32;  // selecting threads
-    static_assert(tk::MAX_BINS % NS == 0, "the bin scan gives each thread the same number of bins");
+    constexpr int NS = sel_threads<FP8>();  // selecting threads
     extern __shared__ uint8_t smem_raw[];
     const Smem<FP8, true> sm(smem_raw);
     __shared__ int never;
@@ -569,9 +571,10 @@ __global__ void __launch_bounds__(num_threads<FP8, true>(), 1)
             }
             tc::mbar_arrive(sm.slot_full(sb));  // releases this thread's score writes
         }
-    } else if (warp >= SEL0) {
+    } else if (warp >= SEL0 || (sel_spare<FP8>() > 0 && (warp == 2 || warp == 3))) {
         // ---------------- selection: the top-k of each filled slot ----------------
-        const int tid = (int)threadIdx.x - SEL0 * 32;
+        // group-local thread index: warps 2, 3 (when they select) first, then the selecting warps
+        const int tid = warp >= SEL0 ? (warp - SEL0 + sel_spare<FP8>()) * 32 + lane : (warp - 2) * 32 + lane;
         uint8_t *sc = sm.sel();
         const tk::FilterSmem fs{(uint32_t *)sc, (int *)(sc + tk::MAX_BINS * 4), (int *)(sc + tk::MAX_BINS * 4 + 128),
                                 (int *)(sc + tk::MAX_BINS * 4 + 256), (uint32_t *)(sc + C::SEL_HEAD),
@@ -581,7 +584,7 @@ __global__ void __launch_bounds__(num_threads<FP8, true>(), 1)
             if (g < 0) break;
             const Group G = group_of(P, g);
             const int sb = j & 1;
-            // one decision for the four selecting warps (their selection synchronises on barrier 2)
+            // one decision for the selecting warps (their selection synchronises on barrier 2)
             if (!bar_and<2, NS>(tc::mbar_wait(sm.slot_full(sb), (j >> 1) & 1, abort_flag, err, 51, P.wait_limit)))
                 break;
             const float *slot = slot0 + (int64_t)sb * TOK * P.ld;

@@ -85,16 +85,16 @@ __device__ __forceinline__ void load_keys(const float *__restrict__ row, int s0,
 
 // The bin b of hist[0..nb) (nb a multiple of NT) holding the need-th largest key, counted from the
 // top: keys in bins above b number `above` < need <= above + hist[b].  Every thread of the group
-// calls it and receives {b, above, above + hist[b]} in res[0..2].  Thread t owns nb / NT
-// consecutive bins from the top, so the search is one group-wide scan.
+// calls it and receives {b, above, above + hist[b]} in res[0..2].  Thread t owns ceil(nb / NT)
+// consecutive bins from the top (the last threads fewer or none), so the search is one group-wide scan.
 template <int NT, int BAR>
 __device__ __forceinline__ void find_bin_from_top(int tid, const uint32_t *hist, int nb, int need, int *res,
                                                   int *warp_sum) {
     constexpr int WARPS = NT / 32;
     const int lane = tid & 31, wid = tid >> 5;
-    const int per = nb / NT, hi = nb - tid * per;
+    const int per = (nb + NT - 1) / NT, hi = nb - tid * per, lo = max(hi - per, 0);
     int mine = 0;
-    for (int b = hi - 1; b >= hi - per; --b) mine += (int)hist[b];
+    for (int b = hi - 1; b >= lo; --b) mine += (int)hist[b];
     int incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -109,7 +109,7 @@ __device__ __forceinline__ void find_bin_from_top(int tid, const uint32_t *hist,
     const int excl = before + incl - mine;
     if (excl < need && need <= excl + mine) {
         int cum = excl;
-        for (int b = hi - 1; b >= hi - per; --b) {
+        for (int b = hi - 1; b >= lo; --b) {
             const int h = (int)hist[b];
             if (cum + h >= need) {
                 res[0] = b;
@@ -306,7 +306,6 @@ __device__ __forceinline__ void filter_row(int tid, const float *__restrict__ ro
 template <int NT, int BAR, class KeyAt>
 __device__ __forceinline__ uint32_t kth_largest_key(int tid, KeyAt key_at, int n, int r, uint32_t *hist,
                                                     int *warp_sum, int *shared3) {
-    static_assert(256 % NT == 0, "the bin scan gives each thread the same number of the 256 bins");
     uint32_t prefix = 0, pmask = 0;
     int remaining = r;
 #pragma unroll 1
