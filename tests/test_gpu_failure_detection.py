@@ -64,3 +64,41 @@ def test_production_kernels_give_up_and_recover():
         assert float(np.abs(out_np[r] - o["out"]).max()) <= H.OUT_ATOL_BF16
     with pytest.raises(dsa.DSAError):
         dsa.dsa_set_wait_limit(-1)
+
+
+def test_fused_indexer_topk_and_gemm_give_up_and_recover():
+    """The same failure path through the kernels of the chunked-prefill configuration: the fused FP8
+    indexer + top-k (its producer, MMA, epilogue and six selecting warps), the attention and the
+    output-projection GEMM, with a 64-cycle wait limit: a production site is reported and every kernel
+    returns; with the limit restored the selection equals the unfused path's exactly."""
+    import math
+
+    import dsa_inputs as di
+    from tests import helpers as H
+    from tests.test_gpu_fused_topk import _unfused_idx
+
+    shape = di.Shape(k=256, idx_fp8=True)
+    wl = di.generate("abort-fused", shape, 6, [700, 513, 900], [3000, 513, 5000], [2300, 0, 4100])
+    t = H.to_device(wl)
+    g = torch.Generator().manual_seed(7)
+    wo = (torch.randn(512, shape.H * shape.d_v, generator=g) / math.sqrt(shape.H * shape.d_v)).to(torch.bfloat16)
+    wo = wo.cuda()
+    assert dsa.dsa_check_device_error() == (_abi.DSA_OK, 0)
+    dsa.dsa_set_fused_topk(True)
+    try:
+        try:
+            dsa.dsa_set_wait_limit(64)
+            H.gpu_forward(wl, t, wo=wo)
+            launched = dsa.last_kernels()
+            st, site = dsa.dsa_check_device_error()
+        finally:
+            dsa.dsa_set_wait_limit(0)
+        assert {"indexer_topk", "mla_tc", "gemm_tc"} <= launched, launched
+        assert st == _abi.DSA_ERR_TIMEOUT, st
+        assert 1 <= site <= 60, site
+        assert dsa.dsa_check_device_error() == (_abi.DSA_OK, 0)
+        out, lse, idx, y = H.gpu_forward(wl, t, wo=wo)
+        assert dsa.dsa_check_device_error() == (_abi.DSA_OK, 0)
+    finally:
+        dsa.dsa_set_fused_topk(-1)
+    assert torch.equal(idx, _unfused_idx(wl, t))
