@@ -223,28 +223,57 @@ __device__ __forceinline__ void epilogue_block(const Smem<FP8, F> &sm, uint32_t 
 #pragma unroll 1
     for (int tt = t_first; tt < G.ntok; tt += t_step) {
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * BN + tt * HI;
-        float v0[32], v1[32];
-        tc::tmem_ld32(taddr, v0);
-        tc::tmem_ld32(taddr + 32, v1);
-        tc::tmem_ld_wait();
-        if (EPI == 16) {  // one token per warp, so the accumulator can go back at once
+        const float4 *wv = (const float4 *)(sm.wsm() + tt * HI);
+        float s0 = 0.0f, s1 = 0.0f;
+        if constexpr (EPI == 16) {
+            // One token per warp, under the 96 registers a 640-thread CTA leaves: heads 0-31, then
+            // 32-63, 32 accumulator values live at a time; the accumulator goes back to the MMA once
+            // the second half is loaded.
+            {
+                float v0[32];
+                tc::tmem_ld32(taddr, v0);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int h4 = 0; h4 < 8; ++h4) {
+                    const float4 a4 = wv[h4];
+                    s0 = fmaf(a4.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
+                    s0 = fmaf(a4.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
+                    s0 = fmaf(a4.z, fmaxf(v0[4 * h4 + 2], 0.0f), s0);
+                    s0 = fmaf(a4.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
+                }
+            }
+            float v1[32];
+            tc::tmem_ld32(taddr + 32, v1);
+            tc::tmem_ld_wait();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(sm.tempty(acc));
-        }
-        const float4 *wv = (const float4 *)(sm.wsm() + tt * HI);
-        float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 a4 = wv[h4], c4 = wv[8 + h4];
-            s0 = fmaf(a4.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
-            s1 = fmaf(c4.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
-            s0 = fmaf(a4.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
-            s1 = fmaf(c4.y, fmaxf(v1[4 * h4 + 1], 0.0f), s1);
-            s0 = fmaf(a4.z, fmaxf(v0[4 * h4 + 2], 0.0f), s0);
-            s1 = fmaf(c4.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
-            s0 = fmaf(a4.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
-            s1 = fmaf(c4.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
+            for (int h4 = 0; h4 < 8; ++h4) {
+                const float4 c4 = wv[8 + h4];
+                s1 = fmaf(c4.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
+                s1 = fmaf(c4.y, fmaxf(v1[4 * h4 + 1], 0.0f), s1);
+                s1 = fmaf(c4.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
+                s1 = fmaf(c4.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
+            }
+        } else {
+            // Two tokens per warp, 128 registers: all 64 heads of a token at once.
+            float v0[32], v1[32];
+            tc::tmem_ld32(taddr, v0);
+            tc::tmem_ld32(taddr + 32, v1);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+                const float4 a4 = wv[h4], c4 = wv[8 + h4];
+                s0 = fmaf(a4.x, fmaxf(v0[4 * h4 + 0], 0.0f), s0);
+                s1 = fmaf(c4.x, fmaxf(v1[4 * h4 + 0], 0.0f), s1);
+                s0 = fmaf(a4.y, fmaxf(v0[4 * h4 + 1], 0.0f), s0);
+                s1 = fmaf(c4.y, fmaxf(v1[4 * h4 + 1], 0.0f), s1);
+                s0 = fmaf(a4.z, fmaxf(v0[4 * h4 + 2], 0.0f), s0);
+                s1 = fmaf(c4.z, fmaxf(v1[4 * h4 + 2], 0.0f), s1);
+                s0 = fmaf(a4.w, fmaxf(v0[4 * h4 + 3], 0.0f), s0);
+                s1 = fmaf(c4.w, fmaxf(v1[4 * h4 + 3], 0.0f), s1);
+            }
         }
         if (key < G.S) out_base[(int64_t)tt * ld + key] = (key <= G.p0 + tt) ? (s0 + s1) * ks : -INFINITY;
     }
