@@ -766,13 +766,16 @@ def measure_e2e(args, dsa, torch, wl, host, t, seqs, out, lse, idx, ws, unit):
                       "host": dict(inputs, out=torch.empty(out.shape, dtype=out.dtype).pin_memory())})
 
     done = [torch.cuda.Event(), torch.cuda.Event()]  # the forward of the slot's last step is enqueued
+    copied = [torch.cuda.Event(), torch.cuda.Event()]  # the input copies of the slot's last step are enqueued
 
     def step(i, n_slots):
         sl = slots[i % n_slots]
         d = sl["dev"]
         # with two slots the forwards run one after the other (each waits for the previous step's),
-        # while the copies of one step overlap the kernels of the other
-        chain = {} if n_slots == 1 else {"compute_done": done[i % 2], "compute_after": done[(i + 1) % 2] if i else None}
+        # while the copies of one step overlap the kernels of the other; the input copies also run
+        # one after the other, so the first forward waits for one step's inputs, not two steps'
+        chain = {} if n_slots == 1 else {"compute_done": done[i % 2], "compute_after": done[(i + 1) % 2] if i else None,
+                                         "copy_done": copied[i % 2], "copy_after": copied[(i + 1) % 2] if i else None}
         dsa.dsa_forward_host(sl["host"], d["qI"], d["kI"], d["w"], d["q_nope"], d["q_pe"], d["kv_cache"][:, :d_c],
                              d["kv_cache"][:, d_c:], d["W_UK"], d["W_UV"], seqs, sh.k, sh.softmax_scale,
                              idx_fp8=sh.idx_fp8, out=sl["out"], lse=sl["lse"], idx_out=sl["idx"], workspace=sl["ws"],
@@ -801,7 +804,8 @@ def measure_e2e(args, dsa, torch, wl, host, t, seqs, out, lse, idx, ws, unit):
     return {"value": wl.total_q / (ms / 1e3), "unit": unit, "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "serial_ms_per_step": serial, "serial_value": wl.total_q / (serial / 1e3),
-            "call": "dsa_forward_host (pinned host buffers), two pipeline slots on their own streams, forwards chained",
+            "call": "dsa_forward_host (pinned host buffers), two pipeline slots on their own streams, forwards and "
+                    "input copies chained",
             "inputs": "the step's queries (q^I, w, q_nope, q_pe) and the cache rows they append "
                       "(latent + k_pe, k^I); the earlier cache rows stay resident"}
 

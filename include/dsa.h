@@ -384,12 +384,17 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
  *   kv_scale_new             e4m3 cache: the same rows' d_c / 128 scales.
  * Host outputs (NULL: not copied back): out (y when p->wo is set: the
  * projected output), lse, idx (requires p->idx_out).
- * Pipelining (both NULL: none): compute_after, a cudaEvent_t the forward
- * waits for once the input copies are enqueued (cudaStreamWaitEvent), and
- * compute_done, a cudaEvent_t recorded once the forward's kernels are
- * enqueued, before the output copies.  Calls on two streams with their own
- * device buffers can so chain their forwards (each waits for the other's
- * compute_done) while one call's copies overlap the other's kernels.
+ * Pipelining (all NULL: none), four cudaEvent_t handles: copy_after, which
+ * the input copies wait for (cudaStreamWaitEvent before the first of them);
+ * copy_done, recorded once the input copies and the append kernel are
+ * enqueued; compute_after, which the forward waits for after that; and
+ * compute_done, recorded once the forward's kernels are enqueued, before the
+ * output copies.  Calls on two streams with their own device buffers can so
+ * chain their forwards (each waits for the previous call's compute_done) while
+ * one call's copies overlap the other's kernels, and chain their input copies
+ * (each waits for the previous call's copy_done) so that two calls' inputs do
+ * not share the host-to-device bandwidth: the first forward then starts after
+ * one call's input copies instead of two.
  * Every check dsa_forward makes runs before the first copy is enqueued, so a
  * refused call changes no device buffer.
  * Returns what dsa_forward returns, DSA_ERR_INVALID_ARG when a sequence has
@@ -404,6 +409,7 @@ typedef struct dsa_host_io {
     float *lse;
     int32_t *idx;
     void *compute_after, *compute_done;
+    void *copy_after, *copy_done;
 } dsa_host_io;
 int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_io *io, void *workspace,
                      size_t ws_bytes, void *stream);

@@ -320,7 +320,8 @@ def dsa_forward(q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, seqs:
 
 def dsa_forward_host(host: dict, q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, seqs: Seqs, top_k: int,
                      softmax_scale: float, idx_fp8: bool = False, out=None, lse=None, idx_out=None, workspace=None,
-                     stream=None, wo=None, y=None, kv_scale=None, compute_after=None, compute_done=None):
+                     stream=None, wo=None, y=None, kv_scale=None, compute_after=None, compute_done=None,
+                     copy_after=None, copy_done=None):
     """One step from HOST tensors (the end-to-end call).  ``host`` maps names to CPU
     tensors (pinned for asynchronous copies): inputs ``q_idx``, ``w``, ``q_nope``,
     ``q_pe`` (the step's queries) and ``kv_new``, ``k_pe_new``, ``k_idx_new``,
@@ -330,7 +331,10 @@ def dsa_forward_host(host: dict, q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, 
     and the forward reads and writes.  Everything is enqueued on ``stream``; returns
     without synchronising.  ``compute_after`` / ``compute_done`` (torch.cuda.Event):
     the forward waits for the first after the input copies and records the second
-    before the output copies, to chain the forwards of calls on two streams."""
+    before the output copies, to chain the forwards of calls on two streams;
+    ``copy_after`` / ``copy_done``: the input copies wait for the first and the
+    second is recorded once they (and the append kernel) are enqueued, to chain
+    the input copies of calls on two streams."""
     lib = _abi.load()
     p = _problem(q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, W_UK, W_UV, top_k, softmax_scale, idx_fp8, out, lse,
                  idx_out, wo, y, kv_scale)
@@ -342,7 +346,8 @@ def dsa_forward_host(host: dict, q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, 
             if ten.device.type != "cpu" or not ten.is_contiguous():
                 raise ValueError(f"host tensor {name} must be a contiguous CPU tensor")
             setattr(io, name, ten.data_ptr())
-    for name, ev in (("compute_after", compute_after), ("compute_done", compute_done)):
+    for name, ev in (("compute_after", compute_after), ("compute_done", compute_done), ("copy_after", copy_after),
+                     ("copy_done", copy_done)):
         if ev is not None:
             if not ev.cuda_event:  # torch creates the CUDA event on its first record
                 ev.record()

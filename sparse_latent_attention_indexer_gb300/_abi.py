@@ -48,6 +48,7 @@ class dsa_host_io(ctypes.Structure):
         ("kv_scale_new", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("idx", ctypes.c_void_p),
         ("compute_after", ctypes.c_void_p), ("compute_done", ctypes.c_void_p),
+        ("copy_after", ctypes.c_void_p), ("copy_done", ctypes.c_void_p),
     ]
 
 

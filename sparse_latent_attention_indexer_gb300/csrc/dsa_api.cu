@@ -651,6 +651,7 @@ int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_
     // everything the forward would refuse is refused before any copy is enqueued
     if (bt.total_q > 0 && (rc = check_forward(p, bt, workspace, ws_bytes))) return rc;
     cudaError_t e = cudaSuccess;
+    if (io->copy_after) e = cudaStreamWaitEvent(s, (cudaEvent_t)io->copy_after, 0);
     auto put = [&](const void *dev, const void *host, size_t bytes) {
         if (e == cudaSuccess && host && bytes) e = cudaMemcpyAsync((void *)dev, host, bytes, cudaMemcpyHostToDevice, s);
     };
@@ -709,6 +710,7 @@ int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_
             put((const char *)p->kv_scale + r0 * sc_row, (const char *)io->kv_scale_new + done * sc_row, n * sc_row);
         done += n;
     }
+    if (e == cudaSuccess && io->copy_done) e = cudaEventRecord((cudaEvent_t)io->copy_done, s);
     if (e == cudaSuccess && io->compute_after) e = cudaStreamWaitEvent(s, (cudaEvent_t)io->compute_after, 0);
     if (e != cudaSuccess) return fail_cuda(e);
     if ((rc = forward_impl(p, seqs, workspace, ws_bytes, stream))) return rc;

@@ -194,3 +194,35 @@ def test_forward_host_refuses_a_short_workspace_before_copying():
     p = _problem()
     io = _abi.dsa_host_io(q_nope=1 << 16)
     assert lib.dsa_forward_host(ctypes.byref(p), s.ref(), ctypes.byref(io), None, 0, None) == _abi.DSA_ERR_WORKSPACE
+
+
+def test_ctypes_structs_match_the_header_layout(tmp_path):
+    """The binding's ctypes structures have the size and field offsets that a C
+    compiler gives the header's structures (a field added to one side only, or in
+    another order, fails here)."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    structs = [_abi.dsa_seqs, _abi.dsa_problem, _abi.dsa_host_io]
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "dsa.h"', "int main(void) {"]
+    for st in structs:
+        n = st.__name__
+        lines.append(f'    printf("{n} size %zu\\n", sizeof({n}));')
+        for f, _ in st._fields_:
+            lines.append(f'    printf("{n} {f} %zu\\n", offsetof({n}, {f}));')
+    lines += ["    return 0;", "}"]
+    src, exe = tmp_path / "layout.c", tmp_path / "layout"
+    src.write_text("\n".join(lines) + "\n")
+    subprocess.run([gcc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines():
+        n, f, v = line.split()
+        got[(n, f)] = int(v)
+    for st in structs:
+        n = st.__name__
+        assert got[(n, "size")] == ctypes.sizeof(st), n
+        for f, _ in st._fields_:
+            assert got[(n, f)] == getattr(st, f).offset, (n, f)

@@ -86,10 +86,12 @@ def test_forward_from_host_pageable_and_partial_copies():
     assert torch.equal(host["out"], out_r.cpu())
 
 
-def test_two_streams_chained_by_compute_events():
+@pytest.mark.parametrize("chain_copies", [False, True])
+def test_two_streams_chained_by_compute_events(chain_copies):
     """Two calls per slot on two streams, each forward waiting for the previous
-    step's (compute_after / compute_done): every host output still equals the
-    device forward's, bit for bit."""
+    step's (compute_after / compute_done), and with chain_copies each call's input
+    copies waiting for the previous call's (copy_after / copy_done): every host
+    output still equals the device forward's, bit for bit."""
     wl = di.generate("host-io-chain", di.Shape(k=64), 73, [70, 30], [500, 30], [430, 0])
     sh = wl.shape
     ref = H.to_device(wl)
@@ -105,14 +107,16 @@ def test_two_streams_chained_by_compute_events():
                       "l": torch.empty_like(lse_r), "i": torch.empty_like(idx_r),
                       "outs": [torch.empty(out_r.shape, dtype=out_r.dtype).pin_memory() for _ in range(2)]})
     done = [torch.cuda.Event(), torch.cuda.Event()]
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
     for i in range(4):
+        chain = {"copy_done": copied[i % 2], "copy_after": copied[(i + 1) % 2] if i else None} if chain_copies else {}
         sl = slots[i % 2]
         d = sl["dev"]
         dsa.dsa_forward_host(dict(host_in, out=sl["outs"][i // 2]), d["qI"], d["kI"], d["w"], d["q_nope"],
                              d["q_pe"], d["kv_cache"][:, :sh.d_c], d["kv_cache"][:, sh.d_c:], ref["W_UK"],
                              ref["W_UV"], H.seqs_of(wl), sh.k, sh.softmax_scale, out=sl["o"], lse=sl["l"],
                              idx_out=sl["i"], stream=sl["stream"],
-                             compute_done=done[i % 2], compute_after=done[(i + 1) % 2] if i else None)
+                             compute_done=done[i % 2], compute_after=done[(i + 1) % 2] if i else None, **chain)
     torch.cuda.synchronize()
     assert dsa.dsa_check_device_error() == (0, 0)
     for sl in slots:
