@@ -10,8 +10,9 @@ times, roofline, kernel timings and end-to-end figure.
 
 A step is one dsa_forward call (FP8 quantisation when configured, indexer,
 top-k, q~ = q_nope W_UK, sparse latent attention, o_lat W_UV) over the whole
-synthetic batch, inputs resident in HBM.  L2 is flushed (a 256 MiB write)
-between timed steps, outside the timed events.  ``--impl reference`` times the
+synthetic batch, inputs resident in HBM.  L2 is flushed between timed steps,
+outside the timed events: a 256 MiB write, then a 256 MiB read of another
+buffer, so the written lines are written back before the step, not inside it.  ``--impl reference`` times the
 plain CPU oracle instead (a bounded sample of rows per step).
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (the
@@ -427,6 +428,23 @@ def last_rows(wl, n):
     return di.Workload(wl.name + f"-last{t}", wl.shape, wl.seed, [t], [wl.S[b]], [wl.start_pos[b] + wl.T[b] - t], ten)
 
 
+class L2Flush:
+    """Evicts L2 (129 MB) before a timed step: a 256 MiB write, then a 256 MiB
+    read of a second buffer.  The read evicts the write's dirty lines, so their
+    write-back happens here and not inside the step that follows."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
+L2_NOTE = "flushed before every timed step (a 256 MiB write, then a 256 MiB read of another buffer)"
+
+
 def measure_workload(cfg, args, world, rank, local, with_cpu):
     """Times whole dsa_forward steps of workload `cfg`, then its indexer and
     top-k kernels on their own, then the end-to-end step from host buffers."""
@@ -450,14 +468,14 @@ def measure_workload(cfg, args, world, rank, local, with_cpu):
     prob = dsa._problem(t["qI"], t["kI"], t["w"], t["q_nope"], t["q_pe"], ckv, kpe, t["W_UK"], t["W_UV"], sh.k,
                         sh.softmax_scale, sh.idx_fp8, out, lse, idx)
     ws = torch.empty(dsa.dsa_forward_workspace_size(prob, seqs), dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
 
     def step():
         dsa.dsa_forward(t["qI"], t["kI"], t["w"], t["q_nope"], t["q_pe"], ckv, kpe, t["W_UK"], t["W_UV"], seqs, sh.k,
                         sh.softmax_scale, idx_fp8=sh.idx_fp8, out=out, lse=lse, idx_out=idx, workspace=ws)
 
     for _ in range(max(args.warmup, 0)):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
 
@@ -469,7 +487,7 @@ def measure_workload(cfg, args, world, rank, local, with_cpu):
     clocks.start()
     launches = 0
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         dsa.set_stage_events(ev[i])
         step()
         launches += dsa.last_launch_count()
@@ -508,7 +526,7 @@ def measure_workload(cfg, args, world, rank, local, with_cpu):
            "dtype": "bf16" if sh.dtype == "bf16" else "f32",
            "config": {"workload": name, "queries_per_step": M, "keys": wl.total_k, "top_k": sh.k,
                       "indexer": "fp8 e4m3 + ue8m0 block scales" if sh.idx_fp8 else sh.dtype,
-                      "l2": "flushed (256 MiB write) before every timed step",
+                      "l2": L2_NOTE,
                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                       **({"seed": args.seed} if args.seed is not None else {})},
            "roofline": roofline, "stages": stages, "kernels": kernels, "gpu_launches": launches, "clocks": clk,
@@ -544,7 +562,7 @@ def measure_indexer_topk(args, dsa, torch, wl, t, flush, peaks, peak_src):
             (sq, sk, sp), b0, b1 = sub_batch(wl, r0, r1)
             s = dsa.Seqs(sq, sk, sp)
             e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-            flush.zero_()
+            flush()
             e[0].record()
             dsa.dsa_indexer_scores(q[r0:r1], k[cu_k[b0]:cu_k[b1]], t["w"][r0:r1], s,
                                    q_scale=None if qs is None else qs[r0 * sh.H_I:r1 * sh.H_I],
@@ -612,11 +630,11 @@ def run_ours(args, world, rank, local):
 def _time_ms(torch, fn, flush, steps, warmup):
     """Mean CUDA-event time of fn() on the current stream, L2 flushed before each call."""
     for _ in range(max(warmup, 1)):
-        flush.zero_()
+        flush()
         fn()
     times = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
@@ -646,7 +664,7 @@ def measure_next(args, local):
 
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     g = torch.Generator().manual_seed(5)
     res = {}
     T, dim = 4096, 7168
