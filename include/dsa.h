@@ -358,12 +358,16 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
 
 /* The forward from HOST buffers: the end-to-end call of one step.  On `stream`
  * it copies the step's inputs from host memory into the device buffers that
- * `p` names, runs dsa_forward, and copies the results back, in the order
- * listed here: one cudaMemcpyAsync per input and output; the appended cache
- * rows of each array go in one copy to the start of `workspace` and a small
- * kernel puts them in their rows (the workspace is free until the forward
- * starts) -- or, when that staging does not fit the workspace or a row is not
- * a multiple of 16 bytes, one copy per sequence and array.  With
+ * `p` names, runs dsa_forward, and copies the results back: one
+ * cudaMemcpyAsync per input and output; the appended cache rows of each array
+ * go in one copy to the start of `workspace` and a small kernel puts them in
+ * their rows (the workspace is free until the forward starts) -- or, when that
+ * staging does not fit the workspace or a row is not a multiple of 16 bytes,
+ * one copy per sequence and array.  q_nope and q_pe, which only the attention
+ * stage reads, are copied last and on a side stream of the library's (one per
+ * host thread and device, created on first use and kept): their transfer
+ * overlaps the quantiser, indexer and top-k, and the attention stage waits for
+ * it on `stream`.  Everything else is enqueued on `stream`.  With
  * page-locked (pinned) host buffers every copy is asynchronous and the call
  * returns once all the work is enqueued; the caller synchronises `stream`
  * before reading the host outputs.  Pageable host memory also works, but then
@@ -386,8 +390,8 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
  * projected output), lse, idx (requires p->idx_out).
  * Pipelining (all NULL: none), four cudaEvent_t handles: copy_after, which
  * the input copies wait for (cudaStreamWaitEvent before the first of them);
- * copy_done, recorded once the input copies and the append kernel are
- * enqueued; compute_after, which the forward waits for after that; and
+ * copy_done, recorded once the input copies (on both streams) and the append
+ * kernel are enqueued; compute_after, which the forward waits for after that; and
  * compute_done, recorded once the forward's kernels are enqueued, before the
  * output copies.  Calls on two streams with their own device buffers can so
  * chain their forwards (each waits for the previous call's compute_done) while

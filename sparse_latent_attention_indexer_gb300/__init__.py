@@ -328,8 +328,9 @@ def dsa_forward_host(host: dict, q_idx, k_idx, w, q_nope, q_pe, kv_cache, k_pe, 
     ``kv_scale_new`` (the cache rows the step appends: rows start_pos[b] .. S_b - 1
     of every sequence, concatenated), outputs ``out`` (y with wo), ``lse``, ``idx``;
     a missing name is not copied.  The device tensors are the buffers the copies fill
-    and the forward reads and writes.  Everything is enqueued on ``stream``; returns
-    without synchronising.  ``compute_after`` / ``compute_done`` (torch.cuda.Event):
+    and the forward reads and writes.  Everything is enqueued on ``stream``, except the
+    copies of q_nope and q_pe, which run on the library's side stream while the indexer
+    runs (the attention waits for them on ``stream``); returns without synchronising.  ``compute_after`` / ``compute_done`` (torch.cuda.Event):
     the forward waits for the first after the input copies and records the second
     before the output copies, to chain the forwards of calls on two streams;
     ``copy_after`` / ``copy_done``: the input copies wait for the first and the

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <map>
 
 #include "dsa_common.cuh"
 
@@ -16,6 +17,9 @@ thread_local uint32_t g_kernels = 0;
 thread_local int g_launches = 0;
 thread_local cudaEvent_t g_stage_events[DSA_STAGE_EVENTS] = {};
 thread_local bool g_stage_on = false;
+// dsa_forward_host: the event that marks its query copies of q_nope and q_pe done on the side stream;
+// the attention stage waits for it before its first read of them (null: nothing to wait for).
+thread_local cudaEvent_t g_query_in = nullptr;
 
 // Records stage boundary i on `s` when the timing hook is on.
 void stage_mark(int i, cudaStream_t s) {
@@ -158,6 +162,10 @@ int run_mla(const void *q_nope, const void *q_pe, int dtype, const void *kv, int
             const float *kv_scale) {
     const MlaWs L = mla_ws_layout(H, d_c, bt.total_q);
     const int M = bt.total_q;
+    if (g_query_in) {  // q_nope and q_pe are still being copied in on dsa_forward_host's side stream
+        const cudaError_t ew = cudaStreamWaitEvent(s, g_query_in, 0);
+        if (ew != cudaSuccess) return fail_cuda(ew);
+    }
     cudaError_t e;
     const bool fast = !force_generic() && absorb_tc_supported(dtype, H, d_n, d_r, d_c, d_v) && aligned(q_nope, 16) &&
                       aligned(q_pe, 16) && aligned(W_UK, 16) && aligned(W_UV, 16) && aligned(out, 16);
@@ -624,6 +632,49 @@ int forward_impl(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, si
                    true, true, p->wo, p->d_model, p->y, ws + L.obuf, p->kv_fp8 ? p->kv_scale : nullptr);
 }
 
+// dsa_forward_host's side stream, one per host thread and device: the copies of q_nope and q_pe,
+// which only the attention stage reads, run on it while the indexer and top-k run on the caller's
+// stream.  Created on first use and kept for the thread's life; null when it cannot be created
+// (the copies then stay on the caller's stream).
+struct QueryCopyStream {
+    cudaStream_t st = nullptr;
+    cudaEvent_t main_in = nullptr, query_in = nullptr;  // the caller stream's inputs are in; q_nope, q_pe are
+};
+
+QueryCopyStream *query_copy_stream() {
+    thread_local std::map<int, QueryCopyStream> tab;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    QueryCopyStream &q = tab[dev];
+    if (!q.st) {
+        cudaStream_t st = nullptr;
+        cudaEvent_t ev[2] = {nullptr, nullptr};
+        bool ok = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) == cudaSuccess;
+        for (int i = 0; ok && i < 2; ++i) ok = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            for (cudaEvent_t x : ev)
+                if (x) cudaEventDestroy(x);
+            if (st) cudaStreamDestroy(st);
+            cudaGetLastError();
+            return nullptr;
+        }
+        q.st = st;
+        q.main_in = ev[0];
+        q.query_in = ev[1];
+    }
+    return &q;
+}
+
+// Sets the attention stage's wait for the side stream's query copies for one forward, and clears it
+// on every way out.
+struct QueryInScope {
+    explicit QueryInScope(cudaEvent_t ev) { g_query_in = ev; }
+    ~QueryInScope() { g_query_in = nullptr; }
+};
+
 }  // namespace
 }  // namespace dsa
 
@@ -652,13 +703,12 @@ int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_
     if (bt.total_q > 0 && (rc = check_forward(p, bt, workspace, ws_bytes))) return rc;
     cudaError_t e = cudaSuccess;
     if (io->copy_after) e = cudaStreamWaitEvent(s, (cudaEvent_t)io->copy_after, 0);
-    auto put = [&](const void *dev, const void *host, size_t bytes) {
-        if (e == cudaSuccess && host && bytes) e = cudaMemcpyAsync((void *)dev, host, bytes, cudaMemcpyHostToDevice, s);
+    auto put_on = [&](const void *dev, const void *host, size_t bytes, cudaStream_t on) {
+        if (e == cudaSuccess && host && bytes) e = cudaMemcpyAsync((void *)dev, host, bytes, cudaMemcpyHostToDevice, on);
     };
+    auto put = [&](const void *dev, const void *host, size_t bytes) { put_on(dev, host, bytes, s); };
     put(p->q_idx, io->q_idx, T * p->H_I * p->D_I * esz);
     put(p->w, io->w, T * p->H_I * sizeof(float));
-    put(p->q_nope, io->q_nope, T * p->H * p->d_n * esz);
-    put(p->q_pe, io->q_pe, T * p->H * p->d_r * esz);
     // Appended cache rows.  Staged: each array in one copy into the workspace (free until the forward
     // starts), then a kernel puts the rows in place -- a decode batch appends one row per sequence, and
     // a copy per row would cost more than the rows.  Otherwise one copy per sequence and array.
@@ -710,10 +760,26 @@ int dsa_forward_host(const dsa_problem *p, const dsa_seqs *seqs, const dsa_host_
             put((const char *)p->kv_scale + r0 * sc_row, (const char *)io->kv_scale_new + done * sc_row, n * sc_row);
         done += n;
     }
-    if (e == cudaSuccess && io->copy_done) e = cudaEventRecord((cudaEvent_t)io->copy_done, s);
+    // q_nope and q_pe, which only the attention stage reads, go in last and on the side stream: their
+    // transfer overlaps the quantiser, indexer and top-k, which start once the inputs above are in;
+    // the attention stage waits for query_in.
+    QueryCopyStream *qs = (io->q_nope || io->q_pe) && T > 0 && e == cudaSuccess ? query_copy_stream() : nullptr;
+    if (qs) {
+        e = cudaEventRecord(qs->main_in, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(qs->st, qs->main_in, 0);
+    }
+    put_on(p->q_nope, io->q_nope, T * p->H * p->d_n * esz, qs ? qs->st : s);
+    put_on(p->q_pe, io->q_pe, T * p->H * p->d_r * esz, qs ? qs->st : s);
+    if (qs && e == cudaSuccess) e = cudaEventRecord(qs->query_in, qs->st);
+    if (e == cudaSuccess && io->copy_done) e = cudaEventRecord((cudaEvent_t)io->copy_done, qs ? qs->st : s);
     if (e == cudaSuccess && io->compute_after) e = cudaStreamWaitEvent(s, (cudaEvent_t)io->compute_after, 0);
     if (e != cudaSuccess) return fail_cuda(e);
-    if ((rc = forward_impl(p, seqs, workspace, ws_bytes, stream))) return rc;
+    {
+        QueryInScope scope(qs ? qs->query_in : nullptr);
+        if ((rc = forward_impl(p, seqs, workspace, ws_bytes, stream))) return rc;
+    }
+    // Nothing on `s` after this point reads q_nope or q_pe; a later call's copies into them wait for
+    // this call's forward through main_in, recorded on its stream after this forward.
     if (io->compute_done && (e = cudaEventRecord((cudaEvent_t)io->compute_done, s)) != cudaSuccess) return fail_cuda(e);
     auto get = [&](void *host, const void *dev, size_t bytes) {
         if (e == cudaSuccess && host && bytes) e = cudaMemcpyAsync(host, dev, bytes, cudaMemcpyDeviceToHost, s);

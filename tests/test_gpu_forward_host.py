@@ -192,3 +192,51 @@ def test_forward_from_host_with_fp8_latent_cache():
     assert torch.equal(dev["codes"], codes) and torch.equal(dev["kpe"], kpe) and torch.equal(dev["kI"], ref["kI"])
     assert torch.equal(dev["scales"], scales)
     assert torch.equal(host["out"], out_r.cpu())
+
+
+@pytest.mark.parametrize("slots", [1, 2])
+def test_consecutive_calls_with_different_queries(slots):
+    """Three calls in a row without a synchronisation between them, each with its
+    own queries (with two slots: alternating device buffers and streams, forwards
+    and input copies chained).  q_nope and q_pe travel on the library's side
+    stream, and no call may read another call's queries: every host output equals
+    the device forward of its own inputs, bit for bit."""
+    shape = di.Shape(k=64)
+    T, S, P = [50, 1], [400, 300], [350, 299]
+    base = di.generate("host-io-seq-0", shape, 90, T, S, P)
+    sh = base.shape
+    dev0 = H.to_device(base)
+    names = ("qI", "w", "q_nope", "q_pe")
+    queries = [{k: di.generate(f"host-io-seq-{j}", shape, 90 + j, T, S, P).tensors[k] for k in names}
+               for j in range(3)]
+    refs = []
+    for q in queries:
+        t = dict(dev0)
+        t.update({k: v.cuda() for k, v in q.items()})
+        refs.append(H.gpu_forward(base, t)[0])
+    torch.cuda.synchronize()
+    assert not torch.equal(refs[0], refs[1]) and not torch.equal(refs[1], refs[2])
+    host_in = [{"q_idx": q["qI"].pin_memory(), "w": q["w"].pin_memory(), "q_nope": q["q_nope"].pin_memory(),
+                "q_pe": q["q_pe"].pin_memory()} for q in queries]
+    outs = [torch.empty(refs[0].shape, dtype=refs[0].dtype).pin_memory() for _ in range(3)]
+    bufs = [{k: torch.zeros_like(dev0[k]) for k in names} for _ in range(slots)]
+    streams = [torch.cuda.Stream() for _ in range(slots)]
+    dev_out = [torch.empty_like(refs[0]) for _ in range(slots)]
+    lse = [torch.empty((base.total_q, sh.H), dtype=torch.float32, device="cuda") for _ in range(slots)]
+    idx = [torch.empty((base.total_q, sh.k), dtype=torch.int32, device="cuda") for _ in range(slots)]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    for i in range(3):
+        s = i % slots
+        b = bufs[s]
+        chain = {}
+        if slots == 2:
+            chain = {"compute_done": done[i % 2], "compute_after": done[(i + 1) % 2] if i else None,
+                     "copy_done": copied[i % 2], "copy_after": copied[(i + 1) % 2] if i else None}
+        dsa.dsa_forward_host(dict(host_in[i], out=outs[i]), b["qI"], dev0["kI"], b["w"], b["q_nope"], b["q_pe"],
+                             dev0["ckv"], dev0["kpe"], dev0["W_UK"], dev0["W_UV"], H.seqs_of(base), sh.k,
+                             sh.softmax_scale, out=dev_out[s], lse=lse[s], idx_out=idx[s], stream=streams[s], **chain)
+    torch.cuda.synchronize()
+    assert dsa.dsa_check_device_error() == (0, 0)
+    for i in range(3):
+        assert torch.equal(outs[i], refs[i].cpu()), i
