@@ -226,3 +226,34 @@ def test_ctypes_structs_match_the_header_layout(tmp_path):
         assert got[(n, "size")] == ctypes.sizeof(st), n
         for f, _ in st._fields_:
             assert got[(n, f)] == getattr(st, f).offset, (n, f)
+
+
+def test_binding_constants_match_the_header():
+    """The status codes, dtype codes, limits, stage count and kernel bits the
+    binding uses are the values include/dsa.h defines (compiled, not parsed)."""
+    import shutil
+    import subprocess
+    import tempfile
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    header = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    bits = re.findall(r"#define (DSA_KERNEL_[A-Z0-9_]+)\s", header)
+    consts = ["DSA_OK", "DSA_ERR_INVALID_ARG", "DSA_ERR_UNSUPPORTED", "DSA_ERR_CUDA", "DSA_ERR_TIMEOUT",
+              "DSA_ERR_WORKSPACE", "DSA_F32", "DSA_BF16", "DSA_E4M3", "DSA_MAX_SEQS", "DSA_NOALLOC_SCRATCH_BYTES",
+              "DSA_STAGE_EVENTS"] + bits
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "c.c"), os.path.join(d, "c")
+        with open(src, "w") as f:
+            f.write('#include <stdio.h>\n#include "dsa.h"\nint main(void) {\n')
+            for c in consts:
+                f.write(f'    printf("{c} %llu\\n", (unsigned long long)({c}));\n')
+            f.write("    return 0;\n}\n")
+        subprocess.run([gcc, "-std=c11", "-I", os.path.join(ROOT, "include"), src, "-o", exe], check=True)
+        got = dict(line.split() for line in subprocess.run([exe], check=True, capture_output=True,
+                                                           text=True).stdout.splitlines())
+    for c in consts[:12]:
+        assert int(got[c]) == getattr(_abi, c), c
+    named = {f"DSA_KERNEL_{k.upper()}": v for k, v in _abi.KERNEL_BITS.items()}
+    assert {b: int(got[b]) for b in bits} == named
