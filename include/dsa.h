@@ -391,14 +391,14 @@ int dsa_forward(const dsa_problem *p, const dsa_seqs *seqs, void *workspace, siz
  * Pipelining (all NULL: none), four cudaEvent_t handles: copy_after, which
  * the input copies wait for (cudaStreamWaitEvent before the first of them);
  * copy_done, recorded once the input copies (on both streams) and the append
- * kernel are enqueued; compute_after, which the forward waits for after that; and
- * compute_done, recorded once the forward's kernels are enqueued, before the
- * output copies.  Calls on two streams with their own device buffers can so
- * chain their forwards (each waits for the previous call's compute_done) while
- * one call's copies overlap the other's kernels, and chain their input copies
- * (each waits for the previous call's copy_done) so that two calls' inputs do
- * not share the host-to-device bandwidth: the first forward then starts after
- * one call's input copies instead of two.
+ * kernel are enqueued; compute_after, which the forward waits for after that;
+ * and compute_done, recorded once the forward's kernels are enqueued, before
+ * the output copies.  Calls on two streams with their own device buffers can
+ * so chain their forwards (each waits for the previous call's compute_done)
+ * while one call's copies overlap the other's kernels, and chain their input
+ * copies (each waits for the previous call's copy_done) so that two calls'
+ * inputs do not share the host-to-device bandwidth: the first forward then
+ * waits for one call's inputs instead of two calls'.
  * Every check dsa_forward makes runs before the first copy is enqueued, so a
  * refused call changes no device buffer.
  * Returns what dsa_forward returns, DSA_ERR_INVALID_ARG when a sequence has
